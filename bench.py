@@ -1,0 +1,408 @@
+"""Benchmark of the Graft hot path on GB300.
+
+One step = graft_assemble + graft_verify_update (checkpoint / static / tail
+selection, template retrieval, flattening, greedy verification, online top-8
+update) for one batch, on the synthetic static-tree workload at batch 16,
+V = 151936, bf16 logits [16, 61, 151936] (296.6 MB per step).
+
+Timed region: CUDA events on the library's stream around the two graft calls
+of each step; the synthetic target's logits are generated between them
+(untimed) and L2 is flushed (256 MB write) before each graft call, so the
+logits are read from HBM.  ``e2e`` repeats the step through the C ABI from
+pinned HOST buffers (draft inputs and logits copied in, accept lengths and
+emitted tokens copied out) inside the timed region.
+
+``--impl reference`` times the CPU oracle (plain C, one thread) on a bounded
+sample of the same workload.  With several GPUs (torchrun) every rank runs an
+independent replica.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "Graft steps/s (assemble+verify+update) and logits HBM GB/s vs GB300 peak"
+UNIT = "steps/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["graft", "reference"], default="graft")
+    p.add_argument("--workload", type=int, default=2, help="synthetic workload id (0-4); 2 is the headline")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(w: W.Workload, budget_s: float, max_steps: int | None = None, sample_b: int = 2):
+    """Closed-loop oracle decode on the first `sample_b` requests of the
+    workload; only the oracle's assemble/verify/update calls are timed (the
+    synthetic logits are generated outside the timed region).  Returns
+    (steps/s of the full batch, details)."""
+    import oracle
+    ws = w.scaled(B=min(sample_b, w.B))
+    h = W.Harness(ws)
+    P = oracle.make_params(ws.V, budget=ws.budget, mode=ws.mode)
+    C = oracle.new_matrix(ws.V)
+    root, prev, ctx = h.init_state()
+    timed = 0.0
+    steps = 0
+    while (max_steps is None and timed < budget_s) or (max_steps is not None and steps < max_steps):
+        tok, par, aux = h.draft(steps, root, prev)
+        t0 = time.perf_counter()
+        trees = [oracle.assemble(P, root[b], tok[b], aux[b], C, None if par is None else par[b])
+                 for b in range(ws.B)]
+        timed += time.perf_counter() - t0
+        lg = h.tree_logits(np.stack([t.tok for t in trees]), np.stack([t.par for t in trees]).astype(np.int8), ctx,
+                           prev)
+        t0 = time.perf_counter()
+        outs, accs = [], []
+        for b in range(ws.B):
+            a, o, topk = oracle.verify(trees[b], lg[b], ws.dtype)
+            oracle.update(C, trees[b], topk)
+            outs.append(o)
+            accs.append(a)
+        timed += time.perf_counter() - t0
+        h.advance(root, prev, ctx, np.stack(outs), np.array(accs, np.int32))
+        steps += 1
+    per_step_full = (timed / steps) * (w.B / ws.B)
+    return 1.0 / per_step_full, dict(steps=steps, requests=ws.B, timed_s=timed)
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+def measured_peak_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record():
+    """Per-launch DRAM bytes of the scan kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    src = open(os.path.join(ROOT, "hybrid_draft_tree_gb300", "csrc", "scan.cu"), "rb").read()
+    if rec.get("scan_cu_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    return rec
+
+
+def run_graft(args, ws, rank, local):
+    import torch
+    import hybrid_draft_tree_gb300 as g
+    from hybrid_draft_tree_gb300 import _build
+    from workloads.device_loop import DeviceLoop
+
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = W.WORKLOADS[args.workload]
+    if rank:
+        w = w.scaled(seed=w.seed + 1000 * rank)
+    eng = g.Graft(g.graft_default_config(w.V, w.B, w.mode, w.dtype, budget=w.budget, max_draft_nodes=w.draft_nodes))
+    stream = torch.cuda.Stream(dev)
+    loop = DeviceLoop(w, eng, device=dev, stream=stream)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    if w.warm != "none":
+        toks_d, logits_d, _ = loop.warm_inputs_device()
+        eng.warmup(toks_d, logits_d, stream=stream)
+        stream.synchronize()
+        del logits_d, toks_d
+        torch.cuda.empty_cache()
+
+    def one_step(ev=None):
+        loop.draft()
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        if ev:
+            ev[0].record(stream)
+        loop.assemble()
+        n = eng.last_launch_count()
+        if ev:
+            ev[1].record(stream)
+        loop.make_logits()
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        if ev:
+            ev[2].record(stream)
+        loop.verify_update()
+        n += eng.last_launch_count()
+        if ev:
+            ev[3].record(stream)
+        loop.advance(read_back=False)
+        stream.synchronize()                             # the next draft needs the state
+        valid = int((loop.tok >= 0).sum().item())
+        acc = loop.accept_len.cpu().numpy()
+        info = loop.info.cpu().numpy()
+        loop.pull_state()
+        return n, valid, acc, info
+
+    for _ in range(args.warmup):
+        one_step()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches = 0
+    valid_rows = []
+    accs = []
+    events_info = []
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        n, valid, acc, info = one_step(events[k])
+        launches += n
+        valid_rows.append(valid)
+        accs.append(acc)
+        events_info.append(info[:, 0])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    t_asm = [e[0].elapsed_time(e[1]) for e in events]
+    t_ver = [e[2].elapsed_time(e[3]) for e in events]
+    total_ms = sum(t_asm) + sum(t_ver)
+    if ws > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = ws * args.steps / (total_ms / 1e3)
+
+    # roofline of the dominant launch (graft_verify_update: scan + scatter)
+    esize = w.esize
+    algo_bytes = [v * w.V * esize for v in valid_rows]
+    mean_ver_s = statistics.mean(t_ver) / 1e3
+    achieved = statistics.mean(algo_bytes) / mean_ver_s / 1e9
+    peak, peak_kind = measured_peak_gbs()
+    tr = traffic_record()
+    mat = float(np.mean(np.concatenate(accs))) + 1.0
+
+    # e2e through the C ABI from pinned host buffers
+    e2e = run_e2e(args, w, eng, loop, stream, dev)
+
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "vocab": w.V, "batch": w.B, "slots_per_request": w.S,
+                   "mode": ["checkpoint", "static", "tail"][w.mode],
+                   "logits_bytes_per_step": w.logits_bytes_per_step(),
+                   "l2": "flushed (256 MB write) before each graft call; logits 296.6 MB > L2",
+                   "timed": "assemble + verify_update per step (CUDA events on the library stream)",
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": tr["bytes_per_launch"] if tr else None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "graft_verify_update (scan + scatter)",
+                     "algorithmic_bytes_per_launch": round(statistics.mean(algo_bytes)),
+                     "ms_per_launch": round(statistics.mean(t_ver), 5)},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "breakdown_ms": {"assemble": round(statistics.mean(t_asm), 5), "verify_update": round(statistics.mean(t_ver), 5)},
+        "stats": {"mean_accepted_tokens_per_step": round(mat, 4), "valid_rows_per_step": statistics.mean(valid_rows),
+                  "wall_s": round(wall, 2)},
+    }
+    return out
+
+
+def run_e2e(args, w, eng, loop, stream, dev):
+    """Same step through the C ABI with host buffers: the inputs of recorded
+    steps are replayed from pinned memory (H2D inside the timed region), the
+    accept lengths and emitted tokens copied back (D2H inside)."""
+    import torch
+    n_rec = 2
+    B, S, n = w.B, w.S, w.draft_nodes
+    rec = []
+    for _ in range(n_rec):
+        loop.draft()
+        loop.assemble()
+        loop.make_logits()
+        stream.synchronize()
+        rec.append(dict(root=loop.root.cpu().pin_memory(), tok=loop.d_tok.cpu().pin_memory(),
+                        par=loop.d_par.cpu().pin_memory(), aux=loop.d_aux.cpu().pin_memory(),
+                        logits=loop.logits.cpu().pin_memory()))
+        loop.verify_update()
+        loop.advance()
+    d_root = torch.empty(B, dtype=torch.int32, device=dev)
+    d_logits = torch.empty_like(loop.logits)
+    h_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_out = torch.empty((B, S), dtype=torch.int32).pin_memory()
+    h2d = rec[0]["root"].numel() * 4 + rec[0]["tok"].numel() * 4 + rec[0]["aux"].numel() * 4 + \
+        rec[0]["logits"].numel() * rec[0]["logits"].element_size()
+    if w.mode != W.MODE_TAIL:
+        h2d += rec[0]["par"].numel() * 2
+    d2h = B * 4 + B * S * 4
+    steps = max(args.e2e_steps, 1)
+    par = None if w.mode == W.MODE_TAIL else loop.d_par
+
+    def step(r):
+        with torch.cuda.stream(stream):
+            d_root.copy_(r["root"], non_blocking=True)
+            loop.d_tok.copy_(r["tok"], non_blocking=True)
+            if par is not None:
+                loop.d_par.copy_(r["par"], non_blocking=True)
+            loop.d_aux.copy_(r["aux"], non_blocking=True)
+            d_logits.copy_(r["logits"], non_blocking=True)
+        eng.assemble(B, d_root, loop.d_tok, par, loop.d_aux, loop.tok, loop.par, loop.pos, loop.mask, loop.info,
+                     stream=stream)
+        eng.verify_update(B, loop.tok, loop.par, loop.pos, loop.mask, d_logits, loop.accept_len, loop.out_tokens,
+                          stream=stream)
+        with torch.cuda.stream(stream):
+            h_acc.copy_(loop.accept_len, non_blocking=True)
+            h_out.copy_(loop.out_tokens, non_blocking=True)
+
+    for k in range(3):
+        step(rec[k % n_rec])
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        step(rec[k % n_rec])
+    e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(steps / (ms / 1e3), 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch
+        backend = "nccl" if args.impl == "graft" else "gloo"
+        if args.impl == "graft":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # the CPU oracle on a bounded sample: 2 of the batch's requests per step
+        if args.warmup > 0:
+            oracle_sample(w, 0.0, max_steps=args.warmup)
+        v, det = oracle_sample(w, 0.0, max_steps=args.steps)
+        sample = (f"{det['steps']} closed-loop oracle steps on {det['requests']} of {w.B} requests "
+                  f"(assemble+verify+update timed, logits generation excluded); steps/s scaled to the full batch")
+        out = {"metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": round(1e3 / v, 3), "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
+               "data": "synthetic", "impl": "reference",
+               "config": {"workload": w.name, "vocab": w.V, "batch": w.B, "slots_per_request": w.S},
+               "cpu_baseline": {"value": round(v, 5), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                                "cpu": cpu_model()},
+               "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(out))
+        return
+    out = run_graft(args, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and ws == 1:
+            v, det = oracle_sample(w, args.cpu_seconds)
+            out["cpu_baseline"] = {"value": round(v, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                   "sample": f"{det['steps']} closed-loop oracle steps on {det['requests']} of "
+                                             f"{w.B} requests ({det['timed_s']:.1f} s timed; logits generation "
+                                             f"excluded); steps/s scaled to the full batch",
+                                   "cpu": cpu_model()}
+        print(json.dumps(out))
+    if ws > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,356 @@
+// C ABI of libgraft: handle management, argument checking and launches.
+// The method (popular-science article on arXiv 2605.20104, section 二) is
+// described in include/graft.h; the kernels live in assemble.cu and scan.cu.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <queue>
+#include <vector>
+
+#include "graft_internal.cuh"
+
+struct graft_handle {
+  graft_config cfg;
+  int S = 0;
+  int device = 0;
+  int num_sms = 0;
+  int warm_ctas = 0;        // resident CTAs of the warm-up scan
+  int scan_ctas_target = 0; // CTAs wanted per verify launch
+  int32_t* C = nullptr;           // [V][8]
+  int32_t* winner = nullptr;      // [V]
+  int32_t* tpl = nullptr;         // [3][tpl_len]: parent, rank, depth
+  int tpl_len = 0;
+  unsigned long long* part = nullptr;  // [rows][MAX_SPLIT][8]
+  int32_t* row_ticket = nullptr;  // [rows]
+  int32_t* req_ticket = nullptr;  // [max_batch]
+  int32_t* topk = nullptr;        // [rows][8]
+  int32_t* list = nullptr;        // [V] warm-up rows
+  int32_t* count = nullptr;       // [1]
+  uint32_t* err = nullptr;        // [1]
+  int32_t last_launches = 0;
+  char msg[256] = {0};
+};
+
+namespace {
+
+int fail(graft_handle* h, int code, const char* fmt, ...) {
+  if (h) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(h->msg, sizeof h->msg, fmt, ap);
+    va_end(ap);
+  }
+  return code;
+}
+
+int cuda_fail(graft_handle* h, cudaError_t e, const char* what) {
+  return fail(h, GRAFT_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Retrieval template (article §二, second gear): rank paths below the anchor;
+// the rank-r successor of a node has max(1, width >> r) children, the anchor
+// `width`; depth <= max_depth.  Entries are emitted in increasing
+// (rank sum, depth, rank path) order by best-first expansion: a child's key
+// is never smaller than its parent's, so popping the smallest key from a
+// frontier seeded with the anchor's children yields the global order.
+struct TplNode {
+  int sum, depth;
+  std::vector<int> path;
+  int index;  // emitted index, set when popped
+};
+struct TplCmp {
+  bool operator()(const TplNode& a, const TplNode& b) const {  // "a after b"
+    if (a.sum != b.sum) return a.sum > b.sum;
+    if (a.depth != b.depth) return a.depth > b.depth;
+    return a.path > b.path;
+  }
+};
+
+void build_template(int max_depth, int width, int len, std::vector<int32_t>& parent, std::vector<int32_t>& rank,
+                    std::vector<int32_t>& depth) {
+  std::priority_queue<TplNode, std::vector<TplNode>, TplCmp> frontier;
+  struct Parented { TplNode node; int parent_index; };
+  // frontier entries carry their parent's emitted index in `index`
+  for (int r = 0; r < width && r < graft::K; ++r) frontier.push(TplNode{r, 1, {r}, -1});
+  while ((int)parent.size() < len && !frontier.empty()) {
+    TplNode nd = frontier.top();
+    frontier.pop();
+    const int me = (int)parent.size();
+    parent.push_back(nd.index);
+    rank.push_back(nd.path.back());
+    depth.push_back(nd.depth);
+    if (nd.depth < max_depth) {
+      int fan = width >> nd.path.back();
+      if (fan < 1) fan = 1;
+      for (int r = 0; r < fan && r < graft::K; ++r) {
+        TplNode c{nd.sum + r, nd.depth + 1, nd.path, me};
+        c.path.push_back(r);
+        frontier.push(c);
+      }
+    }
+  }
+}
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t n) {
+  return cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T) + 16);
+}
+
+void free_all(graft_handle* h) {
+  cudaFree(h->C); cudaFree(h->winner); cudaFree(h->tpl); cudaFree(h->part);
+  cudaFree(h->row_ticket); cudaFree(h->req_ticket); cudaFree(h->topk);
+  cudaFree(h->list); cudaFree(h->count); cudaFree(h->err);
+}
+
+int check_cfg(const graft_config* c, graft_handle* h) {
+  if (c->vocab < 1) return fail(h, GRAFT_EINVAL, "vocab must be >= 1");
+  if (c->topk != graft::K) return fail(h, GRAFT_EINVAL, "topk must be 8");
+  if (c->budget < 1 || c->budget + 1 > graft::MAX_S) return fail(h, GRAFT_EINVAL, "budget must be in [1, 63]");
+  if (c->max_batch < 1 || (int64_t)c->max_batch * (c->budget + 1) > 65535)
+    return fail(h, GRAFT_EINVAL, "max_batch * (budget + 1) must be in [1, 65535]");
+  if (c->mode < GRAFT_MODE_CHECKPOINT || c->mode > GRAFT_MODE_TAIL) return fail(h, GRAFT_EINVAL, "bad mode");
+  if (c->logits_dtype != GRAFT_F32 && c->logits_dtype != GRAFT_BF16) return fail(h, GRAFT_EINVAL, "bad logits dtype");
+  for (int k = 0; k < 3; ++k)
+    if (c->ckpt_draft[k] < 0 || c->ckpt_draft[k] > c->budget || c->ckpt_depth[k] < 0)
+      return fail(h, GRAFT_EINVAL, "checkpoint %d: draft slots must be in [0, budget], depth >= 0", k);
+  if (c->tpl_depth < 1 || c->tpl_depth > 16 || c->tpl_width < 1 || c->tpl_width > graft::K)
+    return fail(h, GRAFT_EINVAL, "template depth must be in [1, 16] and width in [1, 8]");
+  const int maxn = c->mode == GRAFT_MODE_TAIL ? c->budget : graft::MAX_DRAFT;
+  if (c->max_draft_nodes < 0 || c->max_draft_nodes > maxn)
+    return fail(h, GRAFT_EINVAL, "max_draft_nodes must be in [0, %d]", maxn);
+  return GRAFT_OK;
+}
+
+// Geometry of a row scan: 16-byte vector loads when every row start is
+// 16-byte aligned, scalar loads otherwise; `ctas_wanted` CTAs in total.
+graft::ScanGeom scan_geom(const graft_handle* h, const void* logits, int64_t stride, int64_t rows,
+                          int ctas_wanted) {
+  graft::ScanGeom g{};
+  const int es = h->cfg.logits_dtype == GRAFT_BF16 ? 2 : 4;
+  g.V = h->cfg.vocab;
+  g.stride = stride;
+  g.vec = ((reinterpret_cast<uintptr_t>(logits) & 15) == 0) && ((stride * es) % 16 == 0);
+  g.epl = g.vec ? 16 / es : 1;
+  g.nslot = g.V / g.epl;
+  g.tail = (int32_t)(g.V - g.nslot * g.epl);
+  int64_t nsplit = rows > 0 ? (ctas_wanted + rows - 1) / rows : 1;
+  const int64_t by_size = (g.nslot + 1023) / 1024;  // at least ~1024 slots per CTA
+  if (nsplit > by_size) nsplit = by_size;
+  if (nsplit > graft::MAX_SPLIT) nsplit = graft::MAX_SPLIT;
+  if (nsplit < 1) nsplit = 1;
+  g.nsplit = (int32_t)nsplit;
+  g.per_cta = (g.nslot + nsplit - 1) / nsplit;
+  return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+void graft_default_config(graft_config* c, int32_t vocab, int32_t max_batch, int32_t mode, int32_t dtype) {
+  std::memset(c, 0, sizeof *c);
+  c->vocab = vocab;
+  c->topk = graft::K;
+  c->budget = mode == GRAFT_MODE_TAIL ? 16 : 60;
+  c->max_batch = max_batch;
+  c->mode = mode;
+  c->logits_dtype = dtype;
+  c->ckpt_depth[0] = 0; c->ckpt_depth[1] = 1; c->ckpt_depth[2] = 5;
+  c->ckpt_thr[0] = 0.30f; c->ckpt_thr[1] = 0.20f; c->ckpt_thr[2] = 0.10f;
+  c->ckpt_draft[0] = 8; c->ckpt_draft[1] = 24; c->ckpt_draft[2] = 40;
+  c->tpl_depth = 8;
+  c->tpl_width = 8;
+  c->static_thr = 0.15f;
+  c->tail_thr = 0.4f;
+  c->max_draft_nodes = mode == GRAFT_MODE_TAIL ? 16 : 184;
+}
+
+int graft_init(const graft_config* cfg, graft_handle** out) {
+  if (!cfg || !out) return GRAFT_EINVAL;
+  *out = nullptr;
+  graft_handle* h = new (std::nothrow) graft_handle();
+  if (!h) return GRAFT_ENOMEM;
+  int rc = check_cfg(cfg, h);
+  if (rc) { delete h; return rc; }
+  h->cfg = *cfg;
+  h->S = cfg->budget + 1;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) { delete h; return GRAFT_ECUDA; }
+
+  std::vector<int32_t> tp, tr, td;
+  build_template(cfg->tpl_depth, cfg->tpl_width, cfg->budget, tp, tr, td);
+  h->tpl_len = (int)tp.size();
+
+  const size_t V = (size_t)cfg->vocab;
+  const size_t rows = (size_t)cfg->max_batch * h->S;
+  e = dalloc(&h->C, V * graft::K);
+  if (e == cudaSuccess) e = dalloc(&h->winner, V);
+  if (e == cudaSuccess) e = dalloc(&h->tpl, 3 * (size_t)(h->tpl_len > 0 ? h->tpl_len : 1));
+  if (e == cudaSuccess) e = dalloc(&h->part, rows * graft::MAX_SPLIT * graft::K);
+  if (e == cudaSuccess) e = dalloc(&h->row_ticket, rows);
+  if (e == cudaSuccess) e = dalloc(&h->req_ticket, (size_t)cfg->max_batch);
+  if (e == cudaSuccess) e = dalloc(&h->topk, rows * graft::K);
+  if (e == cudaSuccess) e = dalloc(&h->list, V);
+  if (e == cudaSuccess) e = dalloc(&h->count, 1);
+  if (e == cudaSuccess) e = dalloc(&h->err, 1);
+  if (e != cudaSuccess) { free_all(h); delete h; return GRAFT_ENOMEM; }
+
+  e = cudaMemset(h->C, 0xFF, V * graft::K * sizeof(int32_t));  // -1 = empty
+  if (e == cudaSuccess) e = cudaMemset(h->winner, 0, V * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->row_ticket, 0, rows * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->req_ticket, 0, cfg->max_batch * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->count, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(uint32_t));
+  if (e == cudaSuccess && h->tpl_len > 0) {
+    std::vector<int32_t> all(tp);
+    all.insert(all.end(), tr.begin(), tr.end());
+    all.insert(all.end(), td.begin(), td.end());
+    e = cudaMemcpy(h->tpl, all.data(), all.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) { free_all(h); delete h; return GRAFT_ECUDA; }
+  h->warm_ctas = h->num_sms * 4;
+  h->scan_ctas_target = h->num_sms * 8;
+  *out = h;
+  return GRAFT_OK;
+}
+
+int graft_destroy(graft_handle* h) {
+  if (!h) return GRAFT_EINVAL;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+  return GRAFT_OK;
+}
+
+int graft_warmup(graft_handle* h, const int32_t* d_tokens, const void* d_logits, int64_t n_rows, int64_t row_stride,
+                 void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  h->last_launches = 0;
+  if (n_rows < 0 || n_rows >= 0x7FFFFFFF) return fail(h, GRAFT_EINVAL, "n_rows must be in [0, 2^31-1)");
+  if (n_rows == 0) return GRAFT_OK;
+  if (!d_tokens || !d_logits) return fail(h, GRAFT_EINVAL, "null pointer");
+  if (row_stride < h->cfg.vocab) return fail(h, GRAFT_EINVAL, "row_stride < vocab");
+  graft::WarmArgs a{};
+  a.g = scan_geom(h, d_logits, row_stride, n_rows, 0);
+  a.g.nsplit = 1;
+  a.g.per_cta = a.g.nslot;
+  a.n_rows = n_rows;
+  a.logits = d_logits;
+  a.tokens = d_tokens;
+  a.winner = h->winner;
+  a.list = h->list;
+  a.count = h->count;
+  a.C = h->C;
+  a.err = h->err;
+  cudaError_t e = graft::launch_warmup(a, h->cfg.logits_dtype, h->warm_ctas, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_warmup launch");
+  h->last_launches = 4;
+  return GRAFT_OK;
+}
+
+int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                   const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes, int32_t* d_tree_tok,
+                   int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info, void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  h->last_launches = 0;
+  const graft_config& c = h->cfg;
+  if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
+  if (draft_nodes < 0 || draft_nodes > c.max_draft_nodes)
+    return fail(h, GRAFT_EINVAL, "draft_nodes %d outside [0, %d]", draft_nodes, c.max_draft_nodes);
+  if (batch == 0) return GRAFT_OK;
+  if (!d_root_tok || !d_tree_tok || !d_tree_parent || !d_tree_pos || !d_tree_mask || !d_info)
+    return fail(h, GRAFT_EINVAL, "null pointer");
+  if (draft_nodes > 0 && (!d_draft_tok || !d_draft_aux || (c.mode != GRAFT_MODE_TAIL && !d_draft_parent)))
+    return fail(h, GRAFT_EINVAL, "null draft pointer");
+  graft::AssembleArgs a{};
+  a.mode = c.mode; a.V = c.vocab; a.budget = c.budget; a.S = h->S; a.n = draft_nodes; a.batch = batch;
+  for (int k = 0; k < 3; ++k) {
+    a.ckpt_depth[k] = c.ckpt_depth[k];
+    a.ckpt_thr[k] = c.ckpt_thr[k];
+    a.ckpt_draft[k] = c.ckpt_draft[k];
+  }
+  a.static_thr = c.static_thr;
+  a.tail_thr = c.tail_thr;
+  a.root_tok = d_root_tok; a.draft_tok = d_draft_tok; a.draft_parent = d_draft_parent; a.draft_aux = d_draft_aux;
+  a.C = h->C;
+  a.tpl.parent = h->tpl;
+  a.tpl.rank = h->tpl + h->tpl_len;
+  a.tpl.depth = h->tpl + 2 * h->tpl_len;
+  a.tpl.len = h->tpl_len;
+  a.tree_tok = d_tree_tok; a.tree_parent = d_tree_parent; a.tree_pos = d_tree_pos; a.tree_mask = d_tree_mask;
+  a.info = d_info;
+  a.err = h->err;
+  cudaError_t e = graft::launch_assemble(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_assemble launch");
+  h->last_launches = 1;
+  return GRAFT_OK;
+}
+
+int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
+                        const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
+                        int64_t row_stride, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  h->last_launches = 0;
+  const graft_config& c = h->cfg;
+  if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
+  if (batch == 0) return GRAFT_OK;
+  if (!d_tree_tok || !d_tree_parent || !d_tree_pos || !d_tree_mask || !d_logits || !d_accept_len || !d_out_tokens)
+    return fail(h, GRAFT_EINVAL, "null pointer");
+  if (row_stride < c.vocab) return fail(h, GRAFT_EINVAL, "row_stride < vocab");
+  const int64_t rows = (int64_t)batch * h->S;
+  graft::VerifyArgs a{};
+  a.g = scan_geom(h, d_logits, row_stride, rows, h->scan_ctas_target);
+  a.S = h->S; a.batch = batch; a.logits = d_logits;
+  a.tree_tok = d_tree_tok; a.tree_parent = d_tree_parent; a.tree_pos = d_tree_pos; a.tree_mask = d_tree_mask;
+  a.accept_len = d_accept_len; a.out_tokens = d_out_tokens;
+  a.part = h->part; a.row_ticket = h->row_ticket; a.req_ticket = h->req_ticket; a.topk = h->topk;
+  a.winner = h->winner; a.err = h->err;
+  cudaError_t e = graft::launch_verify(a, c.logits_dtype, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update scan launch");
+  graft::ScatterArgs x{};
+  x.rows = (int32_t)rows; x.V = c.vocab; x.tree_tok = d_tree_tok; x.topk = h->topk; x.winner = h->winner; x.C = h->C;
+  e = graft::launch_scatter(x, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update scatter launch");
+  h->last_launches = 2;
+  return GRAFT_OK;
+}
+
+int graft_get_matrix(graft_handle* h, int32_t* host_out, void* stream) {
+  if (!h || !host_out) return fail(h, GRAFT_EINVAL, "null pointer");
+  const size_t bytes = (size_t)h->cfg.vocab * graft::K * sizeof(int32_t);
+  cudaError_t e = cudaMemcpyAsync(host_out, h->C, bytes, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  return e == cudaSuccess ? GRAFT_OK : cuda_fail(h, e, "graft_get_matrix");
+}
+
+int graft_set_matrix(graft_handle* h, const int32_t* host_in, void* stream) {
+  if (!h || !host_in) return fail(h, GRAFT_EINVAL, "null pointer");
+  const size_t bytes = (size_t)h->cfg.vocab * graft::K * sizeof(int32_t);
+  cudaError_t e = cudaMemcpyAsync(h->C, host_in, bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  return e == cudaSuccess ? GRAFT_OK : cuda_fail(h, e, "graft_set_matrix");
+}
+
+int32_t* graft_matrix_device_ptr(graft_handle* h) { return h ? h->C : nullptr; }
+
+int graft_sync(graft_handle* h, void* stream, uint32_t* out_flags) {
+  if (!h) return GRAFT_EINVAL;
+  uint32_t flags = 0;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaMemcpy(&flags, h->err, sizeof flags, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && flags) e = cudaMemset(h->err, 0, sizeof(uint32_t));
+  if (out_flags) *out_flags = flags;
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_sync");
+  if (flags) return fail(h, GRAFT_EDEVICE, "device error flags 0x%x (token %d, nan %d, tree %d)", flags,
+                         !!(flags & GRAFT_ERR_TOKEN), !!(flags & GRAFT_ERR_NAN), !!(flags & GRAFT_ERR_TREE));
+  return GRAFT_OK;
+}
+
+const char* graft_last_error(const graft_handle* h) { return h ? h->msg : "null handle"; }
+
+int32_t graft_last_launch_count(const graft_handle* h) { return h ? h->last_launches : 0; }
+
+}  // extern "C"

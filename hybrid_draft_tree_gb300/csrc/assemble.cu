@@ -1,0 +1,284 @@
+// graft_assemble's kernel: steps 1-3 of a Graft decode step for one request
+// per CTA (popular-science article on arXiv 2605.20104, section 二 gears 1-2
+// and the flatten of gear 3; section 四 static trees; section 七 Graft-TAIL).
+//
+// Work per request is a few KB, so the kernel is latency-bound: everything
+// lives in shared memory, one thread per draft node / template entry / slot,
+// and the only global traffic is the draft input, at most `budget` 32-byte
+// matrix rows gathered for retrieval, and the flattened tree written out.
+#include <climits>
+
+#include "graft_internal.cuh"
+
+namespace graft {
+namespace {
+
+constexpr int AT = 256;  // threads per CTA (>= MAX_DRAFT, >= MAX_S)
+
+__device__ __forceinline__ void raise_err(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
+
+// Block-wide exclusive prefix count of a predicate.  All threads must call.
+__device__ __forceinline__ int block_excl_count(bool v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned m = __ballot_sync(0xffffffffu, v);
+  const int pre = __popc(m & ((1u << lane) - 1u));
+  if (lane == 0) s_warp[warp] = __popc(m);
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < AT / 32; ++w) {
+    const int c = s_warp[w];
+    base += (w < warp) ? c : 0;
+    tot += c;
+  }
+  __syncthreads();
+  total = tot;
+  return base + pre;
+}
+
+__global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
+  const int b = blockIdx.x;
+  const int t = threadIdx.x;
+  const int n = a.n;
+  const int S = a.S;
+
+  __shared__ int32_t s_tok[MAX_DRAFT];
+  __shared__ int32_t s_par[MAX_DRAFT];
+  __shared__ float s_conf[MAX_DRAFT];
+  __shared__ int32_t s_depth[MAX_DRAFT];
+  __shared__ int32_t s_slot[MAX_DRAFT];
+  __shared__ int32_t s_rtok[MAX_S];
+  __shared__ int32_t s_rslot[MAX_S];
+  __shared__ int32_t o_tok[MAX_S];
+  __shared__ int32_t o_par[MAX_S];
+  __shared__ int32_t o_pos[MAX_S];
+  __shared__ int32_t o_rep[MAX_S];
+  __shared__ int s_warp[AT / 32];
+  __shared__ int s_bad, s_best[3], s_tcut, s_maxdepth;
+
+  if (t == 0) { s_bad = 0; s_tcut = n; s_maxdepth = 0; }
+  if (t < 3) s_best[t] = -1;
+  if (t < MAX_S) { o_tok[t] = -1; o_par[t] = -1; o_pos[t] = -1; o_rep[t] = 0; s_rtok[t] = -1; s_rslot[t] = -1; }
+  __syncthreads();
+
+  // ---- load and validate -------------------------------------------------
+  const int32_t root = a.root_tok[b];
+  float prob = 0.f;
+  if (t < n) {
+    const int64_t k = (int64_t)b * n + t;
+    const int32_t tk = a.draft_tok[k];
+    s_tok[t] = tk;
+    if (tk < 0 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); s_bad = 1; }
+    prob = a.draft_aux[k];
+    if (a.mode != GRAFT_MODE_TAIL) {
+      const int p = a.draft_parent[k];
+      s_par[t] = p;
+      if (p < -1 || p >= t) { raise_err(a.err, GRAFT_ERR_TREE); s_bad = 1; }
+      if (!(prob >= 0.f && prob <= 1.f)) { raise_err(a.err, GRAFT_ERR_NAN); s_bad = 1; }
+    } else {
+      s_par[t] = t - 1;
+      if (prob != prob) { raise_err(a.err, GRAFT_ERR_NAN); s_bad = 1; }
+    }
+    s_depth[t] = -1;
+  }
+  const bool root_ok = root >= 0 && root < a.V;
+  if (t == 0 && !root_ok) raise_err(a.err, GRAFT_ERR_TOKEN);
+  __syncthreads();
+  const bool bad = s_bad != 0 || !root_ok;
+  const int nn = bad ? 0 : n;   // a request with bad input degrades to its root only
+
+  int n_draft = 0, n_retr = 0, event = -1;
+  int R = 0, anchor_slot = 0, anchor_pos = 0, rbase = 1;
+  int32_t anchor_tok = root;
+
+  if (a.mode != GRAFT_MODE_TAIL) {
+    // ---- path confidence, root to leaf, one layer per pass (gear 1) -------
+    int my_depth = -1;
+    for (int pass = 0; pass <= nn; ++pass) {
+      float nc = 0.f;
+      int nd = -1;
+      if (t < nn && my_depth < 0) {
+        const int p = s_par[t];
+        if (p < 0) { nc = prob; nd = 0; }
+        else {
+          const int dp = s_depth[p];
+          if (dp >= 0) { nc = __fmul_rn(s_conf[p], prob); nd = dp + 1; }
+        }
+      }
+      __syncthreads();
+      if (nd >= 0) { s_conf[t] = nc; s_depth[t] = nd; my_depth = nd; }
+      if (!__syncthreads_or(t < nn && my_depth < 0)) break;
+    }
+    if (t < nn) atomicMax(&s_maxdepth, my_depth);
+
+    // ---- checkpoints: best path confidence of layers 0, 1, 5 ---------------
+    int D = a.budget, cut = INT_MAX;
+    if (a.mode == GRAFT_MODE_CHECKPOINT) {
+      if (t < nn) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          if (my_depth == a.ckpt_depth[k]) atomicMax(&s_best[k], __float_as_int(s_conf[t]));  // conf >= 0
+      }
+      __syncthreads();
+      for (int k = 0; k < 3; ++k) {
+        const int bi = s_best[k];
+        if (bi >= 0 && __int_as_float(bi) < a.ckpt_thr[k]) {
+          event = a.ckpt_depth[k];
+          D = min(max(a.ckpt_draft[k], 0), a.budget);
+          R = a.budget - D;
+          cut = a.ckpt_depth[k];
+          break;
+        }
+      }
+    }
+
+    // ---- keep the top-D candidates by (confidence desc, index asc) --------
+    bool keep = false;
+    if (t < nn && my_depth <= cut) {
+      const float c = s_conf[t];
+      int r = 0;
+      for (int j = 0; j < nn; ++j) {
+        const float cj = s_conf[j];
+        r += (s_depth[j] <= cut) && (cj > c || (cj == c && j < t));
+      }
+      keep = r < D;
+    }
+    const int pre = block_excl_count(keep, s_warp, n_draft);
+    if (t < MAX_DRAFT) s_slot[t] = keep ? 1 + pre : -1;
+    __syncthreads();
+    if (keep) {
+      const int s = 1 + pre;
+      const int p = s_par[t];
+      int ps = 0;
+      if (p >= 0) {
+        ps = s_slot[p];
+        if (ps < 0) { raise_err(a.err, GRAFT_ERR_TREE); ps = 0; }   // cannot happen for probabilities <= 1
+      }
+      o_tok[s] = s_tok[t];
+      o_par[s] = ps;
+      o_pos[s] = my_depth + 1;
+      o_rep[s] = (a.mode == GRAFT_MODE_STATIC) && (s_conf[t] < a.static_thr);
+    }
+    if (t == 0) { o_tok[0] = root_ok ? root : -1; o_par[0] = -1; o_pos[0] = root_ok ? 0 : -1; }
+    __syncthreads();
+    rbase = 1 + n_draft;
+
+    if (a.mode == GRAFT_MODE_STATIC) {
+      // ---- in-place replacement, parents before children (section 四) -----
+      const int used = 1 + n_draft;
+      const int maxpos = s_maxdepth + 1;
+      int nrep_local = (t >= 1 && t < used) ? o_rep[t] : 0;
+      for (int level = 1; level <= maxpos; ++level) {
+        if (t >= 1 && t < used && o_pos[t] == level) {
+          const int p = o_par[t];
+          const int32_t ptok = o_tok[p];
+          if (ptok < 0) {
+            o_tok[t] = -1;
+          } else if (o_rep[t]) {
+            int srank = 0;
+            for (int q = 1; q < t; ++q) srank += (o_par[q] == p) && o_rep[q];
+            int32_t tk = -1;
+            if (srank < K) {
+              tk = a.C[(int64_t)ptok * K + srank];
+              if (tk < -1 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); tk = -1; }
+            }
+            o_tok[t] = tk;
+          }
+        }
+        __syncthreads();
+      }
+      const bool kept_draft = t >= 1 && t < used && !o_rep[t] && o_tok[t] >= 0;
+      const bool realised = t >= 1 && t < used && o_rep[t] && o_tok[t] >= 0;
+      block_excl_count(kept_draft, s_warp, n_draft);
+      block_excl_count(realised, s_warp, n_retr);
+      event = __syncthreads_count(nrep_local != 0);
+    }
+  } else {
+    // ---- tail mode: keep the confident prefix as a chain (section 七) -------
+    if (t < nn && prob < a.tail_thr) atomicMin(&s_tcut, t);
+    __syncthreads();
+    const int tc = bad ? 0 : min(s_tcut, nn);
+    if (t >= 1 && t <= tc) { o_tok[t] = s_tok[t - 1]; o_par[t] = t - 1; o_pos[t] = t; }
+    if (t == 0) { o_tok[0] = root_ok ? root : -1; o_par[0] = -1; o_pos[0] = root_ok ? 0 : -1; }
+    event = tc;
+    n_draft = tc;
+    R = bad ? 0 : a.budget - tc;
+    anchor_slot = tc;
+    anchor_pos = tc;
+    anchor_tok = (tc == 0) ? root : s_tok[tc - 1];
+    rbase = 1 + tc;
+    __syncthreads();
+  }
+
+  if (a.mode != GRAFT_MODE_STATIC) {
+    // ---- retrieval subtree: a pure gather along the template (gear 2) -----
+    R = min(R, a.tpl.len);
+    const int j = t;
+    const bool mine = j < R;
+    const int jd = mine ? a.tpl.depth[j] : 0;
+    const int jq = mine ? a.tpl.parent[j] : -1;
+    const int jr = mine ? a.tpl.rank[j] : 0;
+    int maxd = 0;
+    for (int q = 0; q < R; ++q) maxd = max(maxd, a.tpl.depth[q]);
+    for (int level = 1; level <= maxd; ++level) {
+      if (mine && jd == level) {
+        const int32_t ptok = (jq < 0) ? anchor_tok : s_rtok[jq];
+        int32_t tk = -1;
+        if (ptok >= 0 && ptok < a.V) {
+          tk = a.C[(int64_t)ptok * K + jr];
+          if (tk < -1 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); tk = -1; }
+        }
+        s_rtok[j] = tk;
+      }
+      __syncthreads();
+    }
+    const bool realised = mine && s_rtok[j] >= 0;
+    const int pre = block_excl_count(realised, s_warp, n_retr);
+    if (realised) s_rslot[j] = rbase + pre;
+    __syncthreads();
+    if (realised) {
+      const int s = rbase + pre;
+      o_tok[s] = s_rtok[j];
+      o_par[s] = (jq < 0) ? anchor_slot : s_rslot[jq];
+      o_pos[s] = anchor_pos + jd;
+    }
+    __syncthreads();
+  }
+
+  // ---- positions are set; ancestor masks by walking parents (gear 3) ------
+  if (t < S) {
+    const int64_t k = (int64_t)b * S + t;
+    const int32_t tk = o_tok[t];
+    if (tk >= 0) {
+      uint64_t m = 1ull << t;
+      int p = o_par[t];
+      for (int steps = 0; p >= 0 && steps < MAX_S; ++steps) { m |= 1ull << p; p = o_par[p]; }
+      a.tree_tok[k] = tk;
+      a.tree_parent[k] = (int8_t)o_par[t];
+      a.tree_pos[k] = o_pos[t];
+      a.tree_mask[k] = m;
+    } else {
+      a.tree_tok[k] = -1;
+      a.tree_parent[k] = -1;
+      a.tree_pos[k] = -1;
+      a.tree_mask[k] = 0ull;
+    }
+  }
+  const int valid = __syncthreads_count(t < S && o_tok[t] >= 0);
+  if (t == 0) {
+    int32_t* info = a.info + (int64_t)b * 4;
+    info[0] = event;
+    info[1] = n_draft;
+    info[2] = n_retr;
+    info[3] = valid;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s) {
+  k_assemble<<<a.batch, AT, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace graft

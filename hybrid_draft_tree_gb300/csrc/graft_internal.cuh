@@ -1,0 +1,98 @@
+// Internal declarations shared by the CUDA translation units of libgraft.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "graft.h"
+
+namespace graft {
+
+constexpr int K = 8;            // successors per continuation-matrix row
+constexpr int MAX_S = 64;       // slots per request (one uint64 mask row)
+constexpr int MAX_DRAFT = 256;  // draft nodes per request in one assemble CTA
+constexpr int MAX_SPLIT = 16;   // CTAs per logits row in the verify scan
+
+// Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth.
+struct TemplateDev {
+  const int32_t* parent;
+  const int32_t* rank;
+  const int32_t* depth;
+  int32_t len;
+};
+
+struct AssembleArgs {
+  int32_t mode, V, budget, S, n, batch;
+  int32_t ckpt_depth[3];
+  float ckpt_thr[3];
+  int32_t ckpt_draft[3];
+  float static_thr, tail_thr;
+  const int32_t* root_tok;
+  const int32_t* draft_tok;
+  const int16_t* draft_parent;
+  const float* draft_aux;
+  const int32_t* C;
+  TemplateDev tpl;
+  int32_t* tree_tok;
+  int8_t* tree_parent;
+  int32_t* tree_pos;
+  uint64_t* tree_mask;
+  int32_t* info;
+  uint32_t* err;
+};
+
+struct ScanGeom {
+  int32_t V;          // elements per row
+  int64_t stride;     // elements between row starts
+  int32_t vec;        // 1 = 16-byte vector loads, 0 = scalar loads
+  int32_t epl;        // elements per load slot (8 bf16 / 4 f32 when vec, else 1)
+  int64_t nslot;      // load slots per row (full vectors only when vec)
+  int32_t tail;       // elements after the last full vector (vec only)
+  int32_t nsplit;     // CTAs per row
+  int64_t per_cta;    // load slots per CTA
+};
+
+struct VerifyArgs {
+  ScanGeom g;
+  int32_t S, batch;
+  const void* logits;
+  const int32_t* tree_tok;
+  const int8_t* tree_parent;
+  const int32_t* tree_pos;
+  const uint64_t* tree_mask;
+  int32_t* accept_len;
+  int32_t* out_tokens;
+  unsigned long long* part;   // [rows][MAX_SPLIT][K] partial top-8 keys
+  int32_t* row_ticket;        // [rows]
+  int32_t* req_ticket;        // [batch]
+  int32_t* topk;              // [rows][K] staged top-8 ids
+  int32_t* winner;            // [V] last-writer key (row + 1), 0 = none
+  uint32_t* err;
+};
+
+struct ScatterArgs {
+  int32_t rows, V;
+  const int32_t* tree_tok;
+  const int32_t* topk;
+  int32_t* winner;
+  int32_t* C;
+};
+
+struct WarmArgs {
+  ScanGeom g;
+  int64_t n_rows;
+  const void* logits;
+  const int32_t* tokens;
+  int32_t* winner;
+  int32_t* list;
+  int32_t* count;
+  int32_t* C;
+  uint32_t* err;
+};
+
+// launchers (return cudaGetLastError())
+cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s);
+cudaError_t launch_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
+cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s);
+
+}  // namespace graft

@@ -1,0 +1,201 @@
+"""Python binding of libgraft (the C ABI declared in include/graft.h).
+
+Argument marshalling only: every step of the Graft hot path runs in the CUDA
+kernels of libgraft.so.  Device buffers are torch CUDA tensors (their
+data_ptr is passed through); the stream is torch's current stream unless one
+is given.  There is no CPU fallback: if the library is missing or no CUDA
+device is present, these calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+GRAFT_OK, GRAFT_EINVAL, GRAFT_ENOMEM, GRAFT_ECUDA, GRAFT_EDEVICE = 0, -1, -2, -3, -4
+GRAFT_ERR_TOKEN, GRAFT_ERR_NAN, GRAFT_ERR_TREE = 1, 2, 4
+GRAFT_MODE_CHECKPOINT, GRAFT_MODE_STATIC, GRAFT_MODE_TAIL = 0, 1, 2
+GRAFT_F32, GRAFT_BF16 = 0, 1
+K = 8
+
+# Entry points declared in include/graft.h (checked by the CPU tests).
+EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup", "graft_assemble",
+           "graft_verify_update", "graft_get_matrix", "graft_set_matrix", "graft_matrix_device_ptr",
+           "graft_sync", "graft_last_error", "graft_last_launch_count")
+
+
+class GraftError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"graft error {code}: {msg}")
+        self.code = code
+
+
+class graft_config(ctypes.Structure):
+    _fields_ = [("vocab", ctypes.c_int32), ("topk", ctypes.c_int32), ("budget", ctypes.c_int32),
+                ("max_batch", ctypes.c_int32), ("mode", ctypes.c_int32), ("logits_dtype", ctypes.c_int32),
+                ("ckpt_depth", ctypes.c_int32 * 3), ("ckpt_thr", ctypes.c_float * 3),
+                ("ckpt_draft", ctypes.c_int32 * 3), ("tpl_depth", ctypes.c_int32), ("tpl_width", ctypes.c_int32),
+                ("static_thr", ctypes.c_float), ("tail_thr", ctypes.c_float), ("max_draft_nodes", ctypes.c_int32)]
+
+
+_lib = None
+vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libgraft.so (building it with nvcc when absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        if not build_if_missing:
+            raise ImportError("libgraft.so is not built; run __graft_entry__.build()")
+        _build.build()
+    L = ctypes.CDLL(_build.LIB)
+    L.graft_default_config.argtypes = [ctypes.POINTER(graft_config), i32, i32, i32, i32]
+    L.graft_default_config.restype = None
+    L.graft_init.argtypes = [ctypes.POINTER(graft_config), ctypes.POINTER(vp)]
+    L.graft_destroy.argtypes = [vp]
+    L.graft_warmup.argtypes = [vp, vp, vp, i64, i64, vp]
+    L.graft_assemble.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
+    L.graft_verify_update.argtypes = [vp, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp]
+    L.graft_get_matrix.argtypes = [vp, vp, vp]
+    L.graft_set_matrix.argtypes = [vp, vp, vp]
+    L.graft_matrix_device_ptr.argtypes = [vp]
+    L.graft_matrix_device_ptr.restype = vp
+    L.graft_sync.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.graft_last_error.argtypes = [vp]
+    L.graft_last_error.restype = ctypes.c_char_p
+    L.graft_last_launch_count.argtypes = [vp]
+    L.graft_last_launch_count.restype = i32
+    for name in ("graft_init", "graft_destroy", "graft_warmup", "graft_assemble", "graft_verify_update",
+                 "graft_get_matrix", "graft_set_matrix", "graft_sync"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return vp(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return vp(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return vp(stream)
+    return vp(stream.cuda_stream)
+
+
+def graft_default_config(vocab, max_batch, mode=GRAFT_MODE_CHECKPOINT, logits_dtype=GRAFT_BF16, **overrides):
+    cfg = graft_config()
+    load().graft_default_config(ctypes.byref(cfg), vocab, max_batch, mode, logits_dtype)
+    for k, v in overrides.items():
+        if k in ("ckpt_depth", "ckpt_thr", "ckpt_draft"):
+            arr = getattr(cfg, k)
+            for i in range(3):
+                arr[i] = v[i]
+        else:
+            setattr(cfg, k, v)
+    return cfg
+
+
+class Graft:
+    """One libgraft handle (owns the continuation matrix on the current device)."""
+
+    def __init__(self, cfg: graft_config):
+        self.L = load()
+        self.cfg = cfg
+        self.S = cfg.budget + 1
+        h = vp()
+        rc = self.L.graft_init(ctypes.byref(cfg), ctypes.byref(h))
+        if rc != GRAFT_OK:
+            raise GraftError(rc, "graft_init failed (bad config, no CUDA device, or out of memory)")
+        self.h = h
+
+    def _check(self, rc):
+        if rc != GRAFT_OK:
+            raise GraftError(rc, self.L.graft_last_error(self.h).decode())
+
+    def close(self):
+        if self.h:
+            self.L.graft_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # --- entry points (same names as the C ABI, without the prefix) ---------------
+    def warmup(self, tokens, logits, stream=None):
+        """tokens: int32 [N] CUDA; logits: [N, >=V] CUDA (bf16 or float32)."""
+        n = tokens.numel()
+        self._check(self.L.graft_warmup(self.h, _ptr(tokens), _ptr(logits), n, logits.stride(0) if n else self.cfg.vocab,
+                                        _stream(stream)))
+
+    def assemble(self, batch, root_tok, draft_tok, draft_parent, draft_aux, tree_tok, tree_parent, tree_pos, tree_mask,
+                 info, stream=None):
+        n = draft_tok.shape[-1]
+        self._check(self.L.graft_assemble(self.h, batch, _ptr(root_tok), _ptr(draft_tok), _ptr(draft_parent),
+                                          _ptr(draft_aux), n, _ptr(tree_tok), _ptr(tree_parent), _ptr(tree_pos),
+                                          _ptr(tree_mask), _ptr(info), _stream(stream)))
+
+    def verify_update(self, batch, tree_tok, tree_parent, tree_pos, tree_mask, logits, accept_len, out_tokens,
+                      stream=None):
+        """logits: [batch*S, >=V] rows (any leading shape; the last dim's stride is 1)."""
+        stride = logits.stride(-2)
+        self._check(self.L.graft_verify_update(self.h, batch, _ptr(tree_tok), _ptr(tree_parent), _ptr(tree_pos),
+                                               _ptr(tree_mask), _ptr(logits), stride, _ptr(accept_len),
+                                               _ptr(out_tokens), _stream(stream)))
+
+    def get_matrix(self, stream=None) -> np.ndarray:
+        out = np.empty((self.cfg.vocab, K), np.int32)
+        self._check(self.L.graft_get_matrix(self.h, out.ctypes.data_as(vp), _stream(stream)))
+        return out
+
+    def set_matrix(self, m: np.ndarray, stream=None):
+        m = np.ascontiguousarray(m, np.int32)
+        assert m.shape == (self.cfg.vocab, K)
+        self._check(self.L.graft_set_matrix(self.h, m.ctypes.data_as(vp), _stream(stream)))
+
+    def matrix_device_ptr(self) -> int:
+        return int(self.L.graft_matrix_device_ptr(self.h))
+
+    def sync(self, stream=None, raise_on_error=True) -> int:
+        flags = ctypes.c_uint32(0)
+        rc = self.L.graft_sync(self.h, _stream(stream), ctypes.byref(flags))
+        if raise_on_error:
+            self._check(rc)
+        return int(flags.value)
+
+    def last_error(self) -> str:
+        return self.L.graft_last_error(self.h).decode()
+
+    def last_launch_count(self) -> int:
+        return int(self.L.graft_last_launch_count(self.h))
+
+
+class TreeBuffers:
+    """Device buffers of flattened trees for `batch` requests of S slots."""
+
+    def __init__(self, batch, S, device):
+        import torch
+        self.tok = torch.empty((batch, S), dtype=torch.int32, device=device)
+        self.parent = torch.empty((batch, S), dtype=torch.int8, device=device)
+        self.pos = torch.empty((batch, S), dtype=torch.int32, device=device)
+        self.mask = torch.empty((batch, S), dtype=torch.int64, device=device)
+        self.info = torch.empty((batch, 4), dtype=torch.int32, device=device)
+        self.accept_len = torch.empty((batch,), dtype=torch.int32, device=device)
+        self.out_tokens = torch.empty((batch, S), dtype=torch.int32, device=device)

@@ -1,0 +1,169 @@
+/*
+ * graft.h — C ABI of the Graft hot path on one GPU (sm_103a).
+ *
+ * Graft (arXiv 2605.20104, "prune then graft" hybrid draft trees for lossless
+ * speculative decoding) runs one decode step as:
+ *   1. a calibrated confidence check at draft depths 0, 1 and 5 that may stop
+ *      the drafter early and split a fixed 60-slot verification budget
+ *      between draft and retrieval nodes (8+52, 24+36, 40+20, or 60+0);
+ *   2. a retrieval subtree gathered from a GPU-resident continuation matrix
+ *      C[V][8] (the 8 most likely successors of every token), expanded from
+ *      the current token by an asymmetric template;
+ *   3. the hybrid tree flattened into tokens, parent indices, tree positions
+ *      and an ancestor mask;
+ *   4. greedy verification against the target's logits (longest accepted
+ *      path, ties to the lower token id);
+ *   5. the online update: every verified position, accepted or rejected,
+ *      overwrites C[its token] with the top-8 of its logits row.
+ * Sources: Hugging Face paper page 2605.20104 (abstract); popular-science
+ * article on the paper, section 二 (the three gears: steps 1-5), section 四
+ * (static-tree batched mode), section 六 (warm-up), section 七 (Graft-TAIL).
+ *
+ * Conventions (all entry points):
+ *   - Pointers named d_* are DEVICE pointers owned by the caller; they must
+ *     stay valid until the work queued on `stream` has finished.  `stream` is
+ *     a cudaStream_t (NULL = legacy default stream).
+ *   - Every call is asynchronous and stream-ordered unless stated otherwise.
+ *     Argument errors are returned at once and nothing is queued.
+ *   - Device-side data errors (token id out of range, NaN logits or
+ *     probabilities, malformed trees) set a sticky device error word; the
+ *     kernels then keep every access in bounds and finish.  graft_sync()
+ *     returns GRAFT_EDEVICE and clears the word.
+ *   - The handle owns the continuation matrix and all scratch memory.  A
+ *     handle is not thread-safe; queue all its work on one stream at a time.
+ *   - Return value: GRAFT_OK (0) or a negative graft_status; the message of
+ *     the last failure is available from graft_last_error().
+ */
+#ifndef GRAFT_H_
+#define GRAFT_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct graft_handle graft_handle;
+
+typedef enum {
+  GRAFT_OK = 0,
+  GRAFT_EINVAL = -1,   /* bad argument; nothing was queued */
+  GRAFT_ENOMEM = -2,   /* device allocation failed (graft_init only) */
+  GRAFT_ECUDA = -3,    /* a CUDA call failed */
+  GRAFT_EDEVICE = -4   /* a kernel flagged bad data (see graft_sync) */
+} graft_status;
+
+/* Device error word bits (graft_sync's *out_flags). */
+#define GRAFT_ERR_TOKEN 1u   /* a token id outside [0, V) (input or matrix) */
+#define GRAFT_ERR_NAN 2u     /* NaN in a logits row or a draft probability */
+#define GRAFT_ERR_TREE 4u    /* parent index not before its child, bad position */
+
+typedef enum {
+  GRAFT_MODE_CHECKPOINT = 0, /* article §二: checkpoints at depths 0/1/5 */
+  GRAFT_MODE_STATIC = 1,     /* article §四: fixed slots, in-place replacement */
+  GRAFT_MODE_TAIL = 2        /* article §七: block draft, tail replaced */
+} graft_mode;
+
+typedef enum { GRAFT_F32 = 0, GRAFT_BF16 = 1 } graft_dtype;
+
+typedef struct {
+  int32_t vocab;          /* V >= 1 */
+  int32_t topk;           /* successors per matrix row; must be 8 */
+  int32_t budget;         /* verification slots besides the root (60; 16 for tail); S = budget + 1 <= 64 */
+  int32_t max_batch;      /* largest batch passed to assemble / verify_update */
+  int32_t mode;           /* graft_mode */
+  int32_t logits_dtype;   /* graft_dtype of every logits buffer */
+  int32_t ckpt_depth[3];  /* checkpoint draft layers, checked in this order (0, 1, 5) */
+  float ckpt_thr[3];      /* fire when the layer's best path confidence < thr (0.30, 0.20, 0.10) */
+  int32_t ckpt_draft[3];  /* draft slots kept when that checkpoint fires (8, 24, 40); retrieval gets the rest */
+  int32_t tpl_depth;      /* retrieval template depth (8) */
+  int32_t tpl_width;      /* template root width; rank-r node fan-out max(1, width >> r) (8) */
+  float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15) */
+  float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4) */
+  int32_t max_draft_nodes;/* largest draft tree (<= 256) or block (<= budget) per request */
+} graft_config;
+
+/* Fill *cfg with the paper's defaults for `mode` and vocabulary V. */
+void graft_default_config(graft_config* cfg, int32_t vocab, int32_t max_batch, int32_t mode,
+                          int32_t logits_dtype);
+
+/* Create a handle on the current CUDA device: allocates the continuation
+ * matrix (V x 8 int32, every entry -1 = empty), builds the retrieval template
+ * and allocates scratch.  Synchronous.  *out receives the handle. */
+int graft_init(const graft_config* cfg, graft_handle** out);
+
+/* Free everything the handle owns (synchronises the device first). */
+int graft_destroy(graft_handle* h);
+
+/* Warm-up bulk load (article §六): for n = 0..n_rows-1 in order,
+ *   C[d_tokens[n]] <- top-8 ids of logits row n  (value descending, id ascending),
+ * so the last occurrence of a token wins.  d_logits row n starts at element
+ * n * row_stride (row_stride >= V).  Rows whose token recurs later are not read.
+ * Queues four kernels; no host synchronisation. */
+int graft_warmup(graft_handle* h, const int32_t* d_tokens, const void* d_logits, int64_t n_rows,
+                 int64_t row_stride, void* stream);
+
+/* Steps 1-3 for `batch` requests (article §二 gears 1-2 and the flatten of
+ * gear 3; §四 in static mode; §七 in tail mode).  Inputs per request b:
+ *   d_root_tok[b]                     last emitted token (the tree root)
+ *   checkpoint / static mode:
+ *     d_draft_tok[b][n], d_draft_parent[b][n] (int16, -1 = child of the root,
+ *     else an earlier index: BFS order), d_draft_aux[b][n] = the node's draft
+ *     probability given its parent, n = draft_nodes
+ *   tail mode:
+ *     d_draft_tok[b][n] block tokens, d_draft_aux[b][n] per-position
+ *     confidences; d_draft_parent is ignored (may be NULL)
+ * Outputs per request, S = budget + 1 slots (slot 0 = root):
+ *   d_tree_tok[b][S]    token, -1 for a pad slot
+ *   d_tree_parent[b][S] parent slot (int8), -1 for the root and pads
+ *   d_tree_pos[b][S]    tree position = depth below the root, -1 for pads
+ *   d_tree_mask[b][S]   bit j set iff slot j is an ancestor of (or is) the slot
+ *   d_info[b][4]        {event, kept draft nodes, realised retrieval nodes, valid slots}
+ *                       event = fired depth or -1 (checkpoint), replaced nodes
+ *                       (static), tail start t (tail)
+ * Reads the matrix as it stands when the kernel runs. */
+int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                   const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes,
+                   int32_t* d_tree_tok, int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask,
+                   int32_t* d_info, void* stream);
+
+/* Steps 4-5 (article §二 gear 3, §三): one streaming pass over the logits of
+ * every valid slot computes its top-8 (element 0 = the greedy argmax), then
+ *   accepted(i)  <=> every non-root node j on the root->i path has
+ *                    tok[j] == argmax(row of parent(j));
+ *   winner       =  the accepted slot of greatest position (ties: lower slot);
+ *   d_accept_len[b] = position of the winner;
+ *   d_out_tokens[b][S] = the winner's path tokens after the root, then the
+ *                        bonus token argmax(row of winner), then -1s;
+ * and every valid slot overwrites C[its token] with its top-8 (the last
+ * writer in (request, slot) order wins).  Pad slots (tok < 0) are not read.
+ * The tree arrays are those written by graft_assemble (or equivalent ones).
+ * d_logits row (b, i) starts at element (b*S + i) * row_stride (row_stride >= V). */
+int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
+                        const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
+                        int64_t row_stride, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream);
+
+/* Copy the continuation matrix (V x 8 int32, row-major) to / from HOST memory.
+ * Synchronous with respect to `stream`. */
+int graft_get_matrix(graft_handle* h, int32_t* host_out, void* stream);
+int graft_set_matrix(graft_handle* h, const int32_t* host_in, void* stream);
+
+/* Device pointer to the continuation matrix (V x 8 int32), owned by the handle. */
+int32_t* graft_matrix_device_ptr(graft_handle* h);
+
+/* Synchronise `stream`, read and clear the device error word.  *out_flags
+ * (may be NULL) receives the GRAFT_ERR_* bits.  Returns GRAFT_EDEVICE if any
+ * bit was set. */
+int graft_sync(graft_handle* h, void* stream, uint32_t* out_flags);
+
+/* Message of the last failed call on this handle ("" if none). */
+const char* graft_last_error(const graft_handle* h);
+
+/* Number of kernel launches the last graft_assemble / graft_verify_update /
+ * graft_warmup call queued. */
+int32_t graft_last_launch_count(const graft_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GRAFT_H_ */

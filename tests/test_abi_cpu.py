@@ -1,0 +1,56 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, and
+exports every entry point include/graft.h declares; the binding's struct
+matches the header's layout.  No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "graft.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(graft_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("graft_init", "graft_destroy", "graft_warmup", "graft_assemble", "graft_verify_update",
+              "graft_get_matrix", "graft_set_matrix", "graft_sync", "graft_last_error"):
+        assert n in names
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    import hybrid_draft_tree_gb300 as g
+    from hybrid_draft_tree_gb300 import _build
+    _build.build()
+    lib = ctypes.CDLL(g.library_path())
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert sorted(g.EXPORTS) == declared_functions()
+
+
+def test_config_struct_layout_and_defaults():
+    import hybrid_draft_tree_gb300 as g
+    cfg = g.graft_default_config(151936, 16, g.GRAFT_MODE_STATIC, g.GRAFT_BF16)
+    assert ctypes.sizeof(cfg) == 4 * 20
+    assert (cfg.vocab, cfg.topk, cfg.budget, cfg.max_batch) == (151936, 8, 60, 16)
+    assert list(cfg.ckpt_depth) == [0, 1, 5]
+    assert [round(x, 6) for x in cfg.ckpt_thr] == [0.3, 0.2, 0.1]
+    assert list(cfg.ckpt_draft) == [8, 24, 40]
+    assert (cfg.tpl_depth, cfg.tpl_width) == (8, 8)
+    assert abs(cfg.static_thr - 0.15) < 1e-7 and abs(cfg.tail_thr - 0.4) < 1e-7
+    tail = g.graft_default_config(151936, 64, g.GRAFT_MODE_TAIL, g.GRAFT_BF16)
+    assert tail.budget == 16 and tail.max_draft_nodes == 16
+
+
+def test_init_without_gpu_fails_cleanly():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("has a GPU")
+    import hybrid_draft_tree_gb300 as g
+    with pytest.raises(g.GraftError):
+        g.Graft(g.graft_default_config(100, 1, 0, g.GRAFT_BF16))

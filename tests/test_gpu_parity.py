@@ -1,0 +1,372 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle,
+element by element on the same seeded inputs — trees, positions, masks,
+acceptance, emitted tokens and the continuation matrix after every step.
+
+Covers the five workloads (checkpoint / static / tail modes, fp32 and bf16),
+ragged and unaligned rows (vector and scalar load paths, tail elements),
+rows that overflow the candidate list (all-equal values), warm-up, the
+device-side error flags, and full-size cases in the benchmark's launch
+configuration.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def G():
+    import hybrid_draft_tree_gb300 as g
+    return g
+
+
+def engine_for(w, **kw):
+    g = G()
+    cfg = g.graft_default_config(w.V, w.B, w.mode, w.dtype, budget=w.budget, max_draft_nodes=w.draft_nodes, **kw)
+    return g.Graft(cfg)
+
+
+def u16_to_bf16_tensor(u16, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def assert_trees_equal(loop, trees, step):
+    B = loop.w.B
+    gt = loop.tok.cpu().numpy()
+    gp = loop.par.cpu().numpy().astype(np.int32)
+    gpos = loop.pos.cpu().numpy()
+    gm = loop.mask.cpu().numpy().view(np.uint64)
+    gi = loop.info.cpu().numpy()
+    for b in range(B):
+        tr = trees[b]
+        assert np.array_equal(gt[b], tr.tok), (step, b, "tok")
+        assert np.array_equal(gp[b], tr.par), (step, b, "parent")
+        assert np.array_equal(gpos[b], tr.pos), (step, b, "pos")
+        assert np.array_equal(gm[b], tr.mask), (step, b, "mask")
+        assert np.array_equal(gi[b], tr.info), (step, b, "info", gi[b], tr.info)
+
+
+def lockstep(w, steps, warm=False, check_rows=0, stats=None):
+    """Run the GPU closed loop and the oracle side by side; compare all."""
+    from workloads.device_loop import DeviceLoop
+    g = engine_for(w)
+    loop = DeviceLoop(w, g)
+    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
+    C = oracle.new_matrix(w.V)
+    if warm:
+        toks_d, logits_d, (toks, rk, pl, bi) = loop.warm_inputs_device()
+        g.warmup(toks_d, logits_d)
+        rows = W.fill_rows(rk, pl, bi, w.V, w.dtype)
+        oracle.warmup(C, toks, rows, w.dtype)
+        assert np.array_equal(g.get_matrix(), C), "matrix after warm-up"
+        del logits_d
+    for step in range(steps):
+        tok, par, aux = loop.draft()
+        loop.assemble()
+        trees = [oracle.assemble(P, loop.root_h[b], tok[b], aux[b], C, None if par is None else par[b])
+                 for b in range(w.B)]
+        assert_trees_equal(loop, trees, step)
+        loop.make_logits()
+        tt = np.stack([t.tok for t in trees])
+        pp = np.stack([t.par for t in trees]).astype(np.int8)
+        lg = loop.h.tree_logits(tt, pp, loop.ctx_h, loop.prev_h)
+        if check_rows:
+            dev = loop.logits.view(torch.int16 if w.dtype else torch.int32).cpu().numpy()
+            flat = lg.reshape(w.B * w.S, -1)
+            for r in np.random.default_rng(step).choice(w.B * w.S, check_rows, replace=False):
+                if tt.reshape(-1)[r] >= 0:
+                    assert np.array_equal(dev[r].view(flat.dtype), flat[r]), ("logits row", step, r)
+        loop.verify_update()
+        acc_g = loop.accept_len.cpu().numpy()
+        out_g = loop.out_tokens.cpu().numpy()
+        for b in range(w.B):
+            acc, out, topk = oracle.verify(trees[b], lg[b], w.dtype)
+            oracle.update(C, trees[b], topk)
+            assert acc_g[b] == acc, (step, b, "accept_len", acc_g[b], acc)
+            assert np.array_equal(out_g[b], out), (step, b, "out_tokens", out_g[b], out)
+            if stats is not None:
+                stats.append((int(trees[b].info[0]), acc))
+        assert np.array_equal(g.get_matrix(), C), (step, "matrix")
+        loop.advance()
+    assert g.sync() == 0
+    g.close()
+
+
+# ------------------------------------------------------------------------------ generator
+def test_generator_device_matches_host():
+    rng = np.random.default_rng(0)
+    h = W.Harness(W.WORKLOADS[1].scaled(V=1037))
+    ds = W.DeviceSynth(h, torch.device("cuda"))
+    for dtype in (W.F32, W.BF16):
+        n = 7
+        rk = rng.integers(0, 2**64, n, dtype=np.uint64)
+        pl = np.array([5, -1, -2, 1036, 0, 77, -1], np.int32)
+        bi = np.full(n, 5.0, np.float32)
+        host = W.fill_rows(rk, pl, bi, 1037, dtype)
+        out = torch.empty((n, 1037), dtype=torch.float32 if dtype == W.F32 else torch.bfloat16, device="cuda")
+        ds.fill_rows(torch.from_numpy(rk.view(np.int64)).cuda(), torch.from_numpy(pl).cuda(),
+                     torch.from_numpy(bi).cuda(), out, torch.cuda.current_stream().cuda_stream)
+        dev = out.view(torch.int32 if dtype == W.F32 else torch.int16).cpu().numpy().view(host.dtype)
+        assert np.array_equal(dev, host)
+    # tree row parameters
+    B, S = 3, 61
+    tok = rng.integers(0, 1037, (B, S)).astype(np.int32)
+    par = np.full((B, S), -1, np.int8)
+    for i in range(1, S):
+        par[:, i] = rng.integers(0, i, B)
+    tok[1, 40:] = -1
+    prev = rng.integers(0, 1037, B).astype(np.int32)
+    ctx = rng.integers(0, 2**64, B, dtype=np.uint64)
+    hk, hp, hb = h.tree_rowparams(tok, par, ctx, prev)
+    dk, dp, db = ds.tree_rowparams(torch.from_numpy(tok).cuda(), torch.from_numpy(par).cuda(),
+                                   torch.from_numpy(ctx.view(np.int64)).cuda(), torch.from_numpy(prev).cuda(),
+                                   torch.cuda.current_stream().cuda_stream)
+    assert np.array_equal(dk.cpu().numpy().view(np.uint64), hk)
+    assert np.array_equal(dp.cpu().numpy(), hp)
+    assert np.array_equal(db.cpu().numpy(), hb)
+
+
+# ------------------------------------------------------------------------------ closed loops
+@pytest.mark.parametrize("wid,V,B,sigma,steps", [
+    (0, 3001, 1, 2.0, 25),      # checkpoint, fp32, ragged V
+    (0, 4000, 1, 0.75, 40),     # checkpoint, all checkpoints fire
+    (0, 4000, 4, 0.5, 20),      # batched checkpoint mode
+    (1, 5003, 1, 0.75, 30),     # bf16 trigram target, ragged V
+    (2, 6000, 16, 2.0, 20),     # static mode, shared matrix across 16 requests
+    (2, 777, 16, 0.75, 20),     # static mode, heavy duplicate tokens (last-writer races)
+    (4, 6007, 64, 2.0, 15),     # tail mode, 64 requests
+    (4, 500, 64, 2.0, 15),      # tail mode, small vocab: many duplicate writers
+])
+def test_lockstep_small(wid, V, B, sigma, steps):
+    w = W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=sigma)
+    stats = []
+    lockstep(w, steps, check_rows=8, stats=stats)
+    assert any(a > 0 for _, a in stats)
+
+
+@pytest.mark.parametrize("wid", [1, 3])
+def test_lockstep_warmup_small(wid):
+    base = W.WORKLOADS[wid]
+    kw = dict(V=2048, draft_sigma=0.75)
+    if base.warm == "history":
+        kw.update(hist_len=3000, hist_active=300)
+    lockstep(base.scaled(**kw), 15, warm=True)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wid,steps", [(0, 100), (1, 6), (2, 3), (4, 2)])
+def test_lockstep_full_size(wid, steps):
+    """Full BASELINE sizes, the launch configuration the benchmark times."""
+    w = W.WORKLOADS[wid]
+    lockstep(w, steps, warm=(w.warm == "rollouts"), check_rows=4)
+
+
+@pytest.mark.slow
+def test_warm_start_32k_full_size_sampled():
+    """32768-row warm start at V=151936 (9.96 GB of bf16 logits on the
+    device): sampled rows of the matrix against the oracle's top-8 of each
+    token's last occurrence, untouched rows stay empty, then decode steps in
+    lockstep."""
+    from workloads.device_loop import DeviceLoop
+    w = W.WORKLOADS[3]
+    g = engine_for(w)
+    loop = DeviceLoop(w, g)
+    toks_d, logits_d, (toks, rk, pl, bi) = loop.warm_inputs_device()
+    g.warmup(toks_d, logits_d)
+    del logits_d
+    torch.cuda.empty_cache()
+    Cg = g.get_matrix()
+    last = {}
+    for n, t in enumerate(toks.tolist()):
+        last[t] = n
+    present = np.zeros(w.V, bool)
+    present[list(last)] = True
+    assert (Cg[~present] == -1).all()
+    assert (Cg[present] >= 0).all()
+    rng = np.random.default_rng(0)
+    sample = rng.choice(sorted(last), 40, replace=False)
+    for t in sample:
+        n = last[t]
+        row = W.fill_rows(rk[n:n + 1], pl[n:n + 1], bi[n:n + 1], w.V, w.dtype)[0]
+        assert np.array_equal(Cg[t], oracle.topk8_row(row, w.dtype)), t
+    # continue decoding in lockstep from the warmed matrix
+    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
+    C = Cg.copy()
+    for step in range(3):
+        tok, par, aux = loop.draft()
+        loop.assemble()
+        trees = [oracle.assemble(P, loop.root_h[0], tok[0], aux[0], C, par[0])]
+        assert_trees_equal(loop, trees, step)
+        loop.make_logits()
+        lg = loop.h.tree_logits(trees[0].tok[None], trees[0].par[None].astype(np.int8), loop.ctx_h, loop.prev_h)
+        loop.verify_update()
+        acc, out, topk = oracle.verify(trees[0], lg[0], w.dtype)
+        oracle.update(C, trees[0], topk)
+        assert loop.accept_len.cpu().numpy()[0] == acc
+        assert np.array_equal(loop.out_tokens.cpu().numpy()[0], out)
+        assert np.array_equal(g.get_matrix(), C)
+        loop.advance()
+    assert g.sync() == 0
+
+
+# ------------------------------------------------------------------------------ verify edge cases
+def _tree_from_parents(tok, par):
+    S = len(tok)
+    t = oracle.Tree(S)
+    t.tok[:] = tok
+    t.par[:] = par
+    for i in range(S):
+        if tok[i] < 0:
+            t.par[i], t.pos[i], t.mask[i] = -1, -1, 0
+        elif i == 0:
+            t.pos[0], t.mask[0] = 0, 1
+        else:
+            t.pos[i] = t.pos[par[i]] + 1
+            t.mask[i] = np.uint64(int(t.mask[par[i]]) | (1 << i))
+    return t
+
+
+def _verify_case(V, dtype, S, B, rows_fn, stride_pad=0, seed=0, offset_elems=0):
+    """Random trees over rows_fn(rng, n, V) logits, each node following its
+    parent's argmax with probability 1/2; GPU verify_update vs the oracle."""
+    g_ = G()
+    rng = np.random.default_rng(seed)
+    vals = rows_fn(rng, B * S, V)                       # float32 [B*S, V]
+    if dtype == W.BF16:
+        host_rows = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    else:
+        host_rows = vals
+    hr = host_rows.reshape(B, S, V)
+    trees = []
+    for b in range(B):
+        n = int(rng.integers(1, S + 1))
+        tok = np.full(S, -1, np.int32)
+        par = np.full(S, -1, np.int32)
+        tok[:n] = rng.integers(0, V, n)
+        for i in range(1, n):
+            par[i] = rng.integers(0, i)
+            if rng.random() < 0.5:
+                tok[i] = oracle.topk8_row(hr[b, par[i]], dtype)[0]
+        trees.append(_tree_from_parents(tok, par))
+    stride = V + stride_pad
+    buf = np.zeros(B * S * stride + offset_elems, host_rows.dtype)
+    buf[offset_elems:].reshape(B * S, stride)[:, :V] = host_rows
+    dev = u16_to_bf16_tensor(buf) if dtype == W.BF16 else torch.from_numpy(buf).cuda()
+    logits = dev[offset_elems:].view(B * S, stride)
+    cfg = g_.graft_default_config(V, B, 0, dtype, budget=S - 1)
+    eng = g_.Graft(cfg)
+    tt = torch.from_numpy(np.stack([t.tok for t in trees])).cuda()
+    tp = torch.from_numpy(np.stack([t.par for t in trees]).astype(np.int8)).cuda()
+    tpos = torch.from_numpy(np.stack([t.pos for t in trees])).cuda()
+    tm = torch.from_numpy(np.stack([t.mask for t in trees]).view(np.int64)).cuda()
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty((B, S), dtype=torch.int32, device="cuda")
+    C0 = rng.integers(-1, V, (V, 8)).astype(np.int32)
+    eng.set_matrix(C0)
+    eng.verify_update(B, tt, tp, tpos, tm, logits, acc, out)
+    C = C0.copy()
+    accepted = 0
+    for b in range(B):
+        a, o, topk = oracle.verify(trees[b], hr[b], dtype)
+        oracle.update(C, trees[b], topk)
+        assert acc.cpu().numpy()[b] == a
+        assert np.array_equal(out.cpu().numpy()[b], o)
+        accepted += a
+    assert np.array_equal(eng.get_matrix(), C)
+    assert eng.sync() == 0
+    eng.close()
+    return accepted
+
+
+def _normal(rng, n, V):
+    return rng.normal(size=(n, V)).astype(np.float32)
+
+
+def _ties(rng, n, V):
+    v = rng.integers(-2, 3, (n, V)).astype(np.float32)
+    v[rng.random((n, V)) < 0.3] = -0.0
+    return v
+
+
+def _constant(rng, n, V):
+    return np.full((n, V), 1.5, np.float32)
+
+
+@pytest.mark.parametrize("V", [1, 7, 8, 37, 1000, 4099, 40000])
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_verify_ragged_vocab(V, dtype):
+    _verify_case(V, dtype, 61, 2, _normal, seed=V)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("pad,off", [(1, 0), (3, 1), (8, 0)])
+def test_verify_unaligned_rows(dtype, pad, off):
+    """Row starts off 16-byte boundaries take the scalar-load path."""
+    _verify_case(3001, dtype, 17, 3, _normal, stride_pad=pad, offset_elems=off, seed=pad)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("fn", [_ties, _constant])
+def test_verify_ties_and_candidate_overflow(dtype, fn):
+    """Heavy ties and all-equal rows (more candidates than the list holds:
+    the exact fallback selection)."""
+    _verify_case(20000, dtype, 33, 2, fn, seed=11)
+
+
+def test_batch_zero_is_a_noop():
+    g_ = G()
+    eng = g_.Graft(g_.graft_default_config(100, 4, 0, W.BF16))
+    eng.verify_update(0, None, None, None, None, torch.empty((1, 100), dtype=torch.bfloat16, device="cuda"),
+                      None, None)
+    assert eng.sync() == 0
+    assert (eng.get_matrix() == -1).all()
+
+
+def test_error_flags_and_recovery():
+    """NaN logits and out-of-range tokens raise device flags (no fault); the
+    handle stays usable."""
+    g_ = G()
+    V, S = 500, 61
+    eng = g_.Graft(g_.graft_default_config(V, 1, 0, W.F32))
+    tok = np.array([3, 4] + [-1] * (S - 2), np.int32)
+    par = np.array([-1, 0] + [-1] * (S - 2), np.int32)
+    tr = _tree_from_parents(tok, par)
+    tt = torch.from_numpy(tr.tok[None]).cuda()
+    tp = torch.from_numpy(tr.par[None].astype(np.int8)).cuda()
+    tpos = torch.from_numpy(tr.pos[None]).cuda()
+    tm = torch.from_numpy(tr.mask[None].view(np.int64)).cuda()
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((1, S), dtype=torch.int32, device="cuda")
+    logits = torch.zeros((S, V), dtype=torch.float32, device="cuda")
+    logits[1, 17] = float("nan")
+    eng.verify_update(1, tt, tp, tpos, tm, logits, acc, out)
+    assert eng.sync(raise_on_error=False) & g_.graft.GRAFT_ERR_NAN
+    assert eng.sync() == 0                               # cleared
+    tt[0, 1] = V + 9
+    logits[1, 17] = 0.0
+    eng.verify_update(1, tt, tp, tpos, tm, logits, acc, out)
+    assert eng.sync(raise_on_error=False) & g_.graft.GRAFT_ERR_TOKEN
+    tt[0, 1] = 4
+    eng.verify_update(1, tt, tp, tpos, tm, logits, acc, out)
+    assert eng.sync() == 0
+    assert acc.item() == 0 and out[0, 0].item() == 0     # argmax of a zero row is id 0
+
+
+def test_invalid_arguments_are_rejected():
+    g_ = G()
+    eng = g_.Graft(g_.graft_default_config(100, 2, 0, W.BF16))
+    with pytest.raises(g_.GraftError):
+        eng.verify_update(3, None, None, None, None, torch.empty((1, 100), device="cuda"), None, None)  # batch > max
+    bad = g_.graft_default_config(100, 2, 0, W.BF16, topk=4)
+    with pytest.raises(g_.GraftError):
+        g_.Graft(bad)

@@ -115,6 +115,7 @@ __global__ void k_tree_rowparams(Target tg, int32_t B, int32_t S, const int32_t*
     if (i == 0) { ctx[i] = root_ctx[b]; prev = root_prev[b]; }
     else {
       int p = parent[k];
+      if (p < 0 || p >= i) { rowkey[k] = 0; planted[k] = -2; bias[k] = 0.f; continue; }  // malformed: pad
       ctx[i] = ctx_push(ctx[p], t);
       prev = tok[(int64_t)b * S + p];
     }

@@ -160,7 +160,7 @@ void syn_tree_rowparams(int32_t V, int32_t kind, int32_t hit_all, uint32_t hit_n
   syn_target tg; mk_target(&tg, V, kind, hit_all, hit_num, bias_val, seed, table);
   uint64_t ctx[256];
   for (int32_t b = 0; b < B; ++b) {
-    for (int32_t i = 0; i < S; ++i) {
+    for (int32_t i = 0; i < S && i < 256; ++i) {
       int64_t k = (int64_t)b * S + i;
       int32_t t = tok[k];
       if (t < 0) { rowkey[k] = 0; planted[k] = -2; bias[k] = 0.f; continue; }
@@ -168,6 +168,7 @@ void syn_tree_rowparams(int32_t V, int32_t kind, int32_t hit_all, uint32_t hit_n
       if (i == 0) { ctx[i] = root_ctx[b]; prev = root_prev[b]; }
       else {
         int p = parent[k];
+        if (p < 0 || p >= i) { rowkey[k] = 0; planted[k] = -2; bias[k] = 0.f; continue; }
         ctx[i] = syn_ctx_push(ctx[p], t);
         prev = tok[(int64_t)b * S + p];
       }
