@@ -70,7 +70,6 @@ struct TplCmp {
 void build_template(int max_depth, int width, int len, std::vector<int32_t>& parent, std::vector<int32_t>& rank,
                     std::vector<int32_t>& depth) {
   std::priority_queue<TplNode, std::vector<TplNode>, TplCmp> frontier;
-  struct Parented { TplNode node; int parent_index; };
   // frontier entries carry their parent's emitted index in `index`
   for (int r = 0; r < width && r < graft::K; ++r) frontier.push(TplNode{r, 1, {r}, -1});
   while ((int)parent.size() < len && !frontier.empty()) {
@@ -111,9 +110,10 @@ int check_cfg(const graft_config* c, graft_handle* h) {
     return fail(h, GRAFT_EINVAL, "max_batch * (budget + 1) must be in [1, 65535]");
   if (c->mode < GRAFT_MODE_CHECKPOINT || c->mode > GRAFT_MODE_TAIL) return fail(h, GRAFT_EINVAL, "bad mode");
   if (c->logits_dtype != GRAFT_F32 && c->logits_dtype != GRAFT_BF16) return fail(h, GRAFT_EINVAL, "bad logits dtype");
-  for (int k = 0; k < 3; ++k)
-    if (c->ckpt_draft[k] < 0 || c->ckpt_draft[k] > c->budget || c->ckpt_depth[k] < 0)
-      return fail(h, GRAFT_EINVAL, "checkpoint %d: draft slots must be in [0, budget], depth >= 0", k);
+  if (c->mode == GRAFT_MODE_CHECKPOINT)
+    for (int k = 0; k < 3; ++k)
+      if (c->ckpt_draft[k] < 0 || c->ckpt_draft[k] > c->budget || c->ckpt_depth[k] < 0)
+        return fail(h, GRAFT_EINVAL, "checkpoint %d: draft slots must be in [0, budget], depth >= 0", k);
   if (c->tpl_depth < 1 || c->tpl_depth > 16 || c->tpl_width < 1 || c->tpl_width > graft::K)
     return fail(h, GRAFT_EINVAL, "template depth must be in [1, 16] and width in [1, 8]");
   const int maxn = c->mode == GRAFT_MODE_TAIL ? c->budget : graft::MAX_DRAFT;

@@ -165,30 +165,29 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
 
     if (a.mode == GRAFT_MODE_STATIC) {
       // ---- in-place replacement, parents before children (section 四) -----
+      // A replaced slot takes C[parent token][its rank among the parent's
+      // replaced children]; with no candidate there it keeps its draft token,
+      // so every request verifies the same number of slots.
       const int used = 1 + n_draft;
       const int maxpos = s_maxdepth + 1;
-      int nrep_local = (t >= 1 && t < used) ? o_rep[t] : 0;
+      const int nrep_local = (t >= 1 && t < used) ? o_rep[t] : 0;
       for (int level = 1; level <= maxpos; ++level) {
-        if (t >= 1 && t < used && o_pos[t] == level) {
+        if (t >= 1 && t < used && o_pos[t] == level && o_rep[t]) {
           const int p = o_par[t];
           const int32_t ptok = o_tok[p];
-          if (ptok < 0) {
-            o_tok[t] = -1;
-          } else if (o_rep[t]) {
-            int srank = 0;
-            for (int q = 1; q < t; ++q) srank += (o_par[q] == p) && o_rep[q];
-            int32_t tk = -1;
-            if (srank < K) {
-              tk = a.C[(int64_t)ptok * K + srank];
-              if (tk < -1 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); tk = -1; }
-            }
-            o_tok[t] = tk;
+          int srank = 0;
+          for (int q = 1; q < t; ++q) srank += (o_par[q] == p) && (o_rep[q] != 0);
+          int32_t tk = -1;
+          if (srank < K && ptok >= 0 && ptok < a.V) {
+            tk = a.C[(int64_t)ptok * K + srank];
+            if (tk < -1 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); tk = -1; }
           }
+          if (tk >= 0) { o_tok[t] = tk; o_rep[t] = 2; }
         }
         __syncthreads();
       }
-      const bool kept_draft = t >= 1 && t < used && !o_rep[t] && o_tok[t] >= 0;
-      const bool realised = t >= 1 && t < used && o_rep[t] && o_tok[t] >= 0;
+      const bool realised = t >= 1 && t < used && o_rep[t] == 2;
+      const bool kept_draft = t >= 1 && t < used && o_rep[t] != 2;
       block_excl_count(kept_draft, s_warp, n_draft);
       block_excl_count(realised, s_warp, n_retr);
       event = __syncthreads_count(nrep_local != 0);

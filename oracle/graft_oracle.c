@@ -35,7 +35,8 @@
  *   kept draft nodes are the top-D by path confidence (ties: lower BFS
  *   index); unused draft slots stay empty; the template is ordered by
  *   (sum of ranks, depth, rank path) and truncated to the retrieval budget;
- *   an empty (-1) matrix entry drops the node and its subtree; flatten order
+ *   an empty (-1) matrix entry drops a template node and its subtree (in the
+ *   static-tree mode the replaced node keeps its draft token); flatten order
  *   is root, kept draft (BFS), realised retrieval (template order); argmax
  *   and top-k ties go to the lower token id, -0 equals +0, NaN is an error;
  *   the last writer in (request, slot) order wins a matrix row.
@@ -259,12 +260,16 @@ int or_assemble_checkpoint(const or_params* P, int32_t root_tok, int32_t n, cons
 }
 
 /* ------------------------------------------------------------------------
- * Static-tree mode, one request [P2 §四]: the top-`budget` draft tree keeps
- * its slots; every kept node whose path confidence is below static_thr is
- * replaced in place.  A replaced node j whose parent p holds token t takes
- * C[t][s], s = j's rank among p's replaced children in slot order; an empty
- * entry turns j and its subtree into pads (slots stay where they are).
- * info = {replaced count, kept draft, realised retrieval, valid slots}.
+ * Static-tree mode, one request [P2 §四]: each request keeps a fixed number of
+ * verify slots (the top-`budget` draft nodes by path confidence, plus the
+ * root), and every kept node whose path confidence is below static_thr is
+ * replaced in place by a retrieval node.  A replaced node j whose parent p
+ * holds token t (after p's own replacement) takes C[t][s], s = j's rank among
+ * p's replaced children in slot order.  When that entry is empty there is no
+ * retrieval candidate to put there, so j keeps its draft token and the slot
+ * count stays fixed.
+ * info = {nodes marked for replacement, slots holding a draft token,
+ *         slots holding a retrieved token, valid slots}.
  * ---------------------------------------------------------------------- */
 int or_assemble_static(const or_params* P, int32_t root_tok, int32_t n, const int32_t* dtok,
                        const int16_t* dpar, const float* dprob, const int32_t* C,
@@ -297,20 +302,17 @@ int or_assemble_static(const or_params* P, int32_t root_tok, int32_t n, const in
   int32_t nd = 0, nr = 0;
   for (int32_t i = 1; i < used; ++i) {                    /* parents precede children */
     int32_t p = par[i];
-    if (tok[p] < 0) { tok[i] = -1; continue; }            /* parent is a pad */
     if (!replaced[i]) { ++nd; continue; }
     int32_t srank = 0;
     for (int32_t q = 1; q < i; ++q) if (par[q] == p && replaced[q]) ++srank;
     int32_t t = srank < OR_K ? C[(int64_t)tok[p] * OR_K + srank] : -1;
     if (t < -1 || t >= P->V) return OR_EDATA;
-    tok[i] = t;
-    if (t >= 0) ++nr;
+    if (t >= 0) { tok[i] = t; ++nr; }
+    else ++nd;                                            /* no candidate: the draft token stays */
   }
   for (; s < P->S; ++s) tok[s] = -1;
-  int32_t nvalid = 0;
-  for (int32_t i = 0; i < P->S; ++i) nvalid += tok[i] >= 0;
-  finish_tree(P->S, P->S, tok, par, pos, mask);
-  info[0] = nrep; info[1] = nd; info[2] = nr; info[3] = nvalid;
+  finish_tree(P->S, used, tok, par, pos, mask);
+  info[0] = nrep; info[1] = nd; info[2] = nr; info[3] = used;
   return OR_OK;
 }
 

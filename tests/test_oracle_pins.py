@@ -293,14 +293,16 @@ def test_static_mode_in_place_replacement():
     kids = [i for i in range(5, 61) if tr.par[i] == 1]
     assert [tr.tok[i] for i in kids] == [C[tok[0], s] for s in range(len(kids))]
     assert tr.info[3] == 61
-    # an empty entry turns the node and its subtree into pads, in place
+    # an empty entry leaves the draft token in place; the slot count stays 61
     C2 = C.copy()
     C2[7, 1] = -1
     tr2 = oracle.assemble(P, 7, tok, prob, C2, par)
-    assert tr2.tok[3] == -1
-    sub = [i for i in range(61) if tr.par[i] == 3]
-    assert all(tr2.tok[i] == -1 for i in sub)
-    assert np.array_equal(np.where(tr2.tok >= 0)[0], [i for i in range(61) if i != 3 and i not in sub])
+    assert tr2.tok[3] == tok[2]
+    assert tr2.info[3] == 61 and tr2.info[2] == tr.info[2] - 1 - sum(
+        1 for i in range(61) if tr.par[i] == 3)
+    # children of the unreplaced slot 3 now gather from its draft token's row
+    kids3 = [i for i in range(61) if tr2.par[i] == 3]
+    assert [tr2.tok[i] for i in kids3] == [C2[tok[2], s] for s in range(len(kids3))]
 
 
 def test_tail_mode():
