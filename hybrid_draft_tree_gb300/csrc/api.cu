@@ -17,6 +17,7 @@ struct graft_handle {
   int num_sms = 0;
   int warm_ctas = 0;        // resident CTAs of the warm-up scan
   int scan_ctas_target = 0; // CTAs wanted per verify launch
+  bool tma_ready = false;   // the TMA scan's shared-memory opt-in succeeded
   int32_t* C = nullptr;           // [V][8]
   int32_t* winner = nullptr;      // [V]
   int32_t* tpl = nullptr;         // [3][tpl_len]: parent, rank, depth
@@ -119,6 +120,7 @@ int check_cfg(const graft_config* c, graft_handle* h) {
   const int maxn = c->mode == GRAFT_MODE_TAIL ? c->budget : graft::MAX_DRAFT;
   if (c->max_draft_nodes < 0 || c->max_draft_nodes > maxn)
     return fail(h, GRAFT_EINVAL, "max_draft_nodes must be in [0, %d]", maxn);
+  if (c->scan_kernel < 0 || c->scan_kernel > 2) return fail(h, GRAFT_EINVAL, "scan_kernel must be 0, 1 or 2");
   return GRAFT_OK;
 }
 
@@ -141,6 +143,8 @@ graft::ScanGeom scan_geom(const graft_handle* h, const void* logits, int64_t str
   if (nsplit < 1) nsplit = 1;
   g.nsplit = (int32_t)nsplit;
   g.per_cta = (g.nslot + nsplit - 1) / nsplit;
+  g.row_vec_bytes = g.nslot * 16;
+  g.cpr = (int32_t)((g.row_vec_bytes + graft::TMA_CHUNK - 1) / graft::TMA_CHUNK);
   return g;
 }
 
@@ -164,6 +168,7 @@ void graft_default_config(graft_config* c, int32_t vocab, int32_t max_batch, int
   c->static_thr = 0.15f;
   c->tail_thr = 0.4f;
   c->max_draft_nodes = mode == GRAFT_MODE_TAIL ? 16 : 184;
+  c->scan_kernel = 0;
 }
 
 int graft_init(const graft_config* cfg, graft_handle** out) {
@@ -213,6 +218,8 @@ int graft_init(const graft_config* cfg, graft_handle** out) {
   if (e != cudaSuccess) { free_all(h); delete h; return GRAFT_ECUDA; }
   h->warm_ctas = h->num_sms * 4;
   h->scan_ctas_target = h->num_sms * 8;
+  h->tma_ready = graft::prepare_verify_tma() == cudaSuccess;
+  cudaGetLastError();
   *out = h;
   return GRAFT_OK;
 }
@@ -308,7 +315,11 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
   a.accept_len = d_accept_len; a.out_tokens = d_out_tokens;
   a.part = h->part; a.row_ticket = h->row_ticket; a.req_ticket = h->req_ticket; a.topk = h->topk;
   a.winner = h->winner; a.err = h->err;
-  cudaError_t e = graft::launch_verify(a, c.logits_dtype, (cudaStream_t)stream);
+  const bool tma_fits = h->tma_ready && a.g.vec && a.g.row_vec_bytes >= graft::TMA_CHUNK &&
+                        a.g.cpr <= graft::MAX_SPLIT && rows <= graft::verify_tma_max_rows(h->num_sms);
+  const bool use_tma = tma_fits && c.scan_kernel != 1;
+  cudaError_t e = use_tma ? graft::launch_verify_tma(a, c.logits_dtype, h->num_sms, (cudaStream_t)stream)
+                          : graft::launch_verify(a, c.logits_dtype, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update scan launch");
   graft::ScatterArgs x{};
   x.rows = (int32_t)rows; x.V = c.vocab; x.tree_tok = d_tree_tok; x.topk = h->topk; x.winner = h->winner; x.C = h->C;
@@ -344,8 +355,9 @@ int graft_sync(graft_handle* h, void* stream, uint32_t* out_flags) {
   if (e == cudaSuccess && flags) e = cudaMemset(h->err, 0, sizeof(uint32_t));
   if (out_flags) *out_flags = flags;
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_sync");
-  if (flags) return fail(h, GRAFT_EDEVICE, "device error flags 0x%x (token %d, nan %d, tree %d)", flags,
-                         !!(flags & GRAFT_ERR_TOKEN), !!(flags & GRAFT_ERR_NAN), !!(flags & GRAFT_ERR_TREE));
+  if (flags) return fail(h, GRAFT_EDEVICE, "device error flags 0x%x (token %d, nan %d, tree %d, timeout %d)", flags,
+                         !!(flags & GRAFT_ERR_TOKEN), !!(flags & GRAFT_ERR_NAN), !!(flags & GRAFT_ERR_TREE),
+                         !!(flags & GRAFT_ERR_TIMEOUT));
   return GRAFT_OK;
 }
 

@@ -11,6 +11,7 @@ constexpr int K = 8;            // successors per continuation-matrix row
 constexpr int MAX_S = 64;       // slots per request (one uint64 mask row)
 constexpr int MAX_DRAFT = 256;  // draft nodes per request in one assemble CTA
 constexpr int MAX_SPLIT = 16;   // CTAs per logits row in the verify scan
+constexpr int TMA_CHUNK = 32768; // bytes per pipeline stage of the TMA verify scan
 
 // Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth.
 struct TemplateDev {
@@ -49,6 +50,8 @@ struct ScanGeom {
   int32_t tail;       // elements after the last full vector (vec only)
   int32_t nsplit;     // CTAs per row
   int64_t per_cta;    // load slots per CTA
+  int32_t cpr;        // TMA scan: 32 KB chunks per row
+  int64_t row_vec_bytes;  // bytes of a row's full 16-byte vectors
 };
 
 struct VerifyArgs {
@@ -92,6 +95,10 @@ struct WarmArgs {
 // launchers (return cudaGetLastError())
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
+cudaError_t prepare_verify_tma();
+cudaError_t launch_verify_tma(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
+size_t verify_tma_smem_bytes();
+int verify_tma_max_rows(int grid);
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
 cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s);
 

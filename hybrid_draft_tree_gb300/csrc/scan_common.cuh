@@ -1,0 +1,202 @@
+// Device helpers shared by the two verify-scan kernels: 64-bit sort keys
+// (value descending, then token id ascending) and warp-level sorting.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "graft_internal.cuh"
+
+namespace graft {
+namespace scan {
+
+typedef unsigned long long u64;
+constexpr unsigned FULL = 0xffffffffu;
+
+// ---- keys ------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ord_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0 ties with +0
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ u64 make_key(float v, int32_t id) {
+  return ((u64)ord_bits(v) << 32) | (u64)(0xFFFFFFFFu - (uint32_t)id);
+}
+__device__ __forceinline__ int32_t key_id(u64 k) { return k ? (int32_t)(0xFFFFFFFFu - (uint32_t)k) : -1; }
+__device__ __forceinline__ float key_val(u64 k) {
+  const uint32_t o = (uint32_t)(k >> 32);
+  return __uint_as_float((o & 0x80000000u) ? (o ^ 0x80000000u) : ~o);
+}
+// signed-int image of a float with the same order (for warp reductions)
+__device__ __forceinline__ int32_t ord_int(float f) {
+  const int32_t i = __float_as_int(f);
+  return i ^ ((i >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ float from_ord_int(int32_t i) { return __int_as_float(i ^ ((i >> 31) & 0x7FFFFFFF)); }
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// ---- warp helpers ------------------------------------------------------------
+__device__ __forceinline__ u64 bitonic32_desc(u64 key, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const u64 o = __shfl_xor_sync(FULL, key, j);
+      const bool desc = (lane & k) == 0;
+      const bool low = (lane & j) == 0;
+      key = (low == desc) ? (key > o ? key : o) : (key < o ? key : o);
+    }
+  }
+  return key;
+}
+__device__ __forceinline__ u64 warp_max_u64(u64 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const u64 x = __shfl_xor_sync(FULL, v, o);
+    v = x > v ? x : v;
+  }
+  return v;
+}
+
+
+// ---- a 16-byte vector of logits: 8 bf16 or 4 fp32 --------------------------------
+template <int DT> struct Vec16;
+template <> struct Vec16<GRAFT_BF16> {
+  uint4 r;
+  static constexpr int EPL = 8;
+  __device__ __forceinline__ float vmax() const {  // NaN-propagating
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
+    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(&m);
+    return max_nan(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  }
+  __device__ __forceinline__ float elem(int e) const {
+    const uint32_t w = (e < 2) ? r.x : (e < 4) ? r.y : (e < 6) ? r.z : r.w;
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+};
+template <> struct Vec16<GRAFT_F32> {
+  uint4 r;
+  static constexpr int EPL = 4;
+  __device__ __forceinline__ float vmax() const {
+    return max_nan(max_nan(__uint_as_float(r.x), __uint_as_float(r.y)),
+                   max_nan(__uint_as_float(r.z), __uint_as_float(r.w)));
+  }
+  __device__ __forceinline__ float elem(int e) const {
+    return __uint_as_float(e == 0 ? r.x : e == 1 ? r.y : e == 2 ? r.z : r.w);
+  }
+};
+
+template <int DT>
+__device__ __forceinline__ float load_scalar(const char* row, int64_t v) {
+  if (DT == GRAFT_BF16) return __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(row)[v] << 16);
+  return reinterpret_cast<const float*>(row)[v];
+}
+
+// Merge `cnt` candidate keys from shared memory into a warp's running top-8
+// (lanes 0..7 hold it, descending; other lanes hold 0).  Returns the lane's
+// new key.
+__device__ __forceinline__ u64 warp_merge(u64 top, const u64* cand, int cnt, int lane) {
+  u64 key = lane < K ? top : 0ull;
+  int base = 0;
+  do {
+    if (lane >= K) {
+      const int c = base + lane - K;
+      key = c < cnt ? cand[c] : 0ull;
+    }
+    key = bitonic32_desc(key, lane);
+    base += 32 - K;
+  } while (base < cnt);
+  return lane < K ? key : 0ull;
+}
+
+// Merge `cnt` keys read from global memory (L2, bypassing L1) into a top-8.
+__device__ __forceinline__ u64 warp_merge_global(const u64* src, int cnt, int lane) {
+  u64 key = 0ull;
+  int base = 0;
+  bool first = true;
+  do {
+    if (first || lane >= K) {
+      const int c = first ? lane : base + lane - K;
+      key = c < cnt ? __ldcg(src + c) : 0ull;
+    }
+    key = bitonic32_desc(key, lane);
+    base = first ? 32 : base + (32 - K);
+    first = false;
+  } while (base < cnt);
+  return lane < K ? key : 0ull;
+}
+
+// ---- greedy acceptance of request b (one warp) -----------------------------------
+// match(i): slot i is valid and is the root or carries its parent's argmax;
+// accepted(i) <=> every ancestor-or-self of i matches <=> mask_i & ~match == 0.
+// The winner is the accepted slot of greatest position (ties: lower slot);
+// its path tokens after the root, then the bonus token argmax(winner), are
+// emitted.
+static __device__ void accept_request(const VerifyArgs& a, int b, int lane) {
+  const int S = a.S;
+  const size_t base = (size_t)b * S;
+  int32_t tk[2], ps[2];
+  uint64_t mk[2];
+  bool ok[2], mt[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    ok[h] = false; mt[h] = false;
+    tk[h] = -1; ps[h] = -1; mk[h] = 0ull;
+    if (s < S) {
+      tk[h] = a.tree_tok[base + s];
+      if (tk[h] >= 0 && tk[h] < a.g.V) {
+        ps[h] = a.tree_pos[base + s];
+        mk[h] = a.tree_mask[base + s];
+        if (s == 0) {
+          ok[h] = ps[h] == 0;
+          mt[h] = ok[h];
+        } else {
+          const int p = a.tree_parent[base + s];
+          ok[h] = p >= 0 && p < s && a.tree_tok[base + p] >= 0 && ps[h] >= 1 && ps[h] < S;
+          if (ok[h]) mt[h] = tk[h] == __ldcg(a.topk + (base + p) * K);
+        }
+        if (!ok[h]) atomicOr(a.err, GRAFT_ERR_TREE);
+      }
+    }
+  }
+  const uint64_t match = (uint64_t)__ballot_sync(FULL, mt[0]) | ((uint64_t)__ballot_sync(FULL, mt[1]) << 32);
+  int wkey = -1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    if (ok[h] && ((mk[h] >> s) & 1ull) && (mk[h] & ~match) == 0ull) wkey = max(wkey, (ps[h] << 8) | (255 - s));
+  }
+  wkey = __reduce_max_sync(FULL, wkey);
+  int32_t* out = a.out_tokens + base;
+  if (wkey < 0) {  // no valid root: nothing accepted, nothing emitted
+    for (int j = lane; j < S; j += 32) out[j] = -1;
+    if (lane == 0) a.accept_len[b] = 0;
+    return;
+  }
+  const int w = 255 - (wkey & 255);
+  const int L = wkey >> 8;
+  const uint64_t mw = a.tree_mask[base + w];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    if (s > 0 && ok[h] && ((mw >> s) & 1ull) && ps[h] <= L) out[ps[h] - 1] = tk[h];
+  }
+  for (int j = lane; j < S; j += 32)
+    if (j > L) out[j] = -1;
+  if (lane == 0) {
+    out[L] = __ldcg(a.topk + (base + w) * K);
+    a.accept_len[b] = L;
+  }
+}
+
+}  // namespace scan
+}  // namespace graft

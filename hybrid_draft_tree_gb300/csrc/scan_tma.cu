@@ -1,0 +1,408 @@
+// Persistent, TMA-pipelined verify scan for 16-byte aligned logits rows.
+//
+// The verify + update pass of a Graft step (popular-science article on arXiv
+// 2605.20104, section 二 third gear) reads every verified slot's logits row
+// once; this kernel streams those rows at HBM speed.
+//
+// Work: the valid rows are compacted in-kernel and cut into 32 KB chunks;
+// CTA c of G (one per SM) owns the contiguous chunk range [cT/G, (c+1)T/G).
+// Per CTA one producer thread issues cp.async.bulk copies (the 1-D TMA path)
+// into a 6-stage shared-memory ring guarded by mbarriers (full: bytes landed;
+// empty: all consumer warps done), keeping up to 192 KB in flight per SM.
+// Each of the 8 consumer warps takes 1/8 of every chunk from shared memory
+// and keeps its own running top-8 of the current row: elements below the
+// warp's 8th best (or, while it has fewer than 8, below the 8th largest lane
+// maximum of the chunk) are discarded with one compare per 16-byte vector;
+// survivors are merged with a 32-lane bitonic sort on 64-bit keys (value
+// desc, id asc).  At the end of a row segment the 8 warps' lists are merged;
+// a row split over several CTAs is finished by the last of them (atomic
+// ticket), which stages the row's top-8, claims the token's matrix row
+// (atomicMax of row+1) and, if it completes its request, runs the acceptance
+// walk.  Every wait is bounded: on expiry the kernel flags GRAFT_ERR_TIMEOUT,
+// drains its copies in flight and finishes.
+#include <cuda_bf16.h>
+
+#include "graft_internal.cuh"
+#include "scan_common.cuh"
+
+namespace graft {
+namespace {
+using namespace scan;
+
+constexpr int NCW = 8;                  // consumer warps
+constexpr int NCT = NCW * 32;           // consumer threads
+constexpr int TPB = NCT + 32;           // + one producer warp
+constexpr int NSTAGE = 6;
+constexpr int VPL = TMA_CHUNK / 16 / NCT;  // 16-byte vectors per consumer lane per chunk
+constexpr int WCAP = 256;               // candidate keys per warp
+constexpr int MAXROWS = 128;            // rows one CTA may touch
+constexpr uint32_t SPIN = 1u << 24;     // try_wait polls before a wait gives up
+
+struct TmaSmem {
+  u64 full[NSTAGE];
+  u64 empty[NSTAGE];
+  u64 wcand[NCW][WCAP];
+  u64 segtop[2][NCW][K];
+  int wcnt[NCW];
+  int rowlist[MAXROWS];
+  int warpsum[TPB / 32];
+  int abort_flag;
+};
+constexpr size_t SMEM_BYTES = (size_t)NSTAGE * TMA_CHUNK + sizeof(TmaSmem);
+
+// ---- mbarrier / bulk-copy primitives (inline PTX) ---------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(u64* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(u64* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(u64* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(u64* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// one thread, bounded
+__device__ __forceinline__ bool mbar_wait(u64* bar, uint32_t parity) {
+  for (uint32_t it = 0; it < SPIN; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// whole warp, bounded, warp-uniform result
+__device__ __forceinline__ bool mbar_wait_warp(u64* bar, uint32_t parity) {
+  bool ok = false;
+  for (uint32_t it = 0; it < SPIN; ++it) {
+    ok = mbar_try_wait(bar, parity);
+    if (__all_sync(FULL, ok)) return true;
+  }
+  return __all_sync(FULL, ok);
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, u64* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
+
+// CTA owning global chunk i when T chunks are split over G CTAs.
+__device__ __forceinline__ int cta_of(int64_t i, int64_t T, int G) { return (int)(((i + 1) * G - 1) / T); }
+
+// ---- row and request completion (one warp) ---------------------------------------
+__device__ void finish_row(const VerifyArgs& a, int row, u64 key, int lane) {
+  if (lane < K) a.topk[(size_t)row * K + lane] = key_id(key);
+  const int32_t tok = a.tree_tok[row];
+  if (lane == 0) atomicMax(&a.winner[tok], row + 1);
+  __threadfence();
+  __syncwarp();
+  const int S = a.S;
+  const int b = row / S;
+  const size_t base = (size_t)b * S;
+  bool v0 = false, v1 = false;
+  if (lane < S) { const int32_t t = a.tree_tok[base + lane]; v0 = t >= 0 && t < a.g.V; }
+  if (lane + 32 < S) { const int32_t t = a.tree_tok[base + lane + 32]; v1 = t >= 0 && t < a.g.V; }
+  const int nv = __popc(__ballot_sync(FULL, v0)) + __popc(__ballot_sync(FULL, v1));
+  int t = 0;
+  if (lane == 0) t = atomicAdd(&a.req_ticket[b], 1);
+  t = __shfl_sync(FULL, t, 0);
+  if (t == nv - 1) {
+    if (lane == 0) a.req_ticket[b] = 0;
+    __threadfence();
+    accept_request(a, b, lane);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ u64 warp_exact_top8(const Vec16<DT>* v, int nvalid_mask, int64_t vbase, int vl0,
+                                               bool has_tail, float tv, int32_t tail_id, u64 top, int lane) {
+  constexpr int EPL = Vec16<DT>::EPL;
+  u64 prev = ~0ull, out = 0ull;
+  for (int r = 0; r < K; ++r) {
+    u64 best = 0ull;
+#pragma unroll
+    for (int kk = 0; kk < VPL; ++kk) {
+      if (nvalid_mask & (1 << kk)) {
+        const int64_t vid = vbase + vl0 + kk * 32;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const u64 key = make_key(v[kk].elem(e), (int32_t)(vid * EPL + e));
+          if (key < prev && key > best) best = key;
+        }
+      }
+    }
+    if (has_tail) {
+      const u64 key = make_key(tv, tail_id);
+      if (key < prev && key > best) best = key;
+    }
+    if (lane < K && top < prev && top > best) best = top;
+    best = warp_max_u64(best);
+    if (lane == r) out = best;
+    prev = best;
+  }
+  return out;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(TPB, 1) k_verify_tma(VerifyArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* ring = smem_raw;
+  TmaSmem& sm = *reinterpret_cast<TmaSmem*>(smem_raw + (size_t)NSTAGE * TMA_CHUNK);
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  constexpr int EPL = 16 / ES;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const ScanGeom& g = a.g;
+  const int S = a.S;
+  const int rows = a.batch * S;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int cpr = g.cpr;
+
+  // ---- compact the valid rows (same result in every CTA) --------------------------
+  const int per = (rows + TPB - 1) / TPB;
+  const int r0 = min(tid * per, rows), r1 = min(r0 + per, rows);
+  int cnt = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int32_t t = a.tree_tok[r];
+    cnt += (t >= 0 && t < g.V);
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.warpsum[warp] = incl;
+  if (tid == 0) sm.abort_flag = 0;
+  if (tid < NCW) sm.wcnt[tid] = 0;
+  __syncthreads();
+  int wbase = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < TPB / 32; ++w) {
+    const int x = sm.warpsum[w];
+    wbase += (w < warp) ? x : 0;
+    total += x;
+  }
+  const int64_t T = (int64_t)total * cpr;
+  const int64_t i0 = (int64_t)c * T / G, i1 = (int64_t)(c + 1) * T / G;
+  const int64_t k0 = i0 / cpr;
+  const int64_t klast = i1 > i0 ? (i1 - 1) / cpr : k0 - 1;
+  int64_t vidx = wbase + incl - cnt;
+  for (int r = r0; r < r1; ++r) {
+    const int32_t t = a.tree_tok[r];
+    if (t >= 0 && t < g.V) {
+      if (vidx >= k0 && vidx <= klast && vidx - k0 < MAXROWS) sm.rowlist[vidx - k0] = r;
+      ++vidx;
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], NCW);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // requests without any valid slot have no row to finish them: CTA 0 does
+  if (c == 0 && warp == NCW) {
+    for (int b = 0; b < a.batch; ++b) {
+      const size_t base = (size_t)b * S;
+      bool v0 = false, v1 = false;
+      if (lane < S) { const int32_t t = a.tree_tok[base + lane]; v0 = t >= 0 && t < g.V; }
+      if (lane + 32 < S) { const int32_t t = a.tree_tok[base + lane + 32]; v1 = t >= 0 && t < g.V; }
+      if (!__any_sync(FULL, v0 || v1)) accept_request(a, b, lane);
+    }
+  }
+  __syncthreads();
+  if (i1 <= i0) return;
+  if (klast - k0 + 1 > MAXROWS) {  // host keeps rows <= (MAXROWS - 2) * G, so this cannot happen
+    if (tid == 0) atomicOr(a.err, GRAFT_ERR_TREE);
+    return;
+  }
+
+  // ---- producer warp ------------------------------------------------------------
+  if (warp == NCW) {
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int64_t i = i0; i < i1; ++i) {
+        const int64_t j = i - i0;
+        const int s = (int)(j % NSTAGE);
+        const uint32_t use = (uint32_t)(j / NSTAGE);
+        if (use > 0 && !mbar_wait(&sm.empty[s], (use - 1) & 1)) {
+          atomicOr(a.err, GRAFT_ERR_TIMEOUT);
+          *(volatile int*)&sm.abort_flag = 1;
+          break;
+        }
+        if (*(volatile int*)&sm.abort_flag) break;
+        const int64_t k = i / cpr;
+        const int q = (int)(i % cpr);
+        const int row = sm.rowlist[k - k0];
+        const int64_t off = (int64_t)q * TMA_CHUNK;
+        const uint32_t bytes = (uint32_t)min((int64_t)TMA_CHUNK, g.row_vec_bytes - off);
+        const char* src = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)g.stride * ES + off;
+        mbar_expect_tx(&sm.full[s], bytes);
+        bulk_g2s(ring + (size_t)s * TMA_CHUNK, src, bytes, &sm.full[s]);
+        ++issued;
+      }
+      // drain: every copy still in flight lands before this CTA may exit
+      for (int64_t j = issued > NSTAGE ? issued - NSTAGE : 0; j < issued; ++j)
+        mbar_wait(&sm.full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1);
+    }
+    return;
+  }
+
+  // ---- consumer warps -------------------------------------------------------------
+  u64 top = 0ull;
+  float thr = -INFINITY;
+  int64_t cur_k = -1;
+  int nseg_done = 0;
+  bool dead = false;
+  const int vl0 = warp * 32 * VPL + lane;
+
+  auto finish_segment = [&](int64_t k) {
+    const int par = nseg_done & 1;
+    if (lane < K) sm.segtop[par][warp][lane] = top;
+    consumers_sync();
+    ++nseg_done;
+    if (warp != 0) return;
+    u64 key = warp_merge(0ull, &sm.segtop[par][0][0], NCW * K, lane);
+    const int row = sm.rowlist[k - k0];
+    const int first = cta_of(k * cpr, T, G);
+    const int last = cta_of(k * cpr + cpr - 1, T, G);
+    const int nseg = last - first + 1;
+    bool fin = true;
+    if (nseg > 1) {
+      if (lane < K) a.part[((size_t)row * MAX_SPLIT + (c - first)) * K + lane] = key;
+      __threadfence();
+      __syncwarp();
+      int t = 0;
+      if (lane == 0) t = atomicAdd(&a.row_ticket[row], 1);
+      t = __shfl_sync(FULL, t, 0);
+      fin = (t == nseg - 1);
+      if (fin) {
+        if (lane == 0) a.row_ticket[row] = 0;
+        __threadfence();
+        key = warp_merge_global(a.part + (size_t)row * MAX_SPLIT * K, nseg * K, lane);
+      }
+    }
+    if (fin) finish_row(a, row, key, lane);
+  };
+
+  for (int64_t i = i0; i < i1; ++i) {
+    const int64_t j = i - i0;
+    const int s = (int)(j % NSTAGE);
+    const uint32_t use = (uint32_t)(j / NSTAGE);
+    const int64_t k = i / cpr;
+    const int q = (int)(i % cpr);
+    if (k != cur_k) {
+      if (cur_k >= 0) finish_segment(cur_k);
+      top = 0ull;
+      thr = -INFINITY;
+      cur_k = k;
+    }
+    if (!dead) dead = __any_sync(FULL, *(volatile int*)&sm.abort_flag != 0);
+    if (!dead && !mbar_wait_warp(&sm.full[s], use & 1)) {
+      if (lane == 0) {
+        atomicOr(a.err, GRAFT_ERR_TIMEOUT);
+        *(volatile int*)&sm.abort_flag = 1;
+      }
+      dead = true;
+    }
+    if (!dead) {
+      const int64_t off = (int64_t)q * TMA_CHUNK;
+      const int nvec = (int)(min((int64_t)TMA_CHUNK, g.row_vec_bytes - off) / 16);
+      const uint4* stage = reinterpret_cast<const uint4*>(ring + (size_t)s * TMA_CHUNK);
+      Vec16<DT> v[VPL];
+      float vm[VPL];
+      int vmask = 0;
+#pragma unroll
+      for (int kk = 0; kk < VPL; ++kk) {
+        const int vl = vl0 + kk * 32;
+        if (vl < nvec) {
+          v[kk].r = stage[vl];
+          vm[kk] = v[kk].vmax();
+          vmask |= 1 << kk;
+        } else {
+          vm[kk] = -INFINITY;
+        }
+      }
+      const int row = sm.rowlist[k - k0];
+      const bool has_tail = (q == cpr - 1) && warp == 0 && lane < g.tail;
+      const int32_t tail_id = (int32_t)(g.nslot * EPL + lane);
+      const float tv = has_tail
+          ? load_scalar<DT>(reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)g.stride * ES, tail_id)
+          : -INFINITY;
+      float lmax = tv;
+#pragma unroll
+      for (int kk = 0; kk < VPL; ++kk) lmax = max_nan(lmax, vm[kk]);
+      if (lmax != lmax) atomicOr(a.err, GRAFT_ERR_NAN);
+      float T8 = thr;
+      if (T8 == -INFINITY) {  // fewer than 8 kept: the 8th largest lane maximum bounds the top-8
+        u64 lk = make_key(lmax, lane);
+        lk = bitonic32_desc(lk, lane);
+        const u64 k8 = __shfl_sync(FULL, lk, K - 1);
+        T8 = key_val(k8);
+      }
+      const int64_t vbase = (int64_t)q * (TMA_CHUNK / 16);
+#pragma unroll
+      for (int kk = 0; kk < VPL; ++kk) {
+        if (vm[kk] >= T8) {
+          const int64_t vid = vbase + vl0 + kk * 32;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            const float x = v[kk].elem(e);
+            if (x >= T8) {
+              const int idx = atomicAdd(&sm.wcnt[warp], 1);
+              if (idx < WCAP) sm.wcand[warp][idx] = make_key(x, (int32_t)(vid * EPL + e));
+            }
+          }
+        }
+      }
+      if (has_tail && tv >= T8) {
+        const int idx = atomicAdd(&sm.wcnt[warp], 1);
+        if (idx < WCAP) sm.wcand[warp][idx] = make_key(tv, tail_id);
+      }
+      __syncwarp();
+      const int cw = *(volatile int*)&sm.wcnt[warp];
+      if (cw > 0) {
+        if (cw <= WCAP) top = warp_merge(top, sm.wcand[warp], cw, lane);
+        else top = warp_exact_top8<DT>(v, vmask, vbase, vl0, has_tail, tv, tail_id, top, lane);
+        const u64 k8 = __shfl_sync(FULL, top, K - 1);
+        thr = k8 ? key_val(k8) : -INFINITY;
+        __syncwarp();
+        if (lane == 0) sm.wcnt[warp] = 0;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+  }
+  if (cur_k >= 0) finish_segment(cur_k);
+}
+
+template <int DT>
+cudaError_t verify_tma_impl(const VerifyArgs& a, int grid, cudaStream_t s) {
+  k_verify_tma<DT><<<grid, TPB, SMEM_BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t verify_tma_smem_bytes() { return SMEM_BYTES; }
+int verify_tma_max_rows(int grid) { return (MAXROWS - 2) * grid; }
+
+cudaError_t prepare_verify_tma() {
+  cudaError_t e = cudaFuncSetAttribute(k_verify_tma<GRAFT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_verify_tma<GRAFT_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  return e;
+}
+
+cudaError_t launch_verify_tma(const VerifyArgs& a, int dtype, int grid, cudaStream_t s) {
+  return dtype == GRAFT_BF16 ? verify_tma_impl<GRAFT_BF16>(a, grid, s) : verify_tma_impl<GRAFT_F32>(a, grid, s);
+}
+
+}  // namespace graft

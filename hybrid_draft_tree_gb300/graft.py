@@ -16,7 +16,7 @@ import numpy as np
 from . import _build
 
 GRAFT_OK, GRAFT_EINVAL, GRAFT_ENOMEM, GRAFT_ECUDA, GRAFT_EDEVICE = 0, -1, -2, -3, -4
-GRAFT_ERR_TOKEN, GRAFT_ERR_NAN, GRAFT_ERR_TREE = 1, 2, 4
+GRAFT_ERR_TOKEN, GRAFT_ERR_NAN, GRAFT_ERR_TREE, GRAFT_ERR_TIMEOUT = 1, 2, 4, 8
 GRAFT_MODE_CHECKPOINT, GRAFT_MODE_STATIC, GRAFT_MODE_TAIL = 0, 1, 2
 GRAFT_F32, GRAFT_BF16 = 0, 1
 K = 8
@@ -38,7 +38,8 @@ class graft_config(ctypes.Structure):
                 ("max_batch", ctypes.c_int32), ("mode", ctypes.c_int32), ("logits_dtype", ctypes.c_int32),
                 ("ckpt_depth", ctypes.c_int32 * 3), ("ckpt_thr", ctypes.c_float * 3),
                 ("ckpt_draft", ctypes.c_int32 * 3), ("tpl_depth", ctypes.c_int32), ("tpl_width", ctypes.c_int32),
-                ("static_thr", ctypes.c_float), ("tail_thr", ctypes.c_float), ("max_draft_nodes", ctypes.c_int32)]
+                ("static_thr", ctypes.c_float), ("tail_thr", ctypes.c_float), ("max_draft_nodes", ctypes.c_int32),
+                ("scan_kernel", ctypes.c_int32)]
 
 
 _lib = None

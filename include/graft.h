@@ -57,6 +57,7 @@ typedef enum {
 #define GRAFT_ERR_TOKEN 1u   /* a token id outside [0, V) (input or matrix) */
 #define GRAFT_ERR_NAN 2u     /* NaN in a logits row or a draft probability */
 #define GRAFT_ERR_TREE 4u    /* parent index not before its child, bad position */
+#define GRAFT_ERR_TIMEOUT 8u /* a bounded wait inside a kernel expired; that call's results are invalid */
 
 typedef enum {
   GRAFT_MODE_CHECKPOINT = 0, /* article §二: checkpoints at depths 0/1/5 */
@@ -81,6 +82,8 @@ typedef struct {
   float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15) */
   float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4) */
   int32_t max_draft_nodes;/* largest draft tree (<= 256) or block (<= budget) per request */
+  int32_t scan_kernel;    /* verify scan: 0 = automatic, 1 = register-tiled, 2 = TMA-pipelined
+                             (used only for 16-byte aligned rows of >= 32 KB; else register-tiled) */
 } graft_config;
 
 /* Fill *cfg with the paper's defaults for `mode` and vocabulary V. */

@@ -36,7 +36,7 @@ def test_library_loads_and_exports_every_declared_symbol():
 def test_config_struct_layout_and_defaults():
     import hybrid_draft_tree_gb300 as g
     cfg = g.graft_default_config(151936, 16, g.GRAFT_MODE_STATIC, g.GRAFT_BF16)
-    assert ctypes.sizeof(cfg) == 4 * 20
+    assert ctypes.sizeof(cfg) == 4 * 21
     assert (cfg.vocab, cfg.topk, cfg.budget, cfg.max_batch) == (151936, 8, 60, 16)
     assert list(cfg.ckpt_depth) == [0, 1, 5]
     assert [round(x, 6) for x in cfg.ckpt_thr] == [0.3, 0.2, 0.1]

@@ -56,10 +56,10 @@ def assert_trees_equal(loop, trees, step):
         assert np.array_equal(gi[b], tr.info), (step, b, "info", gi[b], tr.info)
 
 
-def lockstep(w, steps, warm=False, check_rows=0, stats=None):
+def lockstep(w, steps, warm=False, check_rows=0, stats=None, **cfg):
     """Run the GPU closed loop and the oracle side by side; compare all."""
     from workloads.device_loop import DeviceLoop
-    g = engine_for(w)
+    g = engine_for(w, **cfg)
     loop = DeviceLoop(w, g)
     P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
     C = oracle.new_matrix(w.V)
@@ -155,6 +155,30 @@ def test_lockstep_small(wid, V, B, sigma, steps):
     assert any(a > 0 for _, a in stats)
 
 
+@pytest.mark.parametrize("scan_kernel", [1, 2])
+@pytest.mark.parametrize("wid,V,B,sigma,steps", [
+    (2, 40000, 16, 2.0, 8),     # static, 80 KB rows: 3 chunks per row, rows split over CTAs
+    (4, 24576, 64, 2.0, 6),     # tail, 64 requests x 17 slots
+    (0, 16384, 1, 0.75, 20),    # fp32 checkpoint, 64 KB rows, few rows per step
+])
+def test_lockstep_both_scan_kernels(scan_kernel, wid, V, B, sigma, steps):
+    """The register-tiled and the TMA-pipelined verify scans on rows of
+    >= 32 KB, closed loop against the oracle."""
+    w = W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=sigma)
+    lockstep(w, steps, check_rows=4, scan_kernel=scan_kernel)
+
+
+@pytest.mark.parametrize("scan_kernel", [1, 2])
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("V,pad,fn", [(40000, 0, "normal"), (40003, 5, "normal"), (65536, 0, "ties"),
+                                      (33000, 0, "constant")])
+def test_verify_scan_kernels(scan_kernel, dtype, V, pad, fn):
+    """Both scans on aligned rows: ragged tails (V % 8 != 0 with a padded
+    stride), heavy ties, all-equal rows (candidate overflow)."""
+    fns = {"normal": _normal, "ties": _ties, "constant": _constant}
+    _verify_case(V, dtype, 61, 3, fns[fn], stride_pad=pad, seed=V + pad, scan_kernel=scan_kernel)
+
+
 @pytest.mark.parametrize("wid", [1, 3])
 def test_lockstep_warmup_small(wid):
     base = W.WORKLOADS[wid]
@@ -237,7 +261,7 @@ def _tree_from_parents(tok, par):
     return t
 
 
-def _verify_case(V, dtype, S, B, rows_fn, stride_pad=0, seed=0, offset_elems=0):
+def _verify_case(V, dtype, S, B, rows_fn, stride_pad=0, seed=0, offset_elems=0, scan_kernel=0):
     """Random trees over rows_fn(rng, n, V) logits, each node following its
     parent's argmax with probability 1/2; GPU verify_update vs the oracle."""
     g_ = G()
@@ -264,7 +288,8 @@ def _verify_case(V, dtype, S, B, rows_fn, stride_pad=0, seed=0, offset_elems=0):
     buf[offset_elems:].reshape(B * S, stride)[:, :V] = host_rows
     dev = u16_to_bf16_tensor(buf) if dtype == W.BF16 else torch.from_numpy(buf).cuda()
     logits = dev[offset_elems:].view(B * S, stride)
-    cfg = g_.graft_default_config(V, B, 0, dtype, budget=S - 1, ckpt_draft=(min(8, S - 1), min(24, S - 1), min(40, S - 1)))
+    cfg = g_.graft_default_config(V, B, 0, dtype, budget=S - 1, scan_kernel=scan_kernel,
+                                  ckpt_draft=(min(8, S - 1), min(24, S - 1), min(40, S - 1)))
     eng = g_.Graft(cfg)
     tt = torch.from_numpy(np.stack([t.tok for t in trees])).cuda()
     tp = torch.from_numpy(np.stack([t.par for t in trees]).astype(np.int8)).cuda()
