@@ -26,6 +26,7 @@ struct graft_handle {
   int32_t* row_ticket = nullptr;  // [rows]
   int32_t* req_ticket = nullptr;  // [max_batch]
   int32_t* topk = nullptr;        // [rows][8]
+  int32_t* row_nseg = nullptr;    // [rows]
   int32_t* list = nullptr;        // [V] warm-up rows
   int32_t* count = nullptr;       // [1]
   uint32_t* err = nullptr;        // [1]
@@ -99,7 +100,7 @@ cudaError_t dalloc(T** p, size_t n) {
 
 void free_all(graft_handle* h) {
   cudaFree(h->C); cudaFree(h->winner); cudaFree(h->tpl); cudaFree(h->part);
-  cudaFree(h->row_ticket); cudaFree(h->req_ticket); cudaFree(h->topk);
+  cudaFree(h->row_ticket); cudaFree(h->req_ticket); cudaFree(h->topk); cudaFree(h->row_nseg);
   cudaFree(h->list); cudaFree(h->count); cudaFree(h->err);
 }
 
@@ -197,6 +198,7 @@ int graft_init(const graft_config* cfg, graft_handle** out) {
   if (e == cudaSuccess) e = dalloc(&h->row_ticket, rows);
   if (e == cudaSuccess) e = dalloc(&h->req_ticket, (size_t)cfg->max_batch);
   if (e == cudaSuccess) e = dalloc(&h->topk, rows * graft::K);
+  if (e == cudaSuccess) e = dalloc(&h->row_nseg, rows);
   if (e == cudaSuccess) e = dalloc(&h->list, V);
   if (e == cudaSuccess) e = dalloc(&h->count, 1);
   if (e == cudaSuccess) e = dalloc(&h->err, 1);
@@ -314,17 +316,19 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
   a.tree_tok = d_tree_tok; a.tree_parent = d_tree_parent; a.tree_pos = d_tree_pos; a.tree_mask = d_tree_mask;
   a.accept_len = d_accept_len; a.out_tokens = d_out_tokens;
   a.part = h->part; a.row_ticket = h->row_ticket; a.req_ticket = h->req_ticket; a.topk = h->topk;
-  a.winner = h->winner; a.err = h->err;
+  a.winner = h->winner; a.err = h->err; a.row_nseg = h->row_nseg;
   const bool tma_fits = h->tma_ready && a.g.vec && a.g.row_vec_bytes >= graft::TMA_CHUNK &&
                         a.g.cpr <= graft::MAX_SPLIT && rows <= graft::verify_tma_max_rows(h->num_sms);
-  const bool use_tma = tma_fits && c.scan_kernel != 1;
+  const bool use_tma = tma_fits && c.scan_kernel == 2;
+  const int grid = h->num_sms * graft::verify_ctas_per_sm();
+  if (!use_tma && rows > graft::verify_max_rows(grid))
+    return fail(h, GRAFT_EINVAL, "batch * (budget + 1) = %lld rows exceeds %d on this GPU", (long long)rows,
+                graft::verify_max_rows(grid));
   cudaError_t e = use_tma ? graft::launch_verify_tma(a, c.logits_dtype, h->num_sms, (cudaStream_t)stream)
-                          : graft::launch_verify(a, c.logits_dtype, (cudaStream_t)stream);
+                          : graft::launch_verify(a, c.logits_dtype, grid, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update scan launch");
-  graft::ScatterArgs x{};
-  x.rows = (int32_t)rows; x.V = c.vocab; x.tree_tok = d_tree_tok; x.topk = h->topk; x.winner = h->winner; x.C = h->C;
-  e = graft::launch_scatter(x, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update scatter launch");
+  e = graft::launch_finish(a, h->C, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update finish launch");
   h->last_launches = 2;
   return GRAFT_OK;
 }

@@ -69,6 +69,7 @@ struct VerifyArgs {
   int32_t* req_ticket;        // [batch]
   int32_t* topk;              // [rows][K] staged top-8 ids
   int32_t* winner;            // [V] last-writer key (row + 1), 0 = none
+  int32_t* row_nseg;          // [rows] number of partial top-8s the scan wrote for the row
   uint32_t* err;
 };
 
@@ -94,12 +95,15 @@ struct WarmArgs {
 
 // launchers (return cudaGetLastError())
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s);
-cudaError_t launch_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_verify(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
+int verify_ctas_per_sm();
+int verify_max_rows(int grid);
 cudaError_t prepare_verify_tma();
 cudaError_t launch_verify_tma(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
 size_t verify_tma_smem_bytes();
 int verify_tma_max_rows(int grid);
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
+cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s);
 cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s);
 
 }  // namespace graft

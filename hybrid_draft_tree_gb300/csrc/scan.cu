@@ -44,6 +44,28 @@ template <int DT> struct Slot<DT, true> : Vec16<DT> {
   __device__ __forceinline__ void load(const char* row, int64_t s) {
     this->r = __ldcs(reinterpret_cast<const uint4*>(row) + s);
   }
+  __device__ __forceinline__ void set_neg_inf() {
+    const uint32_t w = DT == GRAFT_BF16 ? 0xFF80FF80u : 0xFF800000u;
+    this->r = make_uint4(w, w, w, w);
+  }
+  // the n < EPL elements after the last full vector; the rest read as -inf
+  __device__ __forceinline__ void load_tail(const char* row, int64_t first, int n) {
+    uint32_t w[4];
+    if (DT == GRAFT_BF16) {
+      const unsigned short* p = reinterpret_cast<const unsigned short*>(row) + first;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = (2 * i < n) ? p[2 * i] : 0xFF80u;
+        const uint32_t hi = (2 * i + 1 < n) ? p[2 * i + 1] : 0xFF80u;
+        w[i] = lo | (hi << 16);
+      }
+    } else {
+      const uint32_t* p = reinterpret_cast<const uint32_t*>(row) + first;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = (i < n) ? p[i] : 0xFF800000u;
+    }
+    this->r = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 };
 template <> struct Slot<GRAFT_BF16, false> {
   uint32_t r;
@@ -53,6 +75,8 @@ template <> struct Slot<GRAFT_BF16, false> {
   }
   __device__ __forceinline__ float vmax() const { return __uint_as_float(r); }
   __device__ __forceinline__ float elem(int) const { return __uint_as_float(r); }
+  __device__ __forceinline__ void load_tail(const char*, int64_t, int) { r = 0xFF800000u; }
+  __device__ __forceinline__ void set_neg_inf() { r = 0xFF800000u; }
 };
 template <> struct Slot<GRAFT_F32, false> {
   uint32_t r;
@@ -62,6 +86,8 @@ template <> struct Slot<GRAFT_F32, false> {
   }
   __device__ __forceinline__ float vmax() const { return __uint_as_float(r); }
   __device__ __forceinline__ float elem(int) const { return __uint_as_float(r); }
+  __device__ __forceinline__ void load_tail(const char*, int64_t, int) { r = 0xFF800000u; }
+  __device__ __forceinline__ void set_neg_inf() { r = 0xFF800000u; }
 };
 
 // Shared state of one CTA's running top-8.
@@ -210,82 +236,253 @@ __device__ __forceinline__ void init_top(ScanSmem& sm) {
   if (threadIdx.x == 0) { sm.thr = -INFINITY; sm.cnt = 0; }
 }
 
-// ---- verify + update scan ----------------------------------------------------
+// ---- verify + update scan: plain loads, one running top-8 per warp ----------------
+// A persistent grid (VCPS CTAs per SM) splits the concatenated valid rows into
+// equal contiguous slices.  Within a row segment every warp takes units of 32
+// x VNV load slots, keeps the next unit's loads in flight while it filters the
+// current one against its own threshold, and merges the rare survivors into
+// its own top-8; the CTA syncs once per row segment to merge its 8 warps.
+constexpr int VT = 256;
+constexpr int VW = VT / 32;
+constexpr int VNV = 4;
+constexpr int VUNIT = 32 * VNV;
+constexpr int VMAXROWS = 192;
+constexpr int VSEGS = 24;     // row segments streamed between two CTA barriers
+#ifndef GRAFT_VERIFY_CTAS_PER_SM
+#define GRAFT_VERIFY_CTAS_PER_SM 4
+#endif
+constexpr int VCPS = GRAFT_VERIFY_CTAS_PER_SM;
+
+struct VSmem {
+  u64 top8[VSEGS][K];  // the CTA's running top-8 of each row segment of the group
+  int warpsum[VW];
+  int rowlist[VMAXROWS];
+};
+
+// Load one unit: slot s = base + kk*32 + lane for kk < VNV; slots at or past
+// `end` (the segment end, never beyond the row's last full vector) read -inf.
+// Full units (all but the last of a segment) take unconditional loads.
 template <int DT, bool VEC>
-__global__ __launch_bounds__(ST) void k_verify(VerifyArgs a) {
-  __shared__ ScanSmem sm;
-  const int split = blockIdx.x;
-  const int row = blockIdx.y;
-  const int S = a.S;
-  const int b = row / S;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int esize = DT == GRAFT_BF16 ? 2 : 4;
+__device__ __forceinline__ void load_unit(Slot<DT, VEC> (&v)[VNV], const char* row, int64_t base, int64_t end,
+                                          int lane) {
+  if (base + VUNIT <= end) {
+#pragma unroll
+    for (int kk = 0; kk < VNV; ++kk) v[kk].load(row, base + kk * 32 + lane);
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < VNV; ++kk) {
+      const int64_t s = base + kk * 32 + lane;
+      if (s < end) v[kk].load(row, s);
+      else v[kk].set_neg_inf();
+    }
+  }
+}
+
+// ---- the CTA's running top-8 of a row segment ------------------------------------
+// top8[0..8) in shared memory, descending, 0 = empty.  A key is inserted by
+// offering it to slot 0 with atomicMax and carrying the smaller of (offered,
+// previous) down to the next slot.  Slot 0 ends as the largest key ever
+// offered, slot 1 as the largest of everything carried out of slot 0 (all keys
+// but one), and so on: at any time the slots hold the exact top-8 of the keys
+// inserted so far, lock-free.  Slot 7's value is the filter threshold every
+// warp of the CTA reads.
+__device__ __forceinline__ void top8_insert(u64* top8, u64 k) {
+#pragma unroll 1
+  for (int i = 0; i < K && k; ++i) {
+    const u64 old = atomicMax(&top8[i], k);
+    if (old < k) k = old;
+    if (k < *(volatile u64*)&top8[K - 1]) return;  // can no longer enter
+  }
+}
+
+__device__ __forceinline__ float top8_threshold(const u64* top8) {
+  const u64 k8 = *(volatile const u64*)&top8[K - 1];
+  return k8 ? key_val(k8) : -INFINITY;
+}
+
+// Insert the elements of one slot that beat the CTA's current 8th key (rare).
+template <int DT, bool VEC>
+__device__ __noinline__ void insert_slot(Slot<DT, VEC> v, int64_t vid, float T, u64* top8) {
+  constexpr int EPL = Slot<DT, VEC>::EPL;
+#pragma unroll 1
+  for (int e = 0; e < EPL; ++e) {
+    const float x = v.elem(e);
+    if (x >= T) {
+      const u64 key = make_key(x, (int32_t)(vid * EPL + e));
+      if (key > *(volatile u64*)&top8[K - 1]) top8_insert(top8, key);
+    }
+  }
+}
+
+// Filter one unit.  The CTA's threshold is read from shared memory once per
+// unit and broadcast (lanes may arrive at different times after the inserts
+// of an earlier unit, and all must take the same branches); the common case is
+// the vector maxima, that read and one vote.  Survivors (rare) are inserted
+// into the CTA's top-8.
+template <int DT, bool VEC>
+__device__ __forceinline__ void process_unit(const Slot<DT, VEC> (&v)[VNV], int64_t base, int64_t end, u64* top8,
+                                             uint32_t* err, int lane) {
+  float vm[VNV];
+  float lmax = -INFINITY;
+#pragma unroll
+  for (int kk = 0; kk < VNV; ++kk) {
+    vm[kk] = v[kk].vmax();
+    lmax = max_nan(lmax, vm[kk]);
+  }
+  float T = __shfl_sync(FULL, top8_threshold(top8), 0);
+  if (!__any_sync(FULL, !(lmax < T))) return;  // nothing reaches T, no NaN
+  if (lmax != lmax) atomicOr(err, GRAFT_ERR_NAN);
+  if (T == -INFINITY) T = eighth_lane_max(lmax, lane);  // top-8 not full yet: 8 lane maxima reach T
+#pragma unroll
+  for (int kk = 0; kk < VNV; ++kk) {
+    const int64_t sl = base + kk * 32 + lane;
+    if (vm[kk] >= T && sl < end) insert_slot<DT, VEC>(v[kk], sl, T, top8);
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ int owner_of(int64_t i, int64_t N, int G) { return (int)(((i + 1) * G - 1) / N); }
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(VT, VCPS) k_verify(VerifyArgs a) {
+  __shared__ VSmem sm;
+  using SlotT = Slot<DT, VEC>;
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const ScanGeom& g = a.g;
+  const int rows = a.batch * a.S;
+  const int64_t nslot = g.nslot;
+  const int64_t npr = nslot + (g.tail > 0 ? 1 : 0);  // load slots per row (+1 for the tail)
 
-  const int32_t tok = a.tree_tok[row];
-  const bool valid = tok >= 0 && tok < g.V;
-  if (tid == 0 && split == 0 && tok >= g.V) atomicOr(a.err, GRAFT_ERR_TOKEN);
-
-  init_top(sm);
-  __syncthreads();
-  if (valid) {
-    const char* rowp = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)g.stride * esize;
-    const int64_t s0 = (int64_t)split * g.per_cta;
-    const int64_t s1 = min(s0 + g.per_cta, g.nslot);
-    const bool owns_tail = split == g.nsplit - 1 && g.tail > 0;
-    scan_range<DT, VEC>(rowp, s0, s1, g.nslot * g.epl, owns_tail ? g.tail : 0, sm, a.err);
+  // compact the valid rows (same result in every CTA)
+  const int per = (rows + VT - 1) / VT;
+  const int r0 = min(tid * per, rows), r1 = min(r0 + per, rows);
+  int cnt = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int32_t t = a.tree_tok[r];
+    cnt += (t >= 0 && t < g.V);
+    if (t >= g.V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
   }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.warpsum[warp] = incl;
+  __syncthreads();
+  int wbase = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < VW; ++w) {
+    const int x = sm.warpsum[w];
+    wbase += (w < warp) ? x : 0;
+    total += x;
+  }
+  const int64_t N = (int64_t)total * npr;
+  if (N == 0) return;
+  // effective grid: every CTA owns >= min_per slots, so a row spans <= MAX_SPLIT CTAs
+  const int64_t min_per = (npr + MAX_SPLIT - 2) / (MAX_SPLIT - 1);
+  const int Ge = (int)max((int64_t)1, min((int64_t)gridDim.x, N / min_per));
+  const int c = blockIdx.x;
+  if (c >= Ge) return;
+  const int64_t s0 = (int64_t)c * N / Ge, s1 = (int64_t)(c + 1) * N / Ge;
+  const int64_t k0 = s0 / npr, klast = (s1 - 1) / npr;
+  if (klast - k0 + 1 > VMAXROWS) {  // the host keeps rows <= (VMAXROWS - 2) * grid
+    if (tid == 0) atomicOr(a.err, GRAFT_ERR_TREE);
+    return;
+  }
+  int64_t vidx = wbase + incl - cnt;
+  for (int r = r0; r < r1; ++r) {
+    const int32_t t = a.tree_tok[r];
+    if (t >= 0 && t < g.V) {
+      if (vidx >= k0 && vidx <= klast) sm.rowlist[vidx - k0] = r;
+      ++vidx;
+    }
+  }
+  __syncthreads();
 
-  if (g.nsplit > 1) {
-    if (valid && tid < K) a.part[((size_t)row * MAX_SPLIT + split) * K + tid] = sm.top[tid];
-    __threadfence();
+  // Stream the CTA's row segments in groups of VSEGS.  Inside a group no warp
+  // waits for another: each keeps its own top-8 per segment and filters
+  // against the segment's shared threshold.  After the group, the segments
+  // are finished by different warps in parallel.
+  for (int64_t g0 = k0; g0 <= klast; g0 += VSEGS) {
+    const int nsg = (int)min((int64_t)VSEGS, klast - g0 + 1);
+    for (int i = tid; i < VSEGS * K; i += VT) (&sm.top8[0][0])[i] = 0ull;
     __syncthreads();
-    if (tid == 0) {
-      const int t = atomicAdd(&a.row_ticket[row], 1);
-      sm.flag = (t == g.nsplit - 1);
-      if (sm.flag) a.row_ticket[row] = 0;
+    for (int j = 0; j < nsg; ++j) {
+      const int64_t k = g0 + j;
+      const int row = sm.rowlist[k - k0];
+      const int64_t lo = max(s0, k * npr) - k * npr, hi = min(s1, (k + 1) * npr) - k * npr;
+      const char* rowp = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)g.stride * ES;
+      u64* top8 = sm.top8[j];
+      const int64_t vhi = min(hi, nslot);  // vector slots of this segment: [lo, vhi)
+      const int64_t nunits = vhi > lo ? (vhi - lo + VUNIT - 1) / VUNIT : 0;
+      for (int64_t u = warp; u < nunits; u += VW) {
+        SlotT v[VNV];
+        load_unit<DT, VEC>(v, rowp, lo + u * VUNIT, vhi, lane);
+        process_unit<DT, VEC>(v, lo + u * VUNIT, vhi, top8, a.err, lane);
+      }
+      if (warp == VW - 1 && hi > nslot && lane < g.tail) {  // the row's last V % EPL elements
+        constexpr int EPLc = SlotT::EPL;
+        const int32_t id = (int32_t)(nslot * EPLc + lane);
+        const float x = load_scalar<DT>(rowp, id);
+        if (x != x) atomicOr(a.err, GRAFT_ERR_NAN);
+        else top8_insert(top8, make_key(x, id));
+      }
     }
     __syncthreads();
-    if (!sm.flag) return;
-    __threadfence();
-    if (valid && tid < 32) {
-      // merge the row's nsplit partial top-8s (<= 128 keys)
-      const u64* p = a.part + (size_t)row * MAX_SPLIT * K;
-      const int cnt = g.nsplit * K;
-      u64 key = 0ull;
-      int base = 0;
-      bool first = true;
-      do {
-        if (first || lane >= K) {
-          const int c = first ? lane : base + lane - K;
-          key = c < cnt ? __ldcg(p + c) : 0ull;
-        }
-        key = bitonic32_desc(key, lane);
-        base = first ? 32 : base + (32 - K);
-        first = false;
-      } while (base < cnt);
-      if (lane < K) sm.top[lane] = key;
+    // hand the segments' top-8s to the finishing kernel: partial `c - first`
+    // of the row's `last - first + 1`
+    for (int i = tid; i < nsg * K; i += VT) {
+      const int j = i / K, e = i % K;
+      const int64_t k = g0 + j;
+      const int row = sm.rowlist[k - k0];
+      const int first = owner_of(k * npr, N, Ge);
+      a.part[((size_t)row * MAX_SPLIT + (c - first)) * K + e] = sm.top8[j][e];
+      if (e == 0 && c == first) a.row_nseg[row] = owner_of(k * npr + npr - 1, N, Ge) - first + 1;
     }
     __syncthreads();
   }
+}
 
-  // this CTA finishes the row: stage its top-8 and claim the matrix row
-  if (valid) {
-    if (tid < K) a.topk[(size_t)row * K + tid] = key_id(sm.top[tid]);
-    if (tid == 0) atomicMax(&a.winner[tok], row + 1);
+// ---- finishing: one CTA per request ---------------------------------------------
+// Warps merge the request's rows (each row's partial top-8s from the scan) and
+// stage them; after one barrier warp 0 runs the acceptance walk; then every
+// valid row writes its top-8 into the continuation matrix unless a later row
+// (in (request, slot) order, any request) carries the same token: the last
+// writer wins without a global winner table or a second kernel.
+constexpr int FT = 1024;
+constexpr int FW = FT / 32;
+__global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x, S = a.S;
+  const int rows = a.batch * S;
+  u64 keys[(MAX_S + FW - 1) / FW];
+#pragma unroll
+  for (int h = 0; h < (MAX_S + FW - 1) / FW; ++h) {
+    const int i = warp + h * FW;
+    keys[h] = 0ull;
+    if (i >= S) continue;
+    const int row = b * S + i;
+    const int32_t t = a.tree_tok[row];
+    if (t < 0 || t >= a.g.V) continue;
+    const int nseg = min(max(a.row_nseg[row], 1), MAX_SPLIT);
+    keys[h] = warp_merge_global(a.part + (size_t)row * MAX_SPLIT * K, nseg * K, lane);
+    if (lane < K) a.topk[(size_t)row * K + lane] = key_id(keys[h]);
   }
-  __threadfence();
   __syncthreads();
-  if (tid == 0) {
-    const int t = atomicAdd(&a.req_ticket[b], 1);
-    sm.flag = (t == S - 1);
-    if (sm.flag) a.req_ticket[b] = 0;
+  if (warp == 0) accept_request(a, b, lane);
+#pragma unroll
+  for (int h = 0; h < (MAX_S + FW - 1) / FW; ++h) {
+    const int i = warp + h * FW;
+    if (i >= S) continue;
+    const int row = b * S + i;
+    const int32_t t = a.tree_tok[row];
+    if (t < 0 || t >= a.g.V) continue;
+    bool later = false;
+    for (int r = row + 1 + lane; r < rows; r += 32) later |= (a.tree_tok[r] == t);
+    if (!__any_sync(FULL, later) && lane < K) C[(size_t)t * K + lane] = key_id(keys[h]);
   }
-  __syncthreads();
-  if (!sm.flag || tid >= 32) return;
-  __threadfence();
-
-  accept_request(a, b, lane);
 }
 
 // ---- last-writer scatter into the matrix -------------------------------------
@@ -347,9 +544,8 @@ __global__ void k_warm_reset(WarmArgs a) {
 }
 
 template <int DT, bool VEC>
-cudaError_t verify_impl(const VerifyArgs& a, cudaStream_t s) {
-  dim3 grid(a.g.nsplit, a.batch * a.S);
-  k_verify<DT, VEC><<<grid, ST, 0, s>>>(a);
+cudaError_t verify_impl(const VerifyArgs& a, int grid, cudaStream_t s) {
+  k_verify<DT, VEC><<<grid, VT, 0, s>>>(a);
   return cudaGetLastError();
 }
 template <int DT, bool VEC>
@@ -365,9 +561,16 @@ cudaError_t warm_impl(const WarmArgs& a, int grid_ctas, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_verify(const VerifyArgs& a, int dtype, cudaStream_t s) {
-  if (dtype == GRAFT_BF16) return a.g.vec ? verify_impl<GRAFT_BF16, true>(a, s) : verify_impl<GRAFT_BF16, false>(a, s);
-  return a.g.vec ? verify_impl<GRAFT_F32, true>(a, s) : verify_impl<GRAFT_F32, false>(a, s);
+int verify_ctas_per_sm() { return VCPS; }
+int verify_max_rows(int grid) { return (VMAXROWS - 2) * grid; }
+cudaError_t launch_verify(const VerifyArgs& a, int dtype, int grid, cudaStream_t s) {
+  if (dtype == GRAFT_BF16)
+    return a.g.vec ? verify_impl<GRAFT_BF16, true>(a, grid, s) : verify_impl<GRAFT_BF16, false>(a, grid, s);
+  return a.g.vec ? verify_impl<GRAFT_F32, true>(a, grid, s) : verify_impl<GRAFT_F32, false>(a, grid, s);
+}
+cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
+  k_finish<<<a.batch, FT, 0, s>>>(a, C);
+  return cudaGetLastError();
 }
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
   k_scatter<<<1, XT, 0, s>>>(a);

@@ -36,7 +36,7 @@ constexpr int NSTAGE = 6;
 constexpr int VPL = TMA_CHUNK / 16 / NCT;  // 16-byte vectors per consumer lane per chunk
 constexpr int WCAP = 256;               // candidate keys per warp
 constexpr int MAXROWS = 128;            // rows one CTA may touch
-constexpr uint32_t SPIN = 1u << 24;     // try_wait polls before a wait gives up
+constexpr uint32_t SPIN = 1u << 22;     // try_wait polls before a wait gives up
 
 struct TmaSmem {
   u64 full[NSTAGE];
@@ -94,30 +94,6 @@ __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;
 // CTA owning global chunk i when T chunks are split over G CTAs.
 __device__ __forceinline__ int cta_of(int64_t i, int64_t T, int G) { return (int)(((i + 1) * G - 1) / T); }
 
-// ---- row and request completion (one warp) ---------------------------------------
-__device__ void finish_row(const VerifyArgs& a, int row, u64 key, int lane) {
-  if (lane < K) a.topk[(size_t)row * K + lane] = key_id(key);
-  const int32_t tok = a.tree_tok[row];
-  if (lane == 0) atomicMax(&a.winner[tok], row + 1);
-  __threadfence();
-  __syncwarp();
-  const int S = a.S;
-  const int b = row / S;
-  const size_t base = (size_t)b * S;
-  bool v0 = false, v1 = false;
-  if (lane < S) { const int32_t t = a.tree_tok[base + lane]; v0 = t >= 0 && t < a.g.V; }
-  if (lane + 32 < S) { const int32_t t = a.tree_tok[base + lane + 32]; v1 = t >= 0 && t < a.g.V; }
-  const int nv = __popc(__ballot_sync(FULL, v0)) + __popc(__ballot_sync(FULL, v1));
-  int t = 0;
-  if (lane == 0) t = atomicAdd(&a.req_ticket[b], 1);
-  t = __shfl_sync(FULL, t, 0);
-  if (t == nv - 1) {
-    if (lane == 0) a.req_ticket[b] = 0;
-    __threadfence();
-    accept_request(a, b, lane);
-  }
-}
-
 template <int DT>
 __device__ __forceinline__ u64 warp_exact_top8(const Vec16<DT>* v, int nvalid_mask, int64_t vbase, int vl0,
                                                bool has_tail, float tv, int32_t tail_id, u64 top, int lane) {
@@ -169,6 +145,7 @@ __global__ void __launch_bounds__(TPB, 1) k_verify_tma(VerifyArgs a) {
   for (int r = r0; r < r1; ++r) {
     const int32_t t = a.tree_tok[r];
     cnt += (t >= 0 && t < g.V);
+    if (t >= g.V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
   }
   int incl = cnt;
 #pragma unroll
@@ -207,15 +184,6 @@ __global__ void __launch_bounds__(TPB, 1) k_verify_tma(VerifyArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // requests without any valid slot have no row to finish them: CTA 0 does
-  if (c == 0 && warp == NCW) {
-    for (int b = 0; b < a.batch; ++b) {
-      const size_t base = (size_t)b * S;
-      bool v0 = false, v1 = false;
-      if (lane < S) { const int32_t t = a.tree_tok[base + lane]; v0 = t >= 0 && t < g.V; }
-      if (lane + 32 < S) { const int32_t t = a.tree_tok[base + lane + 32]; v1 = t >= 0 && t < g.V; }
-      if (!__any_sync(FULL, v0 || v1)) accept_request(a, b, lane);
-    }
-  }
   __syncthreads();
   if (i1 <= i0) return;
   if (klast - k0 + 1 > MAXROWS) {  // host keeps rows <= (MAXROWS - 2) * G, so this cannot happen
@@ -270,25 +238,19 @@ __global__ void __launch_bounds__(TPB, 1) k_verify_tma(VerifyArgs a) {
     if (warp != 0) return;
     u64 key = warp_merge(0ull, &sm.segtop[par][0][0], NCW * K, lane);
     const int row = sm.rowlist[k - k0];
-    const int first = cta_of(k * cpr, T, G);
-    const int last = cta_of(k * cpr + cpr - 1, T, G);
-    const int nseg = last - first + 1;
-    bool fin = true;
-    if (nseg > 1) {
-      if (lane < K) a.part[((size_t)row * MAX_SPLIT + (c - first)) * K + lane] = key;
-      __threadfence();
-      __syncwarp();
-      int t = 0;
-      if (lane == 0) t = atomicAdd(&a.row_ticket[row], 1);
-      t = __shfl_sync(FULL, t, 0);
-      fin = (t == nseg - 1);
-      if (fin) {
-        if (lane == 0) a.row_ticket[row] = 0;
-        __threadfence();
-        key = warp_merge_global(a.part + (size_t)row * MAX_SPLIT * K, nseg * K, lane);
+    // the row's segments: distinct owners of its chunks (owners never decrease;
+    // CTAs with an empty range own nothing and are skipped)
+    int nseg = 0, myseg = 0, prev_owner = -1;
+    for (int qq = 0; qq < cpr; ++qq) {
+      const int o = cta_of(k * cpr + qq, T, G);
+      if (o != prev_owner) {
+        if (o == c) myseg = nseg;
+        ++nseg;
+        prev_owner = o;
       }
     }
-    if (fin) finish_row(a, row, key, lane);
+    if (lane < K) a.part[((size_t)row * MAX_SPLIT + myseg) * K + lane] = key;
+    if (lane == 0 && myseg == 0) a.row_nseg[row] = nseg;
   };
 
   for (int64_t i = i0; i < i1; ++i) {
