@@ -286,9 +286,17 @@ __device__ __forceinline__ void load_unit(Slot<DT, VEC> (&v)[VNV], const char* r
 // but one), and so on: at any time the slots hold the exact top-8 of the keys
 // inserted so far, lock-free.  Slot 7's value is the filter threshold every
 // warp of the CTA reads.
+// Slots only grow during a segment, so a slot already >= k would pass k on
+// unchanged: the cascade may start at the first slot seen below k.
 __device__ __forceinline__ void top8_insert(u64* top8, u64 k) {
+  int i = 0;
+#pragma unroll
+  for (int j = K - 1; j >= 0; --j)
+    if (*(volatile u64*)&top8[j] < k) i = j;
+    else break;
+  if (*(volatile u64*)&top8[K - 1] >= k) return;  // cannot enter
 #pragma unroll 1
-  for (int i = 0; i < K && k; ++i) {
+  for (; i < K && k; ++i) {
     const u64 old = atomicMax(&top8[i], k);
     if (old < k) k = old;
     if (k < *(volatile u64*)&top8[K - 1]) return;  // can no longer enter
@@ -314,14 +322,16 @@ __device__ __noinline__ void insert_slot(Slot<DT, VEC> v, int64_t vid, float T, 
   }
 }
 
-// Filter one unit.  The CTA's threshold is read from shared memory once per
-// unit and broadcast (lanes may arrive at different times after the inserts
-// of an earlier unit, and all must take the same branches); the common case is
-// the vector maxima, that read and one vote.  Survivors (rare) are inserted
-// into the CTA's top-8.
+// Filter one unit.  Common case: the vector maxima, one compare against the
+// warp's cached threshold Treg and one vote (NaN also fails `lmax < Treg`).
+// A stale Treg only lets more through: the CTA's threshold never decreases.
+// Otherwise the threshold is refreshed from shared memory, read once and
+// broadcast (lanes may arrive at different times after the inserts of an
+// earlier unit, and all must take the same branches), and the survivors are
+// inserted into the CTA's top-8.
 template <int DT, bool VEC>
-__device__ __forceinline__ void process_unit(const Slot<DT, VEC> (&v)[VNV], int64_t base, int64_t end, u64* top8,
-                                             uint32_t* err, int lane) {
+__device__ __forceinline__ void process_unit(const Slot<DT, VEC> (&v)[VNV], int64_t base, int64_t end, float& Treg,
+                                             u64* top8, uint32_t* err, int lane) {
   float vm[VNV];
   float lmax = -INFINITY;
 #pragma unroll
@@ -329,10 +339,12 @@ __device__ __forceinline__ void process_unit(const Slot<DT, VEC> (&v)[VNV], int6
     vm[kk] = v[kk].vmax();
     lmax = max_nan(lmax, vm[kk]);
   }
-  float T = __shfl_sync(FULL, top8_threshold(top8), 0);
-  if (!__any_sync(FULL, !(lmax < T))) return;  // nothing reaches T, no NaN
+  if (!__any_sync(FULL, !(lmax < Treg))) return;
   if (lmax != lmax) atomicOr(err, GRAFT_ERR_NAN);
-  if (T == -INFINITY) T = eighth_lane_max(lmax, lane);  // top-8 not full yet: 8 lane maxima reach T
+  float T = __shfl_sync(FULL, top8_threshold(top8), 0);
+  if (T == -INFINITY) T = (Treg != -INFINITY) ? Treg : eighth_lane_max(lmax, lane);  // top-8 not full yet
+  Treg = T;
+  if (!__any_sync(FULL, lmax >= T)) return;
 #pragma unroll
   for (int kk = 0; kk < VNV; ++kk) {
     const int64_t sl = base + kk * 32 + lane;
@@ -415,12 +427,13 @@ __global__ void __launch_bounds__(VT, VCPS) k_verify(VerifyArgs a) {
       const int64_t lo = max(s0, k * npr) - k * npr, hi = min(s1, (k + 1) * npr) - k * npr;
       const char* rowp = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)g.stride * ES;
       u64* top8 = sm.top8[j];
+      float Treg = -INFINITY;
       const int64_t vhi = min(hi, nslot);  // vector slots of this segment: [lo, vhi)
       const int64_t nunits = vhi > lo ? (vhi - lo + VUNIT - 1) / VUNIT : 0;
       for (int64_t u = warp; u < nunits; u += VW) {
         SlotT v[VNV];
         load_unit<DT, VEC>(v, rowp, lo + u * VUNIT, vhi, lane);
-        process_unit<DT, VEC>(v, lo + u * VUNIT, vhi, top8, a.err, lane);
+        process_unit<DT, VEC>(v, lo + u * VUNIT, vhi, Treg, top8, a.err, lane);
       }
       if (warp == VW - 1 && hi > nslot && lane < g.tail) {  // the row's last V % EPL elements
         constexpr int EPLc = SlotT::EPL;
