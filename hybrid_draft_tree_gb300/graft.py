@@ -24,7 +24,7 @@ K = 8
 # Entry points declared in include/graft.h (checked by the CPU tests).
 EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup", "graft_assemble",
            "graft_verify_update", "graft_get_matrix", "graft_set_matrix", "graft_matrix_device_ptr",
-           "graft_sync", "graft_last_error", "graft_last_launch_count")
+           "graft_sync", "graft_last_error", "graft_last_launch_count", "graft_verify_update_noalloc")
 
 
 class GraftError(RuntimeError):
@@ -76,6 +76,8 @@ def load(build_if_missing: bool = True):
     L.graft_last_error.restype = ctypes.c_char_p
     L.graft_last_launch_count.argtypes = [vp]
     L.graft_last_launch_count.restype = i32
+    L.graft_verify_update_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp]
+    L.graft_verify_update_noalloc.restype = ctypes.c_int
     for name in ("graft_init", "graft_destroy", "graft_warmup", "graft_assemble", "graft_verify_update",
                  "graft_get_matrix", "graft_set_matrix", "graft_sync"):
         getattr(L, name).restype = ctypes.c_int

@@ -146,6 +146,40 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
                         const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
                         int64_t row_stride, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream);
 
+/* Allocation-free variant of graft_verify_update.  It has no counterpart in
+ * the paper: it is an integration entry point for callers that cannot call
+ * cudaMalloc, such as an engine that records its decode step into a CUDA
+ * graph (allocation is not allowed while a stream is being captured) or one
+ * whose device memory is fully pre-planned by its own arena or by another
+ * runtime's caching allocator.  Those callers cannot create a graft_handle,
+ * so this call takes the continuation matrix as a caller buffer and runs the
+ * same kernels as graft_verify_update on fixed scratch memory compiled into
+ * the library.
+ *   vocab, logits_dtype      as in graft_config
+ *   batch, slots             requests and slots per request (S); batch * slots
+ *                            must be <= GRAFT_NOALLOC_MAX_ROWS, slots <= 64
+ *   d_tree_*, d_logits, row_stride, d_accept_len, d_out_tokens
+ *                            as in graft_verify_update
+ *   d_matrix                 DEVICE [vocab][8] int32 continuation matrix, read
+ *                            and updated in place (-1 = empty entry)
+ *   d_err_flags              DEVICE uint32 word the kernels OR GRAFT_ERR_* bits
+ *                            into; the caller zeroes and reads it
+ * The scratch is a fixed GRAFT_NOALLOC_BYTES device array: every GPU that
+ * loads the library holds it until the process exits, and all calls share it,
+ * so calls that overlap on the GPU (for example on two streams at once) race.
+ * Nothing is carried from one call to the next.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress, no allocation);
+ * make that first call before any stream capture.  Asynchronous; returns
+ * GRAFT_EINVAL for bad arguments or sizes beyond the limit (nothing queued),
+ * GRAFT_ECUDA if a CUDA call fails. */
+#define GRAFT_NOALLOC_MAX_ROWS 2048
+#define GRAFT_NOALLOC_BYTES (GRAFT_NOALLOC_MAX_ROWS * (16 * 8 * 8 + 4 + 8 * 4))
+int graft_verify_update_noalloc(int32_t vocab, int32_t logits_dtype, int32_t batch, int32_t slots,
+                                const int32_t* d_tree_tok, const int8_t* d_tree_parent, const int32_t* d_tree_pos,
+                                const uint64_t* d_tree_mask, const void* d_logits, int64_t row_stride,
+                                int32_t* d_matrix, int32_t* d_accept_len, int32_t* d_out_tokens,
+                                uint32_t* d_err_flags, void* stream);
+
 /* Copy the continuation matrix (V x 8 int32, row-major) to / from HOST memory.
  * Synchronous with respect to `stream`. */
 int graft_get_matrix(graft_handle* h, int32_t* host_out, void* stream);
