@@ -47,6 +47,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   __shared__ float s_conf[MAX_DRAFT];
   __shared__ int32_t s_depth[MAX_DRAFT];
   __shared__ int32_t s_slot[MAX_DRAFT];
+  __shared__ __align__(16) unsigned long long s_key[MAX_DRAFT];
   __shared__ int32_t s_rtok[MAX_S];
   __shared__ int32_t s_rslot[MAX_S];
   __shared__ int32_t o_tok[MAX_S];
@@ -56,6 +57,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   __shared__ int s_warp[AT / 32];
   __shared__ int s_bad, s_best[3], s_tcut, s_maxdepth;
 
+  const uint64_t keep = l2_keep_policy();
   if (t == 0) { s_bad = 0; s_tcut = n; s_maxdepth = 0; }
   if (t < 3) s_best[t] = -1;
   if (t < MAX_S) { o_tok[t] = -1; o_par[t] = -1; o_pos[t] = -1; o_rep[t] = 0; s_rtok[t] = -1; s_rslot[t] = -1; }
@@ -106,7 +108,9 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
         }
       }
       __syncthreads();
-      if (nd >= 0) { s_conf[t] = nc; s_depth[t] = nd; my_depth = nd; }
+      // -0 (a -0.0 probability) is stored as +0: keys and maxima below use the
+      // bits, and the two compare equal as values
+      if (nd >= 0) { s_conf[t] = nc == 0.f ? 0.f : nc; s_depth[t] = nd; my_depth = nd; }
       if (!__syncthreads_or(t < nn && my_depth < 0)) break;
     }
     if (t < nn) atomicMax(&s_maxdepth, my_depth);
@@ -133,15 +137,35 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
     }
 
     // ---- keep the top-D candidates by (confidence desc, index asc) --------
+    // key = (conf bits << 32) | (~index) for candidates (conf >= 0, so its bits
+    // order like the value), 0 otherwise; rank = number of larger keys.
+    if (t < MAX_DRAFT) {
+      unsigned long long key = 0ull;
+      if (t < nn && my_depth <= cut)
+        key = ((unsigned long long)__float_as_uint(s_conf[t]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+      s_key[t] = key;
+    }
+    __syncthreads();
     bool keep = false;
     if (t < nn && my_depth <= cut) {
-      const float c = s_conf[t];
-      int r = 0;
-      for (int j = 0; j < nn; ++j) {
-        const float cj = s_conf[j];
-        r += (s_depth[j] <= cut) && (cj > c || (cj == c && j < t));
+      const unsigned long long mine = s_key[t];
+      const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(s_key);
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // independent accumulators: the loads overlap
+      const int pairs = (nn + 1) / 2;      // s_key[nn] is 0 when nn is odd
+      int j = 0;
+      for (; j + 2 <= pairs; j += 2) {
+        const ulonglong2 x = k2[j], y = k2[j + 1];
+        r0 += x.x > mine;
+        r1 += x.y > mine;
+        r2 += y.x > mine;
+        r3 += y.y > mine;
       }
-      keep = r < D;
+      for (; j < pairs; ++j) {
+        const ulonglong2 x = k2[j];
+        r0 += x.x > mine;
+        r1 += x.y > mine;
+      }
+      keep = r0 + r1 + r2 + r3 < D;
     }
     const int pre = block_excl_count(keep, s_warp, n_draft);
     if (t < MAX_DRAFT) s_slot[t] = keep ? 1 + pre : -1;
@@ -171,15 +195,19 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
       const int used = 1 + n_draft;
       const int maxpos = s_maxdepth + 1;
       const int nrep_local = (t >= 1 && t < used) ? o_rep[t] : 0;
+      // rank of a replaced slot among its parent's replaced children (slot order)
+      int srank = 0;
+      if (t >= 1 && t < used && o_rep[t]) {
+        const int p = o_par[t];
+        for (int q = 1; q < t; ++q) srank += (o_par[q] == p) && (o_rep[q] != 0);
+      }
       for (int level = 1; level <= maxpos; ++level) {
         if (t >= 1 && t < used && o_pos[t] == level && o_rep[t]) {
           const int p = o_par[t];
           const int32_t ptok = o_tok[p];
-          int srank = 0;
-          for (int q = 1; q < t; ++q) srank += (o_par[q] == p) && (o_rep[q] != 0);
           int32_t tk = -1;
           if (srank < K && ptok >= 0 && ptok < a.V) {
-            tk = a.C[(int64_t)ptok * K + srank];
+            tk = ld_keep(a.C + (int64_t)ptok * K + srank, keep);
             if (tk < -1 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); tk = -1; }
           }
           if (tk >= 0) { o_tok[t] = tk; o_rep[t] = 2; }
@@ -224,7 +252,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
         const int32_t ptok = (jq < 0) ? anchor_tok : s_rtok[jq];
         int32_t tk = -1;
         if (ptok >= 0 && ptok < a.V) {
-          tk = a.C[(int64_t)ptok * K + jr];
+          tk = ld_keep(a.C + (int64_t)ptok * K + jr, keep);
           if (tk < -1 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); tk = -1; }
         }
         s_rtok[j] = tk;
@@ -252,15 +280,15 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
       uint64_t m = 1ull << t;
       int p = o_par[t];
       for (int steps = 0; p >= 0 && steps < MAX_S; ++steps) { m |= 1ull << p; p = o_par[p]; }
-      a.tree_tok[k] = tk;
-      a.tree_parent[k] = (int8_t)o_par[t];
-      a.tree_pos[k] = o_pos[t];
-      a.tree_mask[k] = m;
+      st_keep(a.tree_tok + k, tk, keep);
+      st_keep(a.tree_parent + k, (int8_t)o_par[t], keep);
+      st_keep(a.tree_pos + k, o_pos[t], keep);
+      st_keep(a.tree_mask + k, m, keep);
     } else {
-      a.tree_tok[k] = -1;
-      a.tree_parent[k] = -1;
-      a.tree_pos[k] = -1;
-      a.tree_mask[k] = 0ull;
+      st_keep(a.tree_tok + k, -1, keep);
+      st_keep(a.tree_parent + k, (int8_t)-1, keep);
+      st_keep(a.tree_pos + k, -1, keep);
+      st_keep(a.tree_mask + k, 0ull, keep);
     }
   }
   const int valid = __syncthreads_count(t < S && o_tok[t] >= 0);

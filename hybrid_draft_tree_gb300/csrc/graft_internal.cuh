@@ -93,6 +93,29 @@ struct WarmArgs {
   uint32_t* err;
 };
 
+// L2 residency of the small, hot state (the continuation matrix and the
+// flattened trees): evict-last cache policy on their loads and stores, while
+// the logits stream through with evict-first loads.
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ int32_t ld_keep(const int32_t* ptr, uint64_t pol) {
+  int32_t v;
+  asm volatile("ld.global.L2::cache_hint.s32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_keep(int32_t* ptr, int32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.s32 [%0], %1, %2;" ::"l"(ptr), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep(int8_t* ptr, int8_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b8 [%0], %1, %2;" ::"l"(ptr), "h"((short)v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep(uint64_t* ptr, uint64_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(ptr), "l"(v), "l"(pol) : "memory");
+}
+
 // launchers (return cudaGetLastError())
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);

@@ -470,6 +470,7 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x, S = a.S;
   const int rows = a.batch * S;
+  const uint64_t keep = l2_keep_policy();
   u64 keys[(MAX_S + FW - 1) / FW];
 #pragma unroll
   for (int h = 0; h < (MAX_S + FW - 1) / FW; ++h) {
@@ -494,7 +495,7 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
     if (t < 0 || t >= a.g.V) continue;
     bool later = false;
     for (int r = row + 1 + lane; r < rows; r += 32) later |= (a.tree_tok[r] == t);
-    if (!__any_sync(FULL, later) && lane < K) C[(size_t)t * K + lane] = key_id(keys[h]);
+    if (!__any_sync(FULL, later) && lane < K) st_keep(C + (size_t)t * K + lane, key_id(keys[h]), keep);
   }
 }
 

@@ -244,6 +244,63 @@ def test_warm_start_32k_full_size_sampled():
     assert g.sync() == 0
 
 
+# ------------------------------------------------------------------------------ assemble edge cases
+def _assemble_case(mode, tok, par, prob, C, root, V, budget=60):
+    """One request through graft_assemble vs the oracle."""
+    g_ = G()
+    n = len(tok)
+    cfg = g_.graft_default_config(V, 1, mode, W.BF16, budget=budget, max_draft_nodes=max(n, 1))
+    eng = g_.Graft(cfg)
+    eng.set_matrix(C)
+    S = budget + 1
+    d = lambda a_, dt: torch.from_numpy(np.ascontiguousarray(a_, dt)[None]).cuda()
+    t_tok, t_par, t_pos = (torch.empty((1, S), dtype=x, device="cuda") for x in (torch.int32, torch.int8, torch.int32))
+    t_mask = torch.empty((1, S), dtype=torch.int64, device="cuda")
+    info = torch.empty((1, 4), dtype=torch.int32, device="cuda")
+    eng.assemble(1, torch.tensor([root], dtype=torch.int32, device="cuda"), d(tok, np.int32),
+                 None if par is None else d(par, np.int16), d(prob, np.float32), t_tok, t_par, t_pos, t_mask, info)
+    P = oracle.make_params(V, budget=budget, mode=mode)
+    tr = oracle.assemble(P, root, tok, prob, C, par)
+    assert np.array_equal(t_tok.cpu().numpy()[0], tr.tok)
+    assert np.array_equal(t_par.cpu().numpy()[0].astype(np.int32), tr.par)
+    assert np.array_equal(t_pos.cpu().numpy()[0], tr.pos)
+    assert np.array_equal(t_mask.cpu().numpy()[0].view(np.uint64), tr.mask)
+    assert np.array_equal(info.cpu().numpy()[0], tr.info), (info.cpu().numpy()[0], tr.info)
+    assert eng.sync() == 0
+    eng.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("seed", range(4))
+def test_assemble_degenerate_probabilities(mode, seed):
+    """Signed zeros, exact confidence ties, probability-1 chains and an empty
+    matrix row: kept set, checkpoint firing and replacement match the oracle."""
+    rng = np.random.default_rng(seed)
+    V = 500
+    h = W.Harness(W.WORKLOADS[0].scaled(V=V))
+    root, prev, ctx = h.init_state()
+    tok, par, prob = h.draft(seed, root, prev)
+    tok, par, prob = tok[0], par[0], prob[0].copy()
+    choice = rng.integers(0, 4, len(prob))
+    prob[choice == 0] = 0.0
+    prob[choice == 1] = -0.0
+    prob[choice == 2] = 0.25                      # many exact ties
+    prob[:4] = [0.25, 0.25, -0.0, 0.25]
+    C = rng.integers(-1, V, (V, 8)).astype(np.int32)
+    C[int(root[0])] = -1
+    _assemble_case(mode, tok, par, prob, C, int(root[0]), V)
+
+
+def test_assemble_tail_degenerate():
+    V = 300
+    rng = np.random.default_rng(5)
+    C = rng.integers(-1, V, (V, 8)).astype(np.int32)
+    btok = rng.integers(0, V, 16).astype(np.int32)
+    for conf in ([0.4] * 16, [0.39] + [0.9] * 15, [0.9] * 15 + [-0.0], [0.0] * 16):
+        _assemble_case(2, btok, None, np.array(conf, np.float32), C, 7, V, budget=16)
+    _assemble_case(2, btok[:0], None, np.zeros(0, np.float32), C, 7, V, budget=16)   # empty block
+
+
 # ------------------------------------------------------------------------------ verify edge cases
 def _tree_from_parents(tok, par):
     S = len(tok)
