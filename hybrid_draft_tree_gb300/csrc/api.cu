@@ -27,6 +27,8 @@ struct graft_handle {
   int32_t* req_ticket = nullptr;  // [max_batch]
   int32_t* topk = nullptr;        // [rows][8]
   int32_t* row_nseg = nullptr;    // [rows]
+  float* umax = nullptr;          // [rows][upr_max] two-pass unit maxima
+  int upr_max = 0;
   int32_t* list = nullptr;        // [V] warm-up rows
   int32_t* count = nullptr;       // [1]
   uint32_t* err = nullptr;        // [1]
@@ -100,7 +102,7 @@ cudaError_t dalloc(T** p, size_t n) {
 
 void free_all(graft_handle* h) {
   cudaFree(h->C); cudaFree(h->winner); cudaFree(h->tpl); cudaFree(h->part);
-  cudaFree(h->row_ticket); cudaFree(h->req_ticket); cudaFree(h->topk); cudaFree(h->row_nseg);
+  cudaFree(h->row_ticket); cudaFree(h->req_ticket); cudaFree(h->topk); cudaFree(h->row_nseg); cudaFree(h->umax);
   cudaFree(h->list); cudaFree(h->count); cudaFree(h->err);
 }
 
@@ -121,7 +123,7 @@ int check_cfg(const graft_config* c, graft_handle* h) {
   const int maxn = c->mode == GRAFT_MODE_TAIL ? c->budget : graft::MAX_DRAFT;
   if (c->max_draft_nodes < 0 || c->max_draft_nodes > maxn)
     return fail(h, GRAFT_EINVAL, "max_draft_nodes must be in [0, %d]", maxn);
-  if (c->scan_kernel < 0 || c->scan_kernel > 2) return fail(h, GRAFT_EINVAL, "scan_kernel must be 0, 1 or 2");
+  if (c->scan_kernel < 0 || c->scan_kernel > 3) return fail(h, GRAFT_EINVAL, "scan_kernel must be 0, 1, 2 or 3");
   return GRAFT_OK;
 }
 
@@ -199,6 +201,12 @@ int graft_init(const graft_config* cfg, graft_handle** out) {
   if (e == cudaSuccess) e = dalloc(&h->req_ticket, (size_t)cfg->max_batch);
   if (e == cudaSuccess) e = dalloc(&h->topk, rows * graft::K);
   if (e == cudaSuccess) e = dalloc(&h->row_nseg, rows);
+  {
+    const int64_t epl_min = cfg->logits_dtype == GRAFT_BF16 ? 8 : 4;  // two-pass runs on 16-byte aligned rows only
+    const int64_t upr = (V / epl_min + 31) / 32;
+    h->upr_max = (int)(upr <= graft::TWO_PASS_MAX_UNITS ? upr : 0);
+    if (e == cudaSuccess && h->upr_max > 0) e = dalloc(&h->umax, rows * (size_t)h->upr_max);
+  }
   if (e == cudaSuccess) e = dalloc(&h->list, V);
   if (e == cudaSuccess) e = dalloc(&h->count, 1);
   if (e == cudaSuccess) e = dalloc(&h->err, 1);
@@ -319,17 +327,25 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
   a.winner = h->winner; a.err = h->err; a.row_nseg = h->row_nseg;
   const bool tma_fits = h->tma_ready && a.g.vec && a.g.row_vec_bytes >= graft::TMA_CHUNK &&
                         a.g.cpr <= graft::MAX_SPLIT && rows <= graft::verify_tma_max_rows(h->num_sms);
+  a.upr = (int32_t)((a.g.nslot + 31) / 32);
+  const int grid2 = h->num_sms * graft::two_pass_ctas_per_sm();
+  const bool two_pass_fits = a.g.vec && h->umax && a.g.nslot > 0 && a.upr <= h->upr_max &&
+                             rows <= graft::two_pass_max_rows(grid2);
   const bool use_tma = tma_fits && c.scan_kernel == 2;
+  const bool use_two_pass = !use_tma && two_pass_fits && (c.scan_kernel == 0 || c.scan_kernel == 3);
   const int grid = h->num_sms * graft::verify_ctas_per_sm();
-  if (!use_tma && rows > graft::verify_max_rows(grid))
+  if (!use_tma && !use_two_pass && rows > graft::verify_max_rows(grid))
     return fail(h, GRAFT_EINVAL, "batch * (budget + 1) = %lld rows exceeds %d on this GPU", (long long)rows,
                 graft::verify_max_rows(grid));
-  cudaError_t e = use_tma ? graft::launch_verify_tma(a, c.logits_dtype, h->num_sms, (cudaStream_t)stream)
-                          : graft::launch_verify(a, c.logits_dtype, grid, (cudaStream_t)stream);
+  a.umax = h->umax;
+  a.topk_staged = use_two_pass ? 1 : 0;
+  cudaError_t e = use_tma        ? graft::launch_verify_tma(a, c.logits_dtype, h->num_sms, (cudaStream_t)stream)
+                  : use_two_pass ? graft::launch_two_pass(a, c.logits_dtype, grid2, (cudaStream_t)stream)
+                                 : graft::launch_verify(a, c.logits_dtype, grid, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update scan launch");
   e = graft::launch_finish(a, h->C, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update finish launch");
-  h->last_launches = 2;
+  h->last_launches = use_two_pass ? 3 : 2;
   return GRAFT_OK;
 }
 

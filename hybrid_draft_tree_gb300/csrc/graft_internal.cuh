@@ -12,6 +12,7 @@ constexpr int MAX_S = 64;       // slots per request (one uint64 mask row)
 constexpr int MAX_DRAFT = 256;  // draft nodes per request in one assemble CTA
 constexpr int MAX_SPLIT = 16;   // CTAs per logits row in the verify scan
 constexpr int TMA_CHUNK = 32768; // bytes per pipeline stage of the TMA verify scan
+constexpr int TWO_PASS_MAX_UNITS = 1024;  // 512-byte units per row on the two-pass scan (512 KB rows)
 
 // Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth.
 struct TemplateDev {
@@ -70,6 +71,9 @@ struct VerifyArgs {
   int32_t* topk;              // [rows][K] staged top-8 ids
   int32_t* winner;            // [V] last-writer key (row + 1), 0 = none
   int32_t* row_nseg;          // [rows] number of partial top-8s the scan wrote for the row
+  float* umax;                // two-pass scan: [rows][upr] maximum of every 512-byte unit
+  int32_t upr;                // two-pass scan: units per row
+  int32_t topk_staged;        // 1: the scan staged final top-8 ids in topk (no partials to merge)
   uint32_t* err;
 };
 
@@ -127,6 +131,9 @@ size_t verify_tma_smem_bytes();
 int verify_tma_max_rows(int grid);
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
 cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s);
+cudaError_t launch_two_pass(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
+int two_pass_ctas_per_sm();
+int two_pass_max_rows(int grid);
 cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s);
 
 }  // namespace graft

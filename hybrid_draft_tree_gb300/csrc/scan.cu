@@ -255,6 +255,7 @@ constexpr int VCPS = GRAFT_VERIFY_CTAS_PER_SM;
 
 struct VSmem {
   u64 top8[VSEGS][K];  // the CTA's running top-8 of each row segment of the group
+  u64 seed[2][VW][K];  // each warp's 8 largest lane maxima of its first unit (by segment parity)
   int warpsum[VW];
   int rowlist[VMAXROWS];
 };
@@ -430,10 +431,42 @@ __global__ void __launch_bounds__(VT, VCPS) k_verify(VerifyArgs a) {
       float Treg = -INFINITY;
       const int64_t vhi = min(hi, nslot);  // vector slots of this segment: [lo, vhi)
       const int64_t nunits = vhi > lo ? (vhi - lo + VUNIT - 1) / VUNIT : 0;
-      for (int64_t u = warp; u < nunits; u += VW) {
+      // First round, cooperatively: every warp loads its first unit; the 8th
+      // largest of the CTA's lane maxima (8 distinct elements reach it) seeds
+      // the threshold, so the first round inserts a few keys instead of
+      // every warp filling the top-8 against its own, weaker bound.
+      {
         SlotT v[VNV];
-        load_unit<DT, VEC>(v, rowp, lo + u * VUNIT, vhi, lane);
-        process_unit<DT, VEC>(v, lo + u * VUNIT, vhi, Treg, top8, a.err, lane);
+        float lmax = -INFINITY;
+        const bool has = warp < nunits;
+        if (has) {
+          load_unit<DT, VEC>(v, rowp, lo + warp * VUNIT, vhi, lane);
+#pragma unroll
+          for (int kk = 0; kk < VNV; ++kk) lmax = max_nan(lmax, v[kk].vmax());
+        }
+        const u64 lk = bitonic32_desc(make_key(lmax == lmax ? lmax : -INFINITY, lane), lane);
+        if (lane < K) sm.seed[j & 1][warp][lane] = lk;
+        __syncthreads();
+        const u64 s8 = __shfl_sync(FULL, warp_merge_ool(0ull, &sm.seed[j & 1][0][0], VW * K, lane), K - 1);
+        Treg = s8 ? key_val(s8) : -INFINITY;
+        if (has) process_unit<DT, VEC>(v, lo + warp * VUNIT, vhi, Treg, top8, a.err, lane);
+      }
+      // steady state, double-buffered: the next unit's loads are in flight
+      // while the current one is filtered (and, rarely, inserted)
+      int64_t u = warp + VW;
+      if (u < nunits) {
+        SlotT va[VNV], vb[VNV];
+        load_unit<DT, VEC>(va, rowp, lo + u * VUNIT, vhi, lane);
+        while (true) {
+          if (u + VW < nunits) load_unit<DT, VEC>(vb, rowp, lo + (u + VW) * VUNIT, vhi, lane);
+          process_unit<DT, VEC>(va, lo + u * VUNIT, vhi, Treg, top8, a.err, lane);
+          u += VW;
+          if (u >= nunits) break;
+          if (u + VW < nunits) load_unit<DT, VEC>(va, rowp, lo + (u + VW) * VUNIT, vhi, lane);
+          process_unit<DT, VEC>(vb, lo + u * VUNIT, vhi, Treg, top8, a.err, lane);
+          u += VW;
+          if (u >= nunits) break;
+        }
       }
       if (warp == VW - 1 && hi > nslot && lane < g.tail) {  // the row's last V % EPL elements
         constexpr int EPLc = SlotT::EPL;
@@ -480,6 +513,10 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
     const int row = b * S + i;
     const int32_t t = a.tree_tok[row];
     if (t < 0 || t >= a.g.V) continue;
+    if (a.topk_staged) {  // the scan already staged the row's final top-8 ids
+      keys[h] = lane < K ? (u64)(uint32_t)__ldcg(a.topk + (size_t)row * K + lane) : 0ull;
+      continue;
+    }
     const int nseg = min(max(a.row_nseg[row], 1), MAX_SPLIT);
     keys[h] = warp_merge_global(a.part + (size_t)row * MAX_SPLIT * K, nseg * K, lane);
     if (lane < K) a.topk[(size_t)row * K + lane] = key_id(keys[h]);
@@ -495,7 +532,8 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
     if (t < 0 || t >= a.g.V) continue;
     bool later = false;
     for (int r = row + 1 + lane; r < rows; r += 32) later |= (a.tree_tok[r] == t);
-    if (!__any_sync(FULL, later) && lane < K) st_keep(C + (size_t)t * K + lane, key_id(keys[h]), keep);
+    const int32_t id = a.topk_staged ? (int32_t)(uint32_t)keys[h] : key_id(keys[h]);
+    if (!__any_sync(FULL, later) && lane < K) st_keep(C + (size_t)t * K + lane, id, keep);
   }
 }
 

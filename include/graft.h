@@ -82,8 +82,10 @@ typedef struct {
   float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15) */
   float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4) */
   int32_t max_draft_nodes;/* largest draft tree (<= 256) or block (<= budget) per request */
-  int32_t scan_kernel;    /* verify scan: 0 = automatic, 1 = register-tiled, 2 = TMA-pipelined
-                             (used only for 16-byte aligned rows of >= 32 KB; else register-tiled) */
+  int32_t scan_kernel;    /* verify scan: 0 = automatic (two-pass on 16-byte aligned rows, else
+                             single-pass), 1 = single-pass with a shared running top-8,
+                             2 = TMA-pipelined (aligned rows of >= 32 KB only), 3 = two-pass
+                             (unit maxima, then per-row selection; aligned rows only) */
 } graft_config;
 
 /* Fill *cfg with the paper's defaults for `mode` and vocabulary V. */

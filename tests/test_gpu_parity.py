@@ -155,25 +155,25 @@ def test_lockstep_small(wid, V, B, sigma, steps):
     assert any(a > 0 for _, a in stats)
 
 
-@pytest.mark.parametrize("scan_kernel", [1, 2])
+@pytest.mark.parametrize("scan_kernel", [1, 2, 3])
 @pytest.mark.parametrize("wid,V,B,sigma,steps", [
     (2, 40000, 16, 2.0, 8),     # static, 80 KB rows: 3 chunks per row, rows split over CTAs
     (4, 24576, 64, 2.0, 6),     # tail, 64 requests x 17 slots
     (0, 16384, 1, 0.75, 20),    # fp32 checkpoint, 64 KB rows, few rows per step
 ])
 def test_lockstep_both_scan_kernels(scan_kernel, wid, V, B, sigma, steps):
-    """The register-tiled and the TMA-pipelined verify scans on rows of
+    """The single-pass, TMA-pipelined and two-pass verify scans on rows of
     >= 32 KB, closed loop against the oracle."""
     w = W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=sigma)
     lockstep(w, steps, check_rows=4, scan_kernel=scan_kernel)
 
 
-@pytest.mark.parametrize("scan_kernel", [1, 2])
+@pytest.mark.parametrize("scan_kernel", [1, 2, 3])
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
 @pytest.mark.parametrize("V,pad,fn", [(40000, 0, "normal"), (40003, 5, "normal"), (65536, 0, "ties"),
                                       (33000, 0, "constant")])
 def test_verify_scan_kernels(scan_kernel, dtype, V, pad, fn):
-    """Both scans on aligned rows: ragged tails (V % 8 != 0 with a padded
+    """Every scan on aligned rows: ragged tails (V % 8 != 0 with a padded
     stride), heavy ties, all-equal rows (candidate overflow)."""
     fns = {"normal": _normal, "ties": _ties, "constant": _constant}
     _verify_case(V, dtype, 61, 3, fns[fn], stride_pad=pad, seed=V + pad, scan_kernel=scan_kernel)
