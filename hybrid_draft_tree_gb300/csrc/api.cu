@@ -34,6 +34,12 @@ struct graft_handle {
   uint32_t* err = nullptr;        // [1]
   int32_t last_launches = 0;
   char msg[256] = {0};
+  // tracing: event pairs around kernels, read back by graft_profile_read
+  static constexpr int kProfSlots = 64;
+  bool profiling = false;
+  cudaEvent_t prof_ev[2 * kProfSlots] = {};
+  const char* prof_name[kProfSlots] = {};
+  int prof_n = 0;
 };
 
 namespace {
@@ -95,12 +101,31 @@ void build_template(int max_depth, int width, int len, std::vector<int32_t>& par
   }
 }
 
+// Bracket one kernel launch with profiling events when tracing is on.
+struct ProfScope {
+  graft_handle* h;
+  cudaStream_t s;
+  int slot = -1;
+  ProfScope(graft_handle* h_, cudaStream_t s_, const char* name) : h(h_), s(s_) {
+    if (h->profiling && h->prof_n < graft_handle::kProfSlots) {
+      slot = h->prof_n++;
+      h->prof_name[slot] = name;
+      cudaEventRecord(h->prof_ev[2 * slot], s);
+    }
+  }
+  ~ProfScope() {
+    if (slot >= 0) cudaEventRecord(h->prof_ev[2 * slot + 1], s);
+  }
+};
+
 template <typename T>
 cudaError_t dalloc(T** p, size_t n) {
   return cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T) + 16);
 }
 
 void free_all(graft_handle* h) {
+  for (auto& e : h->prof_ev)
+    if (e) cudaEventDestroy(e);
   cudaFree(h->C); cudaFree(h->winner); cudaFree(h->tpl); cudaFree(h->part);
   cudaFree(h->row_ticket); cudaFree(h->req_ticket); cudaFree(h->topk); cudaFree(h->row_nseg); cudaFree(h->umax);
   cudaFree(h->list); cudaFree(h->count); cudaFree(h->err);
@@ -262,7 +287,11 @@ int graft_warmup(graft_handle* h, const int32_t* d_tokens, const void* d_logits,
   a.count = h->count;
   a.C = h->C;
   a.err = h->err;
-  cudaError_t e = graft::launch_warmup(a, h->cfg.logits_dtype, h->warm_ctas, (cudaStream_t)stream);
+  cudaError_t e;
+  {
+    ProfScope ps(h, (cudaStream_t)stream, "warmup");
+    e = graft::launch_warmup(a, h->cfg.logits_dtype, h->warm_ctas, (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_warmup launch");
   h->last_launches = 4;
   return GRAFT_OK;
@@ -300,7 +329,11 @@ int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
   a.tree_tok = d_tree_tok; a.tree_parent = d_tree_parent; a.tree_pos = d_tree_pos; a.tree_mask = d_tree_mask;
   a.info = d_info;
   a.err = h->err;
-  cudaError_t e = graft::launch_assemble(a, (cudaStream_t)stream);
+  cudaError_t e;
+  {
+    ProfScope ps(h, (cudaStream_t)stream, "k_assemble");
+    e = graft::launch_assemble(a, (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_assemble launch");
   h->last_launches = 1;
   return GRAFT_OK;
@@ -339,11 +372,26 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
                 graft::verify_max_rows(grid));
   a.umax = h->umax;
   a.topk_staged = use_two_pass ? 1 : 0;
-  cudaError_t e = use_tma        ? graft::launch_verify_tma(a, c.logits_dtype, h->num_sms, (cudaStream_t)stream)
-                  : use_two_pass ? graft::launch_two_pass(a, c.logits_dtype, grid2, (cudaStream_t)stream)
-                                 : graft::launch_verify(a, c.logits_dtype, grid, (cudaStream_t)stream);
+  cudaError_t e;
+  if (use_two_pass) {
+    {
+      ProfScope ps(h, (cudaStream_t)stream, "k_umax");
+      e = graft::launch_two_pass_umax(a, c.logits_dtype, grid2, (cudaStream_t)stream);
+    }
+    if (e == cudaSuccess) {
+      ProfScope ps(h, (cudaStream_t)stream, "k_select");
+      e = graft::launch_two_pass_select(a, c.logits_dtype, (cudaStream_t)stream);
+    }
+  } else {
+    ProfScope ps(h, (cudaStream_t)stream, use_tma ? "k_verify_tma" : "k_verify");
+    e = use_tma ? graft::launch_verify_tma(a, c.logits_dtype, h->num_sms, (cudaStream_t)stream)
+                : graft::launch_verify(a, c.logits_dtype, grid, (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update scan launch");
-  e = graft::launch_finish(a, h->C, (cudaStream_t)stream);
+  {
+    ProfScope ps(h, (cudaStream_t)stream, "k_finish");
+    e = graft::launch_finish(a, h->C, (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update finish launch");
   h->last_launches = use_two_pass ? 3 : 2;
   return GRAFT_OK;
@@ -384,5 +432,29 @@ int graft_sync(graft_handle* h, void* stream, uint32_t* out_flags) {
 const char* graft_last_error(const graft_handle* h) { return h ? h->msg : "null handle"; }
 
 int32_t graft_last_launch_count(const graft_handle* h) { return h ? h->last_launches : 0; }
+
+int graft_profile_enable(graft_handle* h, int32_t on) {
+  if (!h) return GRAFT_EINVAL;
+  if (on && !h->prof_ev[0]) {
+    for (auto& e : h->prof_ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return cuda_fail(h, cudaGetLastError(), "graft_profile_enable");
+  }
+  h->profiling = on != 0;
+  h->prof_n = 0;
+  return GRAFT_OK;
+}
+
+int graft_profile_read(graft_handle* h, const char** names, float* ms, int32_t max) {
+  if (!h || (max > 0 && (!names || !ms))) return GRAFT_EINVAL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(h, cudaGetLastError(), "graft_profile_read");
+  const int n = h->prof_n < max ? h->prof_n : max;
+  for (int i = 0; i < n; ++i) {
+    names[i] = h->prof_name[i];
+    ms[i] = 0.f;
+    cudaEventElapsedTime(&ms[i], h->prof_ev[2 * i], h->prof_ev[2 * i + 1]);
+  }
+  h->prof_n = 0;
+  return n;
+}
 
 }  // extern "C"

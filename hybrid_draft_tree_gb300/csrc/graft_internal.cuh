@@ -131,7 +131,8 @@ size_t verify_tma_smem_bytes();
 int verify_tma_max_rows(int grid);
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
 cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s);
-cudaError_t launch_two_pass(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
+cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
+cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, cudaStream_t s);
 int two_pass_ctas_per_sm();
 int two_pass_max_rows(int grid);
 cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s);

@@ -289,8 +289,12 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a) {
 }
 
 template <int DT>
-cudaError_t two_pass_impl(const VerifyArgs& a, int grid, cudaStream_t s) {
+cudaError_t umax_impl(const VerifyArgs& a, int grid, cudaStream_t s) {
   k_umax<DT><<<grid, UT, 0, s>>>(a);
+  return cudaGetLastError();
+}
+template <int DT>
+cudaError_t select_impl(const VerifyArgs& a, cudaStream_t s) {
   const int rows = a.batch * a.S;
   k_select<DT><<<(rows + SW - 1) / SW, SW * 32, 0, s>>>(a);
   return cudaGetLastError();
@@ -301,8 +305,11 @@ cudaError_t two_pass_impl(const VerifyArgs& a, int grid, cudaStream_t s) {
 int two_pass_ctas_per_sm() { return 4; }
 int two_pass_max_rows(int grid) { return (UMAXROWS - 2) * grid; }
 
-cudaError_t launch_two_pass(const VerifyArgs& a, int dtype, int grid, cudaStream_t s) {
-  return dtype == GRAFT_BF16 ? two_pass_impl<GRAFT_BF16>(a, grid, s) : two_pass_impl<GRAFT_F32>(a, grid, s);
+cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaStream_t s) {
+  return dtype == GRAFT_BF16 ? umax_impl<GRAFT_BF16>(a, grid, s) : umax_impl<GRAFT_F32>(a, grid, s);
+}
+cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, cudaStream_t s) {
+  return dtype == GRAFT_BF16 ? select_impl<GRAFT_BF16>(a, s) : select_impl<GRAFT_F32>(a, s);
 }
 
 }  // namespace graft

@@ -24,7 +24,8 @@ K = 8
 # Entry points declared in include/graft.h (checked by the CPU tests).
 EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup", "graft_assemble",
            "graft_verify_update", "graft_get_matrix", "graft_set_matrix", "graft_matrix_device_ptr",
-           "graft_sync", "graft_last_error", "graft_last_launch_count", "graft_verify_update_noalloc")
+           "graft_sync", "graft_last_error", "graft_last_launch_count", "graft_verify_update_noalloc",
+           "graft_profile_enable", "graft_profile_read")
 
 
 class GraftError(RuntimeError):
@@ -76,6 +77,10 @@ def load(build_if_missing: bool = True):
     L.graft_last_error.restype = ctypes.c_char_p
     L.graft_last_launch_count.argtypes = [vp]
     L.graft_last_launch_count.restype = i32
+    L.graft_profile_enable.argtypes = [vp, i32]
+    L.graft_profile_enable.restype = ctypes.c_int
+    L.graft_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), i32]
+    L.graft_profile_read.restype = ctypes.c_int
     L.graft_verify_update_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp]
     L.graft_verify_update_noalloc.restype = ctypes.c_int
     for name in ("graft_init", "graft_destroy", "graft_warmup", "graft_assemble", "graft_verify_update",
@@ -185,6 +190,18 @@ class Graft:
 
     def last_error(self) -> str:
         return self.L.graft_last_error(self.h).decode()
+
+    def profile_enable(self, on=True):
+        self._check(self.L.graft_profile_enable(self.h, 1 if on else 0))
+
+    def profile_read(self, max_kernels=64):
+        """[(kernel name, milliseconds)] of the kernels launched since the last read."""
+        names = (ctypes.c_char_p * max_kernels)()
+        ms = (ctypes.c_float * max_kernels)()
+        n = self.L.graft_profile_read(self.h, names, ms, max_kernels)
+        if n < 0:
+            self._check(n)
+        return [(names[i].decode(), float(ms[i])) for i in range(n)]
 
     def last_launch_count(self) -> int:
         return int(self.L.graft_last_launch_count(self.h))

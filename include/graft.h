@@ -198,6 +198,15 @@ int graft_sync(graft_handle* h, void* stream, uint32_t* out_flags);
 /* Message of the last failed call on this handle ("" if none). */
 const char* graft_last_error(const graft_handle* h);
 
+/* Kernel timing (tracing).  When enabled, every kernel this handle launches
+ * is bracketed by two CUDA events recorded on the call's stream (a few
+ * hundred nanoseconds each).  graft_profile_read synchronises the device and
+ * writes, for the kernels of the most recent calls since the last read (at
+ * most `max` of them), their names (static strings) and durations in
+ * milliseconds; it returns the number written and forgets them. */
+int graft_profile_enable(graft_handle* h, int32_t on);
+int graft_profile_read(graft_handle* h, const char** names, float* ms, int32_t max);
+
 /* Number of kernel launches the last graft_assemble / graft_verify_update /
  * graft_warmup call queued. */
 int32_t graft_last_launch_count(const graft_handle* h);

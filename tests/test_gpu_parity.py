@@ -453,3 +453,25 @@ def test_invalid_arguments_are_rejected():
     bad = g_.graft_default_config(100, 2, 0, W.BF16, topk=4)
     with pytest.raises(g_.GraftError):
         g_.Graft(bad)
+
+
+def test_profile_api_reports_each_kernel():
+    """Tracing: every kernel of a step is bracketed by events and reported."""
+    from workloads.device_loop import DeviceLoop
+    w = W.WORKLOADS[2].scaled(V=40000, B=4)
+    eng = engine_for(w)
+    loop = DeviceLoop(w, eng)
+    eng.profile_enable(True)
+    loop.draft()
+    loop.assemble()
+    loop.make_logits()
+    loop.verify_update()
+    rec = eng.profile_read()
+    names = [n for n, _ in rec]
+    assert names == ["k_assemble", "k_umax", "k_select", "k_finish"], names
+    assert all(ms > 0 for _, ms in rec)
+    assert eng.profile_read() == []
+    eng.profile_enable(False)
+    loop.assemble()
+    assert eng.profile_read() == []
+    eng.close()
