@@ -133,7 +133,9 @@ int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
                    int32_t* d_info, void* stream);
 
 /* Steps 4-5 (article §二 gear 3, §三): one streaming pass over the logits of
- * every valid slot computes its top-8 (element 0 = the greedy argmax), then
+ * every valid slot (plus a re-read of the few 512-byte pieces of a row that
+ * can hold its largest values) computes its top-8 (element 0 = the greedy
+ * argmax), then
  *   accepted(i)  <=> every non-root node j on the root->i path has
  *                    tok[j] == argmax(row of parent(j));
  *   winner       =  the accepted slot of greatest position (ties: lower slot);
