@@ -27,7 +27,7 @@ struct graft_handle {
   int32_t* req_ticket = nullptr;  // [max_batch]
   int32_t* topk = nullptr;        // [rows][8]
   int32_t* row_nseg = nullptr;    // [rows]
-  float* umax = nullptr;          // [rows][upr_max] two-pass unit maxima
+  float* umax = nullptr;          // [rows][upr_max rounded up to 4] two-pass unit maxima
   int upr_max = 0;
   int32_t* list = nullptr;        // [V] warm-up rows
   int32_t* count = nullptr;       // [1]
@@ -230,7 +230,7 @@ int graft_init(const graft_config* cfg, graft_handle** out) {
     const int64_t epl_min = cfg->logits_dtype == GRAFT_BF16 ? 8 : 4;  // two-pass runs on 16-byte aligned rows only
     const int64_t upr = (V / epl_min + 31) / 32;
     h->upr_max = (int)(upr <= graft::TWO_PASS_MAX_UNITS ? upr : 0);
-    if (e == cudaSuccess && h->upr_max > 0) e = dalloc(&h->umax, rows * (size_t)h->upr_max);
+    if (e == cudaSuccess && h->upr_max > 0) e = dalloc(&h->umax, rows * (size_t)((h->upr_max + 3) & ~3));
   }
   if (e == cudaSuccess) e = dalloc(&h->list, V);
   if (e == cudaSuccess) e = dalloc(&h->count, 1);
@@ -361,6 +361,7 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
   const bool tma_fits = h->tma_ready && a.g.vec && a.g.row_vec_bytes >= graft::TMA_CHUNK &&
                         a.g.cpr <= graft::MAX_SPLIT && rows <= graft::verify_tma_max_rows(h->num_sms);
   a.upr = (int32_t)((a.g.nslot + 31) / 32);
+  a.ups = (a.upr + 3) & ~3;
   const int grid2 = h->num_sms * graft::two_pass_ctas_per_sm();
   const bool two_pass_fits = a.g.vec && h->umax && a.g.nslot > 0 && a.upr <= h->upr_max &&
                              rows <= graft::two_pass_max_rows(grid2);
@@ -371,7 +372,6 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
     return fail(h, GRAFT_EINVAL, "batch * (budget + 1) = %lld rows exceeds %d on this GPU", (long long)rows,
                 graft::verify_max_rows(grid));
   a.umax = h->umax;
-  a.topk_staged = use_two_pass ? 1 : 0;
   cudaError_t e;
   if (use_two_pass) {
     {
@@ -380,9 +380,13 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
     }
     if (e == cudaSuccess) {
       ProfScope ps(h, (cudaStream_t)stream, "k_select");
-      e = graft::launch_two_pass_select(a, c.logits_dtype, (cudaStream_t)stream);
+      e = graft::launch_two_pass_select(a, c.logits_dtype, h->C, (cudaStream_t)stream);
     }
-  } else {
+    if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update two-pass launch");
+    h->last_launches = 2;
+    return GRAFT_OK;
+  }
+  {
     ProfScope ps(h, (cudaStream_t)stream, use_tma ? "k_verify_tma" : "k_verify");
     e = use_tma ? graft::launch_verify_tma(a, c.logits_dtype, h->num_sms, (cudaStream_t)stream)
                 : graft::launch_verify(a, c.logits_dtype, grid, (cudaStream_t)stream);
@@ -393,7 +397,7 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
     e = graft::launch_finish(a, h->C, (cudaStream_t)stream);
   }
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update finish launch");
-  h->last_launches = use_two_pass ? 3 : 2;
+  h->last_launches = 2;
   return GRAFT_OK;
 }
 

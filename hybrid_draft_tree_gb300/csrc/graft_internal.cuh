@@ -71,9 +71,9 @@ struct VerifyArgs {
   int32_t* topk;              // [rows][K] staged top-8 ids
   int32_t* winner;            // [V] last-writer key (row + 1), 0 = none
   int32_t* row_nseg;          // [rows] number of partial top-8s the scan wrote for the row
-  float* umax;                // two-pass scan: [rows][upr] maximum of every 512-byte unit
+  float* umax;                // two-pass scan: [rows][ups] maximum of every 512-byte unit
   int32_t upr;                // two-pass scan: units per row
-  int32_t topk_staged;        // 1: the scan staged final top-8 ids in topk (no partials to merge)
+  int32_t ups;                // two-pass scan: row stride of umax (upr rounded up to a multiple of 4)
   uint32_t* err;
 };
 
@@ -100,6 +100,14 @@ struct WarmArgs {
 // L2 residency of the small, hot state (the continuation matrix and the
 // flattened trees): evict-last cache policy on their loads and stores, while
 // the logits stream through with evict-first loads.
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may begin before the kernel ahead of it in the stream ends;
+// grid_dependency_wait() blocks until that kernel has finished and its
+// writes are visible (a no-op for an ordinary launch).  The kernel ahead
+// calls grid_dependents_launch() to let the dependent grid be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t l2_keep_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -132,7 +140,7 @@ int verify_tma_max_rows(int grid);
 cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
 cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s);
 cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
-cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s);
 int two_pass_ctas_per_sm();
 int two_pass_max_rows(int grid);
 cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s);

@@ -513,10 +513,6 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
     const int row = b * S + i;
     const int32_t t = a.tree_tok[row];
     if (t < 0 || t >= a.g.V) continue;
-    if (a.topk_staged) {  // the scan already staged the row's final top-8 ids
-      keys[h] = lane < K ? (u64)(uint32_t)__ldcg(a.topk + (size_t)row * K + lane) : 0ull;
-      continue;
-    }
     const int nseg = min(max(a.row_nseg[row], 1), MAX_SPLIT);
     keys[h] = warp_merge_global(a.part + (size_t)row * MAX_SPLIT * K, nseg * K, lane);
     if (lane < K) a.topk[(size_t)row * K + lane] = key_id(keys[h]);
@@ -532,7 +528,7 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
     if (t < 0 || t >= a.g.V) continue;
     bool later = false;
     for (int r = row + 1 + lane; r < rows; r += 32) later |= (a.tree_tok[r] == t);
-    const int32_t id = a.topk_staged ? (int32_t)(uint32_t)keys[h] : key_id(keys[h]);
+    const int32_t id = key_id(keys[h]);
     if (!__any_sync(FULL, later) && lane < K) st_keep(C + (size_t)t * K + lane, id, keep);
   }
 }

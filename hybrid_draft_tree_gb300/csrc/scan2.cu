@@ -14,7 +14,9 @@
 //   the row's top-8 is >= T and lies in a unit whose maximum is >= T.  The
 //   warp re-reads only those units (about 8 of ~600 for V = 151936), keeps
 //   the elements >= T and sorts them (64-bit keys, value desc, id asc).
-// The request kernel (k_finish) then runs acceptance and the matrix update.
+// Pass 2 also finishes: a row writes C[its token] when no later row (in
+// (request, slot) order) carries the same token, and the warp that completes
+// the last valid row of a request (atomic ticket) runs its acceptance.
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -28,8 +30,10 @@ constexpr int UT = 256;            // pass-1 threads per CTA
 constexpr int UW = UT / 32;
 constexpr int UNV = 4;             // units (one 16-byte load per lane each) per warp iteration
 constexpr int UMAXROWS = 192;
-constexpr int MPL = TWO_PASS_MAX_UNITS / 32;  // unit maxima per lane in pass 2
-constexpr int CCAP = 256;          // candidate keys per warp in pass 2
+constexpr int CCAP = 256;          // shared 64-bit words per warp in pass 2
+constexpr int ECAP = 192;          // candidate elements per row in pass 2
+constexpr int UCAP = 2 * (CCAP - ECAP);  // candidate units per row in pass 2 (int ids after the keys)
+constexpr int UB = 16;             // candidate units loaded at once per lane
 
 __device__ __forceinline__ uint4 neg_inf_vec(int dt) {
   const uint32_t w = dt == GRAFT_BF16 ? 0xFF80FF80u : 0xFF800000u;
@@ -41,6 +45,7 @@ template <int DT>
 __global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a) {
   __shared__ int warpsum[UW];
   __shared__ int rowlist[UMAXROWS];
+  grid_dependents_launch();  // pass 2 may be scheduled as SMs free up; it waits for this grid's results
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const ScanGeom& g = a.g;
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a) {
     const int64_t ulo = max(u0, k * upr) - k * upr, uhi = min(u1, (k + 1) * upr) - k * upr;
     const uint4* rowv = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(a.logits) +
                                                        (size_t)row * (size_t)g.stride * ES);
-    float* um = a.umax + (size_t)row * upr;
+    float* um = a.umax + (size_t)row * a.ups;
     for (int64_t ub = ulo + (int64_t)warp * UNV; ub < uhi; ub += (int64_t)UW * UNV) {
       Vec16<DT> v[UNV];
       if (ub + UNV <= uhi && (ub + UNV) * 32 <= nslot) {
@@ -150,142 +155,217 @@ __device__ __noinline__ u64 exact_row(const uint4* rowv, int64_t nslot, const ch
   return out;
 }
 
-constexpr int SW = 8;  // pass-2 warps per CTA
+constexpr int SW = 4;  // pass-2 warps per CTA
+constexpr int STOK = 4096;  // tree tokens a pass-2 CTA keeps in shared memory (all rows when they fit)
 
-// Warp-aggregated append of this lane's keys (n of them, in keys[0..n)) to a
-// per-warp list; returns the warp's total.  No atomics, no divergent loops.
-__device__ __forceinline__ int warp_append(u64* list, int cap, int base, const u64* keys, int n, int lane) {
-  int incl = n;
+// Value of the 8th largest of the 32 lanes' x (descending bitonic sort).
+__device__ __forceinline__ float eighth_of_lanes(float x, int lane) {
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(FULL, incl, o);
-    if (lane >= o) incl += y;
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(FULL, x, j);
+      const bool desc = (lane & k) == 0;
+      const bool low = (lane & j) == 0;
+      x = (low == desc) ? fmaxf(x, o) : fminf(x, o);
+    }
   }
-  const int off = base + incl - n;
-  for (int i = 0; i < n; ++i)
-    if (off + i < cap) list[off + i] = keys[i];
-  return base + __shfl_sync(FULL, incl, 31);
+  return __shfl_sync(FULL, x, K - 1);
+}
+
+// Tree token of row r: from the CTA's shared copy when all rows fit in it.
+__device__ __forceinline__ int32_t row_token(const VerifyArgs& a, const int32_t* stok, bool in_smem, int r) {
+  return in_smem ? stok[r] : __ldcg(a.tree_tok + r);
+}
+
+// Number of valid slots (0 <= token < V) of request b (one warp).
+__device__ __forceinline__ int request_valid(const VerifyArgs& a, const int32_t* stok, bool in_smem, int b,
+                                             int lane) {
+  const int base = b * a.S;
+  bool v0 = false, v1 = false;
+  if (lane < a.S) { const int32_t t = row_token(a, stok, in_smem, base + lane); v0 = t >= 0 && t < a.g.V; }
+  if (lane + 32 < a.S) { const int32_t t = row_token(a, stok, in_smem, base + lane + 32); v1 = t >= 0 && t < a.g.V; }
+  return __popc(__ballot_sync(FULL, v0)) + __popc(__ballot_sync(FULL, v1));
 }
 
 template <int DT>
-__global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a) {
+__global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
   __shared__ u64 cand[SW][CCAP];
+  __shared__ int32_t stok[STOK];
+  __shared__ __align__(16) float smax[SW][TWO_PASS_MAX_UNITS];
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   constexpr int EPL = Vec16<DT>::EPL;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = a.batch * a.S;
   const int row = blockIdx.x * SW + warp;
-  if (row >= a.batch * a.S) return;
-  const int32_t tok = a.tree_tok[row];
-  if (tok < 0 || tok >= a.g.V) return;
+  const bool live = row < rows;
   const ScanGeom& g = a.g;
   const int64_t nslot = g.nslot;
   const int upr = a.upr;
-  const char* rowp = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)g.stride * ES;
+  const char* rowp = reinterpret_cast<const char*>(a.logits) + (size_t)(live ? row : 0) * (size_t)g.stride * ES;
   const uint4* rowv = reinterpret_cast<const uint4*>(rowp);
-  const float* um = a.umax + (size_t)row * upr;
+  const float4* um4 = reinterpret_cast<const float4*>(a.umax + (size_t)(live ? row : 0) * a.ups);
   u64* list = cand[warp];
 
-  // 1. unit maxima; T0 = 8th largest lane maximum: 8 distinct units reach it
-  float m[MPL];
-  float lmax = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < MPL; ++i) {
-    const int u = i * 32 + lane;
-    const float x = u < upr ? __ldcg(um + u) : -INFINITY;
-    m[i] = x == x ? x : -INFINITY;  // NaN rows were flagged by pass 1
-    lmax = fmaxf(lmax, m[i]);
+  // the tree tokens of all rows (last-writer test, request sizes); written
+  // before pass 1 started, so read before waiting for it
+  const bool tok_in_smem = rows <= STOK;
+  if (tok_in_smem) {
+#pragma unroll 8
+    for (int r = threadIdx.x; r < rows; r += SW * 32) stok[r] = __ldcg(a.tree_tok + r);
   }
-  const float T0 = key_val(__shfl_sync(FULL, bitonic32_desc(make_key(lmax, lane), lane), K - 1));
 
-  // 2. exact 8th largest unit maximum T, from the units >= T0 (value, unit) keys
-  bool overflow = T0 == -INFINITY;  // fewer than 8 finite maxima
-  u64 top = 0ull;
-  int nu = 0;
-  if (!overflow) {
-    int n = 0, over = 0;
-    u64 mine[K];
+  // 1. unit maxima; T0 = 8th largest lane maximum.  Eight distinct elements
+  //    (one per lane holding such a maximum) reach T0, so every element of
+  //    the row's top-8 is >= T0 and lies in a unit whose maximum is >= T0.
+  //    Pass 2 runs once per SM and is bound by instruction fetch, so its
+  //    loops stay rolled: the code a warp runs is a few hundred instructions.
+  float lmax = -INFINITY;
+  grid_dependency_wait();  // the unit maxima come from pass 1
+  float* mx = smax[warp];
+  {
+    constexpr int NQ = TWO_PASS_MAX_UNITS / 128;  // float4 loads per lane, all in flight
+    const int n4 = (upr + 3) >> 2;
+    float4 x[NQ];
 #pragma unroll
-    for (int i = 0; i < MPL; ++i) {
-      if (m[i] >= T0) {
-        if (n < K) mine[n] = make_key(m[i], i * 32 + lane);
-        n += 1;
+    for (int k = 0; k < NQ; ++k) {
+      const int i4 = k * 32 + lane;
+      x[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      if (live && i4 < n4) x[k] = __ldcg(um4 + i4);
+    }
+#pragma unroll
+    for (int k = 0; k < NQ; ++k) {
+      const int i4 = k * 32 + lane;
+      if (k * 32 < n4 && i4 < n4) {
+        // units past the row's last are padding; NaN rows were flagged by pass 1
+        float4 y = x[k];
+        y.x = (y.x == y.x) ? y.x : -INFINITY;
+        y.y = (y.y == y.y && 4 * i4 + 1 < upr) ? y.y : -INFINITY;
+        y.z = (y.z == y.z && 4 * i4 + 2 < upr) ? y.z : -INFINITY;
+        y.w = (y.w == y.w && 4 * i4 + 3 < upr) ? y.w : -INFINITY;
+        reinterpret_cast<float4*>(mx)[i4] = y;
+        lmax = fmaxf(lmax, fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
       }
     }
-    over = n > K;
-    n = min(n, K);
-    nu = warp_append(list, CCAP, 0, mine, n, lane);
-    overflow = nu > CCAP || __any_sync(FULL, over);
   }
-  float T = -INFINITY;
+  __syncthreads();
+  // requests with no valid slot have no row to finish them
+  if (warp == 0)
+    for (int b = blockIdx.x; b < a.batch; b += gridDim.x)
+      if (request_valid(a, stok, tok_in_smem, b, lane) == 0) accept_request(a, b, lane, tok_in_smem ? stok : nullptr);
+  if (!live) return;
+  const int32_t tok = row_token(a, stok, tok_in_smem, row);
+  if (tok < 0 || tok >= g.V) return;
+
+  const float T0 = eighth_of_lanes(lmax, lane);
+  bool overflow = !(T0 > -INFINITY);  // fewer than 8 finite unit maxima: tiny or -inf rows
+  u64 top = 0ull;
   if (!overflow) {
-    __syncwarp();
-    const u64 k8 = __shfl_sync(FULL, warp_merge_ool(0ull, list, nu, lane), K - 1);
-    T = key_val(k8);
-    // units with maximum >= T (the 8 largest and any tied with the 8th), as unit ids
-    __syncwarp();
-    int n = 0;
-    int mine[4];
-    for (int q = lane; q < nu && n < 4; q += 32) {
-      const u64 key = list[q];
-      if (key_val(key) >= T) mine[n++] = (int)(0xFFFFFFFFu - (uint32_t)key);
+    // 2. the candidate units (maximum >= T0), listed in shared memory
+    int* ulist = reinterpret_cast<int*>(list + ECAP);
+    const unsigned lt = (1u << lane) - 1u;
+    int nu = 0;
+    for (int u0 = 0; u0 < upr; u0 += 32) {
+      const int u = u0 + lane;
+      const bool c = u < upr && mx[u] >= T0;
+      const unsigned bm = __ballot_sync(FULL, c);
+      const int pos = nu + __popc(bm & lt);
+      if (c && pos < UCAP) ulist[pos] = u;
+      nu += __popc(bm);
     }
-    if (nu > 128) overflow = true;  // more than 4 candidate keys per lane: leave it to the exact rescan
-    __syncwarp();
-    int incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int nunits = __shfl_sync(FULL, incl, 31);
-    int* ulist = reinterpret_cast<int*>(list + CCAP / 2);  // the upper half of the list is free now
-    for (int i = 0; i < n; ++i) ulist[incl - n + i] = mine[i];
+    overflow = nu > UCAP;  // heavy ties at the top: exact rescan below
     __syncwarp();
 
-    // 3. read those units (eight loads in flight per lane); keep elements >= T
+    // 3. read them (UB loads in flight per lane); append every element >= T0:
+    //    per-lane bit masks, one warp scan for the offsets, then each lane
+    //    writes its own (about one element per candidate unit in all)
     int nc = 0;
-    for (int base = 0; base < nunits && !overflow; base += K) {
-      Vec16<DT> v[K];
-      int64_t sl[K];
+    for (int base = 0; base < nu && !overflow; base += UB) {
+      Vec16<DT> v[UB];
+      int32_t sl[UB];
+      unsigned mq[UB];
 #pragma unroll
-      for (int q = 0; q < K; ++q) {
+      for (int q = 0; q < UB; ++q) {
         sl[q] = -1;
-        if (base + q < nunits) {
-          const int64_t s = (int64_t)ulist[base + q] * 32 + lane;
+        if (base + q < nu) {
+          const int32_t s = ulist[base + q] * 32 + lane;
           if (s < nslot) { sl[q] = s; v[q].r = __ldcg(rowv + s); }
         }
       }
+      int cnt = 0;
 #pragma unroll
-      for (int q = 0; q < K; ++q) {
-        u64 keys[EPL];
-        int kn = 0;
-        if (sl[q] >= 0 && v[q].vmax() >= T) {
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            const float x = v[q].elem(e);
-            if (x >= T) keys[kn++] = make_key(x, (int32_t)(sl[q] * EPL + e));
-          }
-        }
-        nc = warp_append(list, CCAP / 2, nc, keys, kn, lane);
+      for (int q = 0; q < UB; ++q) {
+        mq[q] = sl[q] >= 0 ? v[q].ge_mask(T0) : 0u;
+        cnt += __popc(mq[q]);
       }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int total = __shfl_sync(FULL, incl, 31);
+      if (nc + total > ECAP) { overflow = true; break; }
+      int off = nc + incl - cnt;
+#pragma unroll
+      for (int q = 0; q < UB; ++q) {
+        unsigned m = mq[q];
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1;
+          list[off++] = make_key(v[q].elem(e), sl[q] * EPL + e);
+        }
+      }
+      nc += total;
     }
     if (!overflow) {
-      u64 keys[1];
-      int kn = 0;
-      if (lane < g.tail) {  // the row's last V % EPL elements
-        const int32_t id = (int32_t)(nslot * EPL + lane);
-        const float x = load_scalar<DT>(rowp, id);
+      // the row's last V % EPL elements are not in any unit
+      bool c = false;
+      float x = 0.f;
+      const int32_t id = (int32_t)(nslot * EPL + lane);
+      if (lane < g.tail) {
+        x = load_scalar<DT>(rowp, id);
         if (x != x) atomicOr(a.err, GRAFT_ERR_NAN);
-        else if (x >= T) keys[kn++] = make_key(x, id);
+        else c = x >= T0;
       }
-      nc = warp_append(list, CCAP / 2, nc, keys, kn, lane);
-      __syncwarp();
-      if (nc <= CCAP / 2) top = warp_merge_ool(0ull, list, nc, lane);
-      else overflow = true;
+      const unsigned bm = __ballot_sync(FULL, c);
+      const int pos = nc + __popc(bm & lt);
+      if (c && pos < ECAP) list[pos] = make_key(x, id);
+      nc += __popc(bm);
+      overflow = nc > ECAP;
+    }
+    __syncwarp();
+    // 4. top-8 of the candidates: one sort when they fit the warp
+    if (!overflow) {
+      if (nc <= 16) top = bitonic_desc<16>(lane < nc ? list[lane] : 0ull, lane);
+      else if (nc <= 32) top = bitonic_desc<32>(lane < nc ? list[lane] : 0ull, lane);
+      else top = warp_merge_ool(0ull, list, nc, lane);
     }
   }
   if (overflow) top = exact_row<DT>(rowv, nslot, rowp, g.tail, lane);  // ties, tiny rows: exact rescan
-  if (lane < K) a.topk[(size_t)row * K + lane] = key_id(top);
+  const int32_t id = key_id(top);
+  if (lane < K) a.topk[(size_t)row * K + lane] = id;
+
+  // 4. matrix update: this row is its token's last writer unless a later row
+  //    (in (request, slot) order) carries the same token
+  bool later = false;
+#pragma unroll 4
+  for (int r = row + 1 + lane; r < rows; r += 32) later |= row_token(a, stok, tok_in_smem, r) == tok;
+  if (!__any_sync(FULL, later) && lane < K) st_keep(C + (size_t)tok * K + lane, id, l2_keep_policy());
+
+  // 5. the warp that completes the request's last valid row runs acceptance
+  __threadfence();
+  __syncwarp();
+  const int b = row / a.S;
+  const int nv = request_valid(a, stok, tok_in_smem, b, lane);
+  int t = 0;
+  if (lane == 0) t = atomicAdd(&a.req_ticket[b], 1);
+  t = __shfl_sync(FULL, t, 0);
+  if (t == nv - 1) {
+    if (lane == 0) a.req_ticket[b] = 0;
+    __threadfence();
+    accept_request(a, b, lane, tok_in_smem ? stok : nullptr);
+  }
 }
 
 template <int DT>
@@ -294,10 +374,21 @@ cudaError_t umax_impl(const VerifyArgs& a, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 template <int DT>
-cudaError_t select_impl(const VerifyArgs& a, cudaStream_t s) {
+cudaError_t select_impl(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
   const int rows = a.batch * a.S;
-  k_select<DT><<<(rows + SW - 1) / SW, SW * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  // programmatic dependent launch: pass 2's CTAs start as pass 1's leave the
+  // SMs, load the tree tokens, then wait for pass 1's unit maxima
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((rows + SW - 1) / SW);
+  cfg.blockDim = dim3(SW * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_select<DT>, a, C);
 }
 
 }  // namespace
@@ -308,8 +399,8 @@ int two_pass_max_rows(int grid) { return (UMAXROWS - 2) * grid; }
 cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaStream_t s) {
   return dtype == GRAFT_BF16 ? umax_impl<GRAFT_BF16>(a, grid, s) : umax_impl<GRAFT_F32>(a, grid, s);
 }
-cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, cudaStream_t s) {
-  return dtype == GRAFT_BF16 ? select_impl<GRAFT_BF16>(a, s) : select_impl<GRAFT_F32>(a, s);
+cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s) {
+  return dtype == GRAFT_BF16 ? select_impl<GRAFT_BF16>(a, C, s) : select_impl<GRAFT_F32>(a, C, s);
 }
 
 }  // namespace graft

@@ -40,6 +40,22 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 }
 
 // ---- warp helpers ------------------------------------------------------------
+// Bitonic sort of the keys of each group of W lanes; lanes 0..W-1 end up
+// descending (for W = 32: the whole warp).
+template <int W>
+__device__ __forceinline__ u64 bitonic_desc(u64 key, int lane) {
+#pragma unroll
+  for (int k = 2; k <= W; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const u64 o = __shfl_xor_sync(FULL, key, j);
+      const bool desc = (lane & k) == 0;
+      const bool low = (lane & j) == 0;
+      key = (low == desc) ? (key > o ? key : o) : (key < o ? key : o);
+    }
+  }
+  return key;
+}
 __device__ __forceinline__ u64 bitonic32_desc(u64 key, int lane) {
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {
@@ -81,6 +97,17 @@ template <> struct Vec16<GRAFT_BF16> {
     const uint32_t w = (e < 2) ? r.x : (e < 4) ? r.y : (e < 6) ? r.z : r.w;
     return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
   }
+  // bit e set iff elem(e) >= t; t must be a bf16 value (exact in bf16), NaN compares false
+  __device__ __forceinline__ unsigned ge_mask(float t) const {
+    const __nv_bfloat162 t2 = __float2bfloat162_rn(t);
+    const unsigned m0 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&r.x), t2);
+    const unsigned m1 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&r.y), t2);
+    const unsigned m2 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&r.z), t2);
+    const unsigned m3 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&r.w), t2);
+    // low halves (even elements) land on bits 0,2,4,6, high halves on 16,18,20,22
+    const unsigned x = (m0 & 0x10001u) | ((m1 & 0x10001u) << 2) | ((m2 & 0x10001u) << 4) | ((m3 & 0x10001u) << 6);
+    return (x & 0x55u) | ((x >> 15) & 0xAAu);
+  }
 };
 template <> struct Vec16<GRAFT_F32> {
   uint4 r;
@@ -91,6 +118,11 @@ template <> struct Vec16<GRAFT_F32> {
   }
   __device__ __forceinline__ float elem(int e) const {
     return __uint_as_float(e == 0 ? r.x : e == 1 ? r.y : e == 2 ? r.z : r.w);
+  }
+  // bit e set iff elem(e) >= t (NaN compares false)
+  __device__ __forceinline__ unsigned ge_mask(float t) const {
+    return (unsigned)(__uint_as_float(r.x) >= t) | ((unsigned)(__uint_as_float(r.y) >= t) << 1) |
+           ((unsigned)(__uint_as_float(r.z) >= t) << 2) | ((unsigned)(__uint_as_float(r.w) >= t) << 3);
   }
 };
 
@@ -151,7 +183,9 @@ __device__ __forceinline__ u64 warp_merge_global(const u64* src, int cnt, int la
 // The winner is the accepted slot of greatest position (ties: lower slot);
 // its path tokens after the root, then the bonus token argmax(winner), are
 // emitted.
-static __device__ void accept_request(const VerifyArgs& a, int b, int lane) {
+// stok: the tree tokens of all rows in shared memory, or nullptr to read them
+// from global memory.
+static __device__ void accept_request(const VerifyArgs& a, int b, int lane, const int32_t* stok = nullptr) {
   const int S = a.S;
   const size_t base = (size_t)b * S;
   int32_t tk[2], ps[2];
@@ -163,7 +197,7 @@ static __device__ void accept_request(const VerifyArgs& a, int b, int lane) {
     ok[h] = false; mt[h] = false;
     tk[h] = -1; ps[h] = -1; mk[h] = 0ull;
     if (s < S) {
-      tk[h] = a.tree_tok[base + s];
+      tk[h] = stok ? stok[base + s] : a.tree_tok[base + s];
       if (tk[h] >= 0 && tk[h] < a.g.V) {
         ps[h] = a.tree_pos[base + s];
         mk[h] = a.tree_mask[base + s];
@@ -172,7 +206,7 @@ static __device__ void accept_request(const VerifyArgs& a, int b, int lane) {
           mt[h] = ok[h];
         } else {
           const int p = a.tree_parent[base + s];
-          ok[h] = p >= 0 && p < s && a.tree_tok[base + p] >= 0 && ps[h] >= 1 && ps[h] < S;
+          ok[h] = p >= 0 && p < s && (stok ? stok[base + p] : a.tree_tok[base + p]) >= 0 && ps[h] >= 1 && ps[h] < S;
           if (ok[h]) mt[h] = tk[h] == __ldcg(a.topk + (base + p) * K);
         }
         if (!ok[h]) atomicOr(a.err, GRAFT_ERR_TREE);

@@ -468,7 +468,7 @@ def test_profile_api_reports_each_kernel():
     loop.verify_update()
     rec = eng.profile_read()
     names = [n for n, _ in rec]
-    assert names == ["k_assemble", "k_umax", "k_select", "k_finish"], names
+    assert names == ["k_assemble", "k_umax", "k_select"], names
     assert all(ms > 0 for _, ms in rec)
     assert eng.profile_read() == []
     eng.profile_enable(False)
