@@ -12,6 +12,7 @@ constexpr int MAX_S = 64;       // slots per request (one uint64 mask row)
 constexpr int MAX_DRAFT = 256;  // draft nodes per request in one assemble CTA
 constexpr int MAX_SPLIT = 16;   // CTAs per logits row in the verify scan
 constexpr int TMA_CHUNK = 32768; // bytes per pipeline stage of the TMA verify scan
+constexpr int TWO_PASS_MAX_ROWS = 4096;   // verified rows per call on the two-pass scan
 constexpr int TWO_PASS_MAX_UNITS = 1024;  // 512-byte units per row on the two-pass scan (512 KB rows)
 
 // Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth.

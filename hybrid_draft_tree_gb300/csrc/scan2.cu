@@ -27,9 +27,9 @@ namespace {
 using namespace scan;
 
 constexpr int UT = 256;            // pass-1 threads per CTA
+constexpr int UMAXROWS = 192;      // rows one pass-1 CTA's slice may touch
 constexpr int UW = UT / 32;
 constexpr int UNV = 4;             // units (one 16-byte load per lane each) per warp iteration
-constexpr int UMAXROWS = 192;
 constexpr int CCAP = 256;          // shared 64-bit words per warp in pass 2
 constexpr int ECAP = 192;          // candidate elements per row in pass 2
 constexpr int UCAP = 2 * (CCAP - ECAP);  // candidate units per row in pass 2 (int ids after the keys)
@@ -156,7 +156,6 @@ __device__ __noinline__ u64 exact_row(const uint4* rowv, int64_t nslot, const ch
 }
 
 constexpr int SW = 4;  // pass-2 warps per CTA
-constexpr int STOK = 4096;  // tree tokens a pass-2 CTA keeps in shared memory (all rows when they fit)
 
 // Value of the 8th largest of the 32 lanes' x (descending bitonic sort).
 __device__ __forceinline__ float eighth_of_lanes(float x, int lane) {
@@ -173,30 +172,32 @@ __device__ __forceinline__ float eighth_of_lanes(float x, int lane) {
   return __shfl_sync(FULL, x, K - 1);
 }
 
-// Tree token of row r: from the CTA's shared copy when all rows fit in it.
-__device__ __forceinline__ int32_t row_token(const VerifyArgs& a, const int32_t* stok, bool in_smem, int r) {
-  return in_smem ? stok[r] : __ldcg(a.tree_tok + r);
+// *p += 1 with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int ticket_acq_rel(int32_t* p) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
 }
 
-// Number of valid slots (0 <= token < V) of request b (one warp).
-__device__ __forceinline__ int request_valid(const VerifyArgs& a, const int32_t* stok, bool in_smem, int b,
-                                             int lane) {
+// Number of valid slots (0 <= token < V) of request b, from the shared tree
+// tokens (one warp).
+__device__ __forceinline__ int request_valid(const VerifyArgs& a, const int32_t* stok, int b, int lane) {
   const int base = b * a.S;
   bool v0 = false, v1 = false;
-  if (lane < a.S) { const int32_t t = row_token(a, stok, in_smem, base + lane); v0 = t >= 0 && t < a.g.V; }
-  if (lane + 32 < a.S) { const int32_t t = row_token(a, stok, in_smem, base + lane + 32); v1 = t >= 0 && t < a.g.V; }
+  if (lane < a.S) { const int32_t t = stok[base + lane]; v0 = t >= 0 && t < a.g.V; }
+  if (lane + 32 < a.S) { const int32_t t = stok[base + lane + 32]; v1 = t >= 0 && t < a.g.V; }
   return __popc(__ballot_sync(FULL, v0)) + __popc(__ballot_sync(FULL, v1));
 }
 
 template <int DT>
 __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
   __shared__ u64 cand[SW][CCAP];
-  __shared__ int32_t stok[STOK];
-  __shared__ __align__(16) float smax[SW][TWO_PASS_MAX_UNITS];
+  __shared__ int32_t stok[TWO_PASS_MAX_ROWS];
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   constexpr int EPL = Vec16<DT>::EPL;
+  constexpr int NQ = TWO_PASS_MAX_UNITS / 128;  // float4 unit-maxima loads per lane, all in flight
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows = a.batch * a.S;
+  const int rows = a.batch * a.S;  // the host keeps rows <= TWO_PASS_MAX_ROWS
   const int row = blockIdx.x * SW + warp;
   const bool live = row < rows;
   const ScanGeom& g = a.g;
@@ -206,56 +207,58 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
   const uint4* rowv = reinterpret_cast<const uint4*>(rowp);
   const float4* um4 = reinterpret_cast<const float4*>(a.umax + (size_t)(live ? row : 0) * a.ups);
   u64* list = cand[warp];
+  const unsigned lt = (1u << lane) - 1u;
 
   // the tree tokens of all rows (last-writer test, request sizes); written
   // before pass 1 started, so read before waiting for it
-  const bool tok_in_smem = rows <= STOK;
-  if (tok_in_smem) {
 #pragma unroll 8
-    for (int r = threadIdx.x; r < rows; r += SW * 32) stok[r] = __ldcg(a.tree_tok + r);
-  }
+  for (int r = threadIdx.x; r < rows; r += SW * 32) stok[r] = __ldcg(a.tree_tok + r);
 
   // 1. unit maxima; T0 = 8th largest lane maximum.  Eight distinct elements
   //    (one per lane holding such a maximum) reach T0, so every element of
   //    the row's top-8 is >= T0 and lies in a unit whose maximum is >= T0.
-  //    Pass 2 runs once per SM and is bound by instruction fetch, so its
-  //    loops stay rolled: the code a warp runs is a few hundred instructions.
-  float lmax = -INFINITY;
+  //    Lane l holds units 4i..4i+3 for i = l, l + 32, ...
   grid_dependency_wait();  // the unit maxima come from pass 1
-  float* mx = smax[warp];
-  {
-    constexpr int NQ = TWO_PASS_MAX_UNITS / 128;  // float4 loads per lane, all in flight
-    const int n4 = (upr + 3) >> 2;
-    float4 x[NQ];
+  const int n4 = (upr + 3) >> 2;
+  float4 y[NQ];
+  float lmax = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < NQ; ++k) {
-      const int i4 = k * 32 + lane;
-      x[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      if (live && i4 < n4) x[k] = __ldcg(um4 + i4);
-    }
+  for (int k = 0; k < NQ; ++k) {
+    const int i4 = k * 32 + lane;
+    y[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (live && i4 < n4) y[k] = __ldcg(um4 + i4);
+  }
 #pragma unroll
-    for (int k = 0; k < NQ; ++k) {
-      const int i4 = k * 32 + lane;
-      if (k * 32 < n4 && i4 < n4) {
-        // units past the row's last are padding; NaN rows were flagged by pass 1
-        float4 y = x[k];
-        y.x = (y.x == y.x) ? y.x : -INFINITY;
-        y.y = (y.y == y.y && 4 * i4 + 1 < upr) ? y.y : -INFINITY;
-        y.z = (y.z == y.z && 4 * i4 + 2 < upr) ? y.z : -INFINITY;
-        y.w = (y.w == y.w && 4 * i4 + 3 < upr) ? y.w : -INFINITY;
-        reinterpret_cast<float4*>(mx)[i4] = y;
-        lmax = fmaxf(lmax, fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
-      }
-    }
+  for (int k = 0; k < NQ; ++k) {
+    // units past the row's last are padding; NaN rows were flagged by pass 1
+    const int u = 4 * (k * 32 + lane);
+    y[k].x = (y[k].x == y[k].x) ? y[k].x : -INFINITY;
+    y[k].y = (y[k].y == y[k].y && u + 1 < upr) ? y[k].y : -INFINITY;
+    y[k].z = (y[k].z == y[k].z && u + 2 < upr) ? y[k].z : -INFINITY;
+    y[k].w = (y[k].w == y[k].w && u + 3 < upr) ? y[k].w : -INFINITY;
+    lmax = fmaxf(lmax, fmaxf(fmaxf(y[k].x, y[k].y), fmaxf(y[k].z, y[k].w)));
   }
   __syncthreads();
   // requests with no valid slot have no row to finish them
   if (warp == 0)
     for (int b = blockIdx.x; b < a.batch; b += gridDim.x)
-      if (request_valid(a, stok, tok_in_smem, b, lane) == 0) accept_request(a, b, lane, tok_in_smem ? stok : nullptr);
+      if (request_valid(a, stok, b, lane) == 0) accept_request(a, b, lane, stok);
   if (!live) return;
-  const int32_t tok = row_token(a, stok, tok_in_smem, row);
+  const int32_t tok = stok[row];
   if (tok < 0 || tok >= g.V) return;
+
+  // last-writer test and request size: shared-memory work, done while the
+  // candidate units are in flight (or before the exact rescan)
+  bool later = false;
+  int nv = 0;
+  bool have_lw = false;
+  auto writer_and_size = [&]() {
+#pragma unroll 4
+    for (int r = row + 1 + lane; r < rows; r += 32) later |= stok[r] == tok;
+    later = __any_sync(FULL, later);
+    nv = request_valid(a, stok, row / a.S, lane);
+    have_lw = true;
+  };
 
   const float T0 = eighth_of_lanes(lmax, lane);
   bool overflow = !(T0 > -INFINITY);  // fewer than 8 finite unit maxima: tiny or -inf rows
@@ -263,17 +266,29 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
   if (!overflow) {
     // 2. the candidate units (maximum >= T0), listed in shared memory
     int* ulist = reinterpret_cast<int*>(list + ECAP);
-    const unsigned lt = (1u << lane) - 1u;
-    int nu = 0;
-    for (int u0 = 0; u0 < upr; u0 += 32) {
-      const int u = u0 + lane;
-      const bool c = u < upr && mx[u] >= T0;
-      const unsigned bm = __ballot_sync(FULL, c);
-      const int pos = nu + __popc(bm & lt);
-      if (c && pos < UCAP) ulist[pos] = u;
-      nu += __popc(bm);
+    int cu = 0;
+#pragma unroll
+    for (int k = 0; k < NQ; ++k)
+      cu += (y[k].x >= T0) + (y[k].y >= T0) + (y[k].z >= T0) + (y[k].w >= T0);
+    int incl = cu;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int z = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += z;
     }
+    const int nu = __shfl_sync(FULL, incl, 31);
     overflow = nu > UCAP;  // heavy ties at the top: exact rescan below
+    if (!overflow && cu > 0) {
+      int off = incl - cu;
+#pragma unroll
+      for (int k = 0; k < NQ; ++k) {
+        const int u = 4 * (k * 32 + lane);
+        if (y[k].x >= T0) ulist[off++] = u;
+        if (y[k].y >= T0) ulist[off++] = u + 1;
+        if (y[k].z >= T0) ulist[off++] = u + 2;
+        if (y[k].w >= T0) ulist[off++] = u + 3;
+      }
+    }
     __syncwarp();
 
     // 3. read them (UB loads in flight per lane); append every element >= T0:
@@ -292,21 +307,22 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
           if (s < nslot) { sl[q] = s; v[q].r = __ldcg(rowv + s); }
         }
       }
+      if (!have_lw) writer_and_size();
       int cnt = 0;
 #pragma unroll
       for (int q = 0; q < UB; ++q) {
         mq[q] = sl[q] >= 0 ? v[q].ge_mask(T0) : 0u;
         cnt += __popc(mq[q]);
       }
-      int incl = cnt;
+      int inc = cnt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o) incl += y;
+        const int z = __shfl_up_sync(FULL, inc, o);
+        if (lane >= o) inc += z;
       }
-      const int total = __shfl_sync(FULL, incl, 31);
+      const int total = __shfl_sync(FULL, inc, 31);
       if (nc + total > ECAP) { overflow = true; break; }
-      int off = nc + incl - cnt;
+      int off = nc + inc - cnt;
 #pragma unroll
       for (int q = 0; q < UB; ++q) {
         unsigned m = mq[q];
@@ -342,29 +358,27 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
       else top = warp_merge_ool(0ull, list, nc, lane);
     }
   }
+  if (!have_lw) writer_and_size();
   if (overflow) top = exact_row<DT>(rowv, nslot, rowp, g.tail, lane);  // ties, tiny rows: exact rescan
   const int32_t id = key_id(top);
   if (lane < K) a.topk[(size_t)row * K + lane] = id;
 
-  // 4. matrix update: this row is its token's last writer unless a later row
+  // 5. matrix update: this row is its token's last writer unless a later row
   //    (in (request, slot) order) carries the same token
-  bool later = false;
-#pragma unroll 4
-  for (int r = row + 1 + lane; r < rows; r += 32) later |= row_token(a, stok, tok_in_smem, r) == tok;
-  if (!__any_sync(FULL, later) && lane < K) st_keep(C + (size_t)tok * K + lane, id, l2_keep_policy());
+  if (!later && lane < K) st_keep(C + (size_t)tok * K + lane, id, l2_keep_policy());
 
-  // 5. the warp that completes the request's last valid row runs acceptance
-  __threadfence();
+  // 6. the warp that completes the request's last valid row runs acceptance:
+  //    the warp's writes are released by lane 0's ticket increment, and the
+  //    last incrementer acquires every other row's
   __syncwarp();
   const int b = row / a.S;
-  const int nv = request_valid(a, stok, tok_in_smem, b, lane);
   int t = 0;
-  if (lane == 0) t = atomicAdd(&a.req_ticket[b], 1);
+  if (lane == 0) t = ticket_acq_rel(&a.req_ticket[b]);
   t = __shfl_sync(FULL, t, 0);
   if (t == nv - 1) {
     if (lane == 0) a.req_ticket[b] = 0;
-    __threadfence();
-    accept_request(a, b, lane, tok_in_smem ? stok : nullptr);
+    __syncwarp();
+    accept_request(a, b, lane, stok);
   }
 }
 
@@ -394,7 +408,7 @@ cudaError_t select_impl(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
 }  // namespace
 
 int two_pass_ctas_per_sm() { return 4; }
-int two_pass_max_rows(int grid) { return (UMAXROWS - 2) * grid; }
+int two_pass_max_rows(int grid) { return min(TWO_PASS_MAX_ROWS, (UMAXROWS - 2) * grid); }
 
 cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaStream_t s) {
   return dtype == GRAFT_BF16 ? umax_impl<GRAFT_BF16>(a, grid, s) : umax_impl<GRAFT_F32>(a, grid, s);
