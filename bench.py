@@ -175,7 +175,11 @@ def traffic_record(kernel):
         rec = json.load(f).get(kernel)
     if not rec:
         return None
-    src = open(os.path.join(ROOT, "hybrid_draft_tree_gb300", "csrc", rec["source"]), "rb").read()
+    path = os.path.join(ROOT, "hybrid_draft_tree_gb300", "csrc", rec["source"])
+    if not os.path.exists(path):
+        return None
+    with open(path, "rb") as f:
+        src = f.read()
     if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
         return None
     return rec

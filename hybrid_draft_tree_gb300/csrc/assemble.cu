@@ -14,6 +14,7 @@ namespace graft {
 namespace {
 
 constexpr int AT = 256;  // threads per CTA (>= MAX_DRAFT, >= MAX_S)
+constexpr int WALK = 8;  // ancestors a node walks for its path confidence (deeper trees: layer passes)
 
 __device__ __forceinline__ void raise_err(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
 
@@ -45,6 +46,8 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   __shared__ int32_t s_tok[MAX_DRAFT];
   __shared__ int32_t s_par[MAX_DRAFT];
   __shared__ float s_conf[MAX_DRAFT];
+  __shared__ float s_prob[MAX_DRAFT];
+  __shared__ int s_cnt0[MAX_S];
   __shared__ int32_t s_depth[MAX_DRAFT];
   __shared__ int32_t s_slot[MAX_DRAFT];
   __shared__ __align__(16) unsigned long long s_key[MAX_DRAFT];
@@ -60,7 +63,9 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   const uint64_t keep = l2_keep_policy();
   if (t == 0) { s_bad = 0; s_tcut = n; s_maxdepth = 0; }
   if (t < 3) s_best[t] = -1;
-  if (t < MAX_S) { o_tok[t] = -1; o_par[t] = -1; o_pos[t] = -1; o_rep[t] = 0; s_rtok[t] = -1; s_rslot[t] = -1; }
+  if (t < MAX_S) {
+    o_tok[t] = -1; o_par[t] = -1; o_pos[t] = -1; o_rep[t] = 0; s_rtok[t] = -1; s_rslot[t] = -1; s_cnt0[t] = 0;
+  }
   __syncthreads();
 
   // ---- load and validate -------------------------------------------------
@@ -72,6 +77,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
     s_tok[t] = tk;
     if (tk < 0 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); s_bad = 1; }
     prob = a.draft_aux[k];
+    s_prob[t] = prob;
     if (a.mode != GRAFT_MODE_TAIL) {
       const int p = a.draft_parent[k];
       s_par[t] = p;
@@ -94,9 +100,40 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   int32_t anchor_tok = root;
 
   if (a.mode != GRAFT_MODE_TAIL) {
-    // ---- path confidence, root to leaf, one layer per pass (gear 1) -------
+    // ---- path confidence, root to leaf (gear 1) ---------------------------
+    // Each node walks up to WALK ancestors and multiplies their probabilities
+    // root first: the same fp32 products, in the same order, as computing one
+    // layer after the other.  Trees deeper than WALK take the layer passes.
     int my_depth = -1;
-    for (int pass = 0; pass <= nn; ++pass) {
+    bool deep = false;
+    if (t < nn) {
+      float pr[WALK];  // pr[i]: probability of the ancestor i levels up (pr[0]: this node)
+      int p = t, d = 0;
+#pragma unroll
+      for (int i = 0; i < WALK; ++i) {
+        const bool in = p >= 0;
+        const int q = in ? p : 0;
+        pr[i] = in ? s_prob[q] : 1.f;
+        d += in;
+        p = in ? s_par[q] : -1;
+      }
+      deep = p >= 0;
+      if (!deep) {
+        float c = 0.f;
+#pragma unroll
+        for (int k = 0; k < WALK; ++k) {
+          const int i = WALK - 1 - k;
+          const float x = (i == d - 1) ? pr[i] : __fmul_rn(c, pr[i]);
+          c = (i < d) ? (x == 0.f ? 0.f : x) : c;  // -0 is stored as +0, as below
+        }
+        s_conf[t] = c;
+        my_depth = d - 1;
+      }
+    }
+    // (uniform: every thread takes the passes or none does)
+    const bool layered = __syncthreads_or(deep);
+    if (layered) my_depth = -1;
+    for (int pass = 0; layered && pass <= nn; ++pass) {
       float nc = 0.f;
       int nd = -1;
       if (t < nn && my_depth < 0) {
@@ -153,6 +190,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
       int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // independent accumulators: the loads overlap
       const int pairs = (nn + 1) / 2;      // s_key[nn] is 0 when nn is odd
       int j = 0;
+#pragma unroll 4
       for (; j + 2 <= pairs; j += 2) {
         const ulonglong2 x = k2[j], y = k2[j + 1];
         r0 += x.x > mine;
@@ -195,12 +233,19 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
       const int used = 1 + n_draft;
       const int maxpos = s_maxdepth + 1;
       const int nrep_local = (t >= 1 && t < used) ? o_rep[t] : 0;
-      // rank of a replaced slot among its parent's replaced children (slot order)
+      // rank of a replaced slot among its parent's replaced children (slot
+      // order): lanes of one warp with the same parent match, and warp 1 adds
+      // the count of warp 0 (all slots are in warps 0 and 1)
       int srank = 0;
-      if (t >= 1 && t < used && o_rep[t]) {
-        const int p = o_par[t];
-        for (int q = 1; q < t; ++q) srank += (o_par[q] == p) && (o_rep[q] != 0);
+      const bool rep_me = t >= 1 && t < used && o_rep[t] != 0;
+      const int pkey = rep_me ? o_par[t] : -2 - t;  // replaced slots match on their parent
+      if (t < MAX_S) {
+        const unsigned same = __match_any_sync(0xffffffffu, pkey);
+        srank = __popc(same & ((1u << (t & 31)) - 1u));
+        if (t < 32 && rep_me && (same >> t) == 1u) s_cnt0[pkey] = __popc(same);  // the group's last lane
       }
+      __syncthreads();
+      if (t >= 32 && rep_me) srank += s_cnt0[pkey];
       for (int level = 1; level <= maxpos; ++level) {
         if (t >= 1 && t < used && o_pos[t] == level && o_rep[t]) {
           const int p = o_par[t];

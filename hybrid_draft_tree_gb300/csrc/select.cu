@@ -1,22 +1,16 @@
-// Two-pass verify scan for 16-byte aligned logits rows (the default path).
+// Pass 2 of the two-pass verify scan: exact top-8 of every verified row from
+// the unit maxima of pass 1 (umax.cu), then the row's share of the update and
+// the request's acceptance.
 //
-// The verify + update pass of a Graft step (popular-science article on arXiv
-// 2605.20104, section 二 third gear) needs, for every verified slot, the top-8
-// of its logits row (element 0 = the greedy argmax).  Selection work on the
-// streaming path costs memory parallelism, so it is moved off it:
-//
-// Pass 1 (k_umax): a persistent grid streams the valid rows once, in equal
-//   contiguous slices, with 16-byte evict-first loads, and writes only the
-//   maximum of every 512-byte unit (32 lanes x 16 bytes): 1/128 of the bytes
-//   read.  No shared state, no barriers on the stream.
-// Pass 2 (k_select): one warp per row reads the row's unit maxima.  The 8th
-//   largest of them, T, is reached by 8 distinct elements, so every element of
-//   the row's top-8 is >= T and lies in a unit whose maximum is >= T.  The
-//   warp re-reads only those units (about 8 of ~600 for V = 151936), keeps
-//   the elements >= T and sorts them (64-bit keys, value desc, id asc).
-// Pass 2 also finishes: a row writes C[its token] when no later row (in
-// (request, slot) order) carries the same token, and the warp that completes
-// the last valid row of a request (atomic ticket) runs its acceptance.
+// One warp per row reads the row's unit maxima.  T0, the 8th largest of the
+// 32 lanes' maxima, is reached by 8 distinct elements, so every element of the
+// row's top-8 is >= T0 and lies in a unit whose maximum is >= T0.  The warp
+// re-reads only those units (about 9 of 594 for V = 151936 bf16), keeps the
+// elements >= T0 and sorts them (64-bit keys, value desc, id asc).  Then
+// (popular-science article on arXiv 2605.20104, section 二 third gear): a row
+// writes C[its token] when no later row in (request, slot) order carries the
+// same token, and the warp that completes the last valid row of a request
+// (atomic ticket) runs its greedy acceptance.
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -26,108 +20,11 @@ namespace graft {
 namespace {
 using namespace scan;
 
-constexpr int UT = 256;            // pass-1 threads per CTA
-constexpr int UMAXROWS = 192;      // rows one pass-1 CTA's slice may touch
-constexpr int UW = UT / 32;
-constexpr int UNV = 4;             // units (one 16-byte load per lane each) per warp iteration
-constexpr int CCAP = 256;          // shared 64-bit words per warp in pass 2
-constexpr int ECAP = 192;          // candidate elements per row in pass 2
-constexpr int UCAP = 2 * (CCAP - ECAP);  // candidate units per row in pass 2 (int ids after the keys)
+constexpr int CCAP = 256;          // shared 64-bit words per warp
+constexpr int ECAP = 192;          // candidate elements per row
+constexpr int UCAP = 2 * (CCAP - ECAP);  // candidate units per row (int ids after the keys)
 constexpr int UB = 16;             // candidate units loaded at once per lane
 
-__device__ __forceinline__ uint4 neg_inf_vec(int dt) {
-  const uint32_t w = dt == GRAFT_BF16 ? 0xFF80FF80u : 0xFF800000u;
-  return make_uint4(w, w, w, w);
-}
-
-// ---- pass 1: unit maxima -----------------------------------------------------------
-template <int DT>
-__global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a) {
-  __shared__ int warpsum[UW];
-  __shared__ int rowlist[UMAXROWS];
-  grid_dependents_launch();  // pass 2 may be scheduled as SMs free up; it waits for this grid's results
-  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const ScanGeom& g = a.g;
-  const int rows = a.batch * a.S;
-  const int64_t nslot = g.nslot;
-  const int64_t upr = a.upr;
-
-  // compact the valid rows (same result in every CTA)
-  const int per = (rows + UT - 1) / UT;
-  const int r0 = min(tid * per, rows), r1 = min(r0 + per, rows);
-  int cnt = 0;
-  for (int r = r0; r < r1; ++r) {
-    const int32_t t = a.tree_tok[r];
-    cnt += (t >= 0 && t < g.V);
-    if (t >= g.V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
-  }
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(FULL, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warpsum[warp] = incl;
-  __syncthreads();
-  int wbase = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < UW; ++w) {
-    const int x = warpsum[w];
-    wbase += (w < warp) ? x : 0;
-    total += x;
-  }
-  const int64_t NU = (int64_t)total * upr;
-  if (NU == 0) return;
-  const int Ge = (int)min((int64_t)gridDim.x, NU);
-  const int c = blockIdx.x;
-  if (c >= Ge) return;
-  const int64_t u0 = (int64_t)c * NU / Ge, u1 = (int64_t)(c + 1) * NU / Ge;
-  const int64_t k0 = u0 / upr, klast = (u1 - 1) / upr;
-  if (klast - k0 + 1 > UMAXROWS) {  // the host keeps rows <= (UMAXROWS - 2) * grid
-    if (tid == 0) atomicOr(a.err, GRAFT_ERR_TREE);
-    return;
-  }
-  int64_t vidx = wbase + incl - cnt;
-  for (int r = r0; r < r1; ++r) {
-    const int32_t t = a.tree_tok[r];
-    if (t >= 0 && t < g.V) {
-      if (vidx >= k0 && vidx <= klast) rowlist[vidx - k0] = r;
-      ++vidx;
-    }
-  }
-  __syncthreads();
-
-  for (int64_t k = k0; k <= klast; ++k) {
-    const int row = rowlist[k - k0];
-    const int64_t ulo = max(u0, k * upr) - k * upr, uhi = min(u1, (k + 1) * upr) - k * upr;
-    const uint4* rowv = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(a.logits) +
-                                                       (size_t)row * (size_t)g.stride * ES);
-    float* um = a.umax + (size_t)row * a.ups;
-    for (int64_t ub = ulo + (int64_t)warp * UNV; ub < uhi; ub += (int64_t)UW * UNV) {
-      Vec16<DT> v[UNV];
-      if (ub + UNV <= uhi && (ub + UNV) * 32 <= nslot) {
-#pragma unroll
-        for (int kk = 0; kk < UNV; ++kk) v[kk].r = __ldcs(rowv + (ub + kk) * 32 + lane);
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < UNV; ++kk) {
-          const int64_t s = (ub + kk) * 32 + lane;
-          v[kk].r = (ub + kk < uhi && s < nslot) ? __ldcs(rowv + s) : neg_inf_vec(DT);
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < UNV; ++kk) {
-        const float m = v[kk].vmax();
-        if (m != m) atomicOr(a.err, GRAFT_ERR_NAN);
-        const int32_t mi = __reduce_max_sync(FULL, ord_int(m));
-        if (lane == kk && ub + kk < uhi) um[ub + kk] = from_ord_int(mi);
-      }
-    }
-  }
-}
-
-// ---- pass 2: exact top-8 of each row from its candidate units ---------------------
 template <int DT>
 __device__ __noinline__ u64 exact_row(const uint4* rowv, int64_t nslot, const char* rowp, int tail, int lane) {
   constexpr int EPL = Vec16<DT>::EPL;
@@ -383,11 +280,6 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
 }
 
 template <int DT>
-cudaError_t umax_impl(const VerifyArgs& a, int grid, cudaStream_t s) {
-  k_umax<DT><<<grid, UT, 0, s>>>(a);
-  return cudaGetLastError();
-}
-template <int DT>
 cudaError_t select_impl(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
   const int rows = a.batch * a.S;
   // programmatic dependent launch: pass 2's CTAs start as pass 1's leave the
@@ -407,12 +299,6 @@ cudaError_t select_impl(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
 
 }  // namespace
 
-int two_pass_ctas_per_sm() { return 4; }
-int two_pass_max_rows(int grid) { return min(TWO_PASS_MAX_ROWS, (UMAXROWS - 2) * grid); }
-
-cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaStream_t s) {
-  return dtype == GRAFT_BF16 ? umax_impl<GRAFT_BF16>(a, grid, s) : umax_impl<GRAFT_F32>(a, grid, s);
-}
 cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s) {
   return dtype == GRAFT_BF16 ? select_impl<GRAFT_BF16>(a, C, s) : select_impl<GRAFT_F32>(a, C, s);
 }

@@ -157,8 +157,9 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
  * whose device memory is fully pre-planned by its own arena or by another
  * runtime's caching allocator.  Those callers cannot create a graft_handle,
  * so this call takes the continuation matrix as a caller buffer and runs the
- * same kernels as graft_verify_update on fixed scratch memory compiled into
- * the library.
+ * single-pass scan and finishing kernels (graft_verify_update's path for
+ * unaligned rows; same results) on fixed scratch memory compiled into the
+ * library.
  *   vocab, logits_dtype      as in graft_config
  *   batch, slots             requests and slots per request (S); batch * slots
  *                            must be <= GRAFT_NOALLOC_MAX_ROWS, slots <= 64

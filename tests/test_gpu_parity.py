@@ -291,6 +291,25 @@ def test_assemble_degenerate_probabilities(mode, seed):
     _assemble_case(mode, tok, par, prob, C, int(root[0]), V)
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("shape", ["chain8", "chain9", "chain40", "deep_random"])
+def test_assemble_deep_trees(mode, shape):
+    """Trees whose depth reaches and passes the eight ancestors a node walks
+    for its path confidence (deeper ones take the layer-by-layer passes)."""
+    rng = np.random.default_rng(len(shape) + 10 * mode)
+    V = 400
+    if shape.startswith("chain"):
+        n = int(shape[5:])
+        par = np.arange(-1, n - 1, dtype=np.int16)
+    else:
+        n = 120
+        par = np.array([-1] + [int(rng.integers(max(0, i - 3), i)) for i in range(1, n)], np.int16)
+    tok = rng.integers(0, V, n).astype(np.int32)
+    prob = rng.choice(np.array([1.0, 0.97, 0.9, 0.5, 0.25], np.float32), n)
+    C = rng.integers(-1, V, (V, 8)).astype(np.int32)
+    _assemble_case(mode, tok, par, prob, C, 3, V)
+
+
 def test_assemble_tail_degenerate():
     V = 300
     rng = np.random.default_rng(5)
