@@ -76,6 +76,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
     const int32_t tk = a.draft_tok[k];
     s_tok[t] = tk;
     if (tk < 0 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); s_bad = 1; }
+    else prefetch_keep(a.C + (int64_t)tk * K);  // matrix rows the first gathers may read
     prob = a.draft_aux[k];
     s_prob[t] = prob;
     if (a.mode != GRAFT_MODE_TAIL) {
@@ -91,6 +92,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   }
   const bool root_ok = root >= 0 && root < a.V;
   if (t == 0 && !root_ok) raise_err(a.err, GRAFT_ERR_TOKEN);
+  if (t == 0 && root_ok) prefetch_keep(a.C + (int64_t)root * K);
   __syncthreads();
   const bool bad = s_bad != 0 || !root_ok;
   const int nn = bad ? 0 : n;   // a request with bad input degrades to its root only

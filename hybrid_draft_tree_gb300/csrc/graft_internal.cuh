@@ -114,6 +114,10 @@ __device__ __forceinline__ uint64_t l2_keep_policy() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// Fetch the line holding ptr into L2 with the evict-last priority (no data returned).
+__device__ __forceinline__ void prefetch_keep(const void* ptr) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(ptr));
+}
 __device__ __forceinline__ int32_t ld_keep(const int32_t* ptr, uint64_t pol) {
   int32_t v;
   asm volatile("ld.global.L2::cache_hint.s32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol) : "memory");

@@ -11,6 +11,8 @@
 // writes C[its token] when no later row in (request, slot) order carries the
 // same token, and the warp that completes the last valid row of a request
 // (atomic ticket) runs its greedy acceptance.
+#include <climits>
+
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -54,19 +56,21 @@ __device__ __noinline__ u64 exact_row(const uint4* rowv, int64_t nslot, const ch
 
 constexpr int SW = 4;  // pass-2 warps per CTA
 
-// Value of the 8th largest of the 32 lanes' x (descending bitonic sort).
+// Value of the 8th largest of the 32 lanes' x: seven rounds remove the
+// current maximum (one lane each, the lowest on ties), the eighth reads it.
+// x must not be NaN.
 __device__ __forceinline__ float eighth_of_lanes(float x, int lane) {
+  int32_t k = ord_int(x);
+  int32_t m = 0;
 #pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float o = __shfl_xor_sync(FULL, x, j);
-      const bool desc = (lane & k) == 0;
-      const bool low = (lane & j) == 0;
-      x = (low == desc) ? fmaxf(x, o) : fminf(x, o);
+  for (int r = 0; r < K; ++r) {
+    m = __reduce_max_sync(FULL, k);
+    if (r < K - 1) {
+      const unsigned owner = __ffs(__ballot_sync(FULL, k == m)) - 1;
+      if (lane == (int)owner) k = INT_MIN;
     }
   }
-  return __shfl_sync(FULL, x, K - 1);
+  return from_ord_int(m);
 }
 
 // *p += 1 with acquire-release semantics at GPU scope; returns the old value.
@@ -86,10 +90,89 @@ __device__ __forceinline__ int request_valid(const VerifyArgs& a, const int32_t*
   return __popc(__ballot_sync(FULL, v0)) + __popc(__ballot_sync(FULL, v1));
 }
 
+// Greedy acceptance of request b (one warp) from tree arrays staged in shared
+// memory (sp/spos/smask indexed by slot): match(i) = slot i is valid and is the
+// root or carries its parent's argmax; accepted(i) <=> mask_i & ~match == 0;
+// the winner is the accepted slot of greatest position (ties: lower slot); its
+// path tokens after the root, then the bonus token argmax(winner), are emitted.
+// The argmax of every slot's row is fetched in one round trip to L2.
+__device__ __forceinline__ void accept_staged(const VerifyArgs& a, int b, int lane, const int32_t* stok,
+                                           const int8_t* sp, const int32_t* spos, const uint64_t* smask) {
+  const int S = a.S;
+  const size_t base = (size_t)b * S;
+  int32_t tk[2], ps[2], am[2], pp[2];
+  uint64_t mk[2];
+  bool ok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    tk[h] = s < S ? stok[base + s] : -1;  // raw: a token >= V (flagged by pass 1) still counts as a node
+    const bool v = tk[h] >= 0 && tk[h] < a.g.V;
+    am[h] = v ? __ldcg(a.topk + (base + s) * K) : -1;
+    ps[h] = v ? spos[s] : -1;
+    mk[h] = v ? smask[s] : 0ull;
+    pp[h] = v && s > 0 ? (int)sp[s] : -1;
+  }
+  bool mt[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    const int p = pp[h];
+    const int q = p >= 0 ? p : 0;
+    const int32_t pa0 = __shfl_sync(FULL, am[0], q & 31), pa1 = __shfl_sync(FULL, am[1], q & 31);
+    const int32_t ptk0 = __shfl_sync(FULL, tk[0], q & 31), ptk1 = __shfl_sync(FULL, tk[1], q & 31);
+    const int32_t pam = q < 32 ? pa0 : pa1, ptk = q < 32 ? ptk0 : ptk1;
+    ok[h] = false;
+    mt[h] = false;
+    if (tk[h] >= 0 && tk[h] < a.g.V) {
+      if (s == 0) {
+        ok[h] = ps[h] == 0;
+        mt[h] = ok[h];
+      } else {
+        ok[h] = p >= 0 && p < s && ptk >= 0 && ps[h] >= 1 && ps[h] < S;
+        mt[h] = ok[h] && tk[h] == pam;
+      }
+      if (!ok[h]) atomicOr(a.err, GRAFT_ERR_TREE);
+    }
+  }
+  const uint64_t match = (uint64_t)__ballot_sync(FULL, mt[0]) | ((uint64_t)__ballot_sync(FULL, mt[1]) << 32);
+  int wkey = -1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    if (ok[h] && ((mk[h] >> s) & 1ull) && (mk[h] & ~match) == 0ull) wkey = max(wkey, (ps[h] << 8) | (255 - s));
+  }
+  wkey = __reduce_max_sync(FULL, wkey);
+  int32_t* out = a.out_tokens + base;
+  if (wkey < 0) {  // no valid root: nothing accepted, nothing emitted
+    for (int j = lane; j < S; j += 32) out[j] = -1;
+    if (lane == 0) a.accept_len[b] = 0;
+    return;
+  }
+  const int w = 255 - (wkey & 255);
+  const int L = wkey >> 8;
+  const uint64_t mw = smask[w];
+  const int32_t bonus0 = __shfl_sync(FULL, am[0], w & 31), bonus1 = __shfl_sync(FULL, am[1], w & 31);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    if (s > 0 && ok[h] && ((mw >> s) & 1ull) && ps[h] <= L) out[ps[h] - 1] = tk[h];
+  }
+  for (int j = lane; j < S; j += 32)
+    if (j > L) out[j] = -1;
+  if (lane == 0) {
+    out[L] = w < 32 ? bonus0 : bonus1;
+    a.accept_len[b] = L;
+  }
+}
+
 template <int DT>
 __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
   __shared__ u64 cand[SW][CCAP];
   __shared__ int32_t stok[TWO_PASS_MAX_ROWS];
+  __shared__ uint64_t smask[SW * MAX_S];  // tree arrays of the requests this CTA's rows belong to
+  __shared__ int32_t spos[SW * MAX_S];
+  __shared__ int8_t spar[SW * MAX_S];
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   constexpr int EPL = Vec16<DT>::EPL;
   constexpr int NQ = TWO_PASS_MAX_UNITS / 128;  // float4 unit-maxima loads per lane, all in flight
@@ -110,6 +193,18 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
   // before pass 1 started, so read before waiting for it
 #pragma unroll 8
   for (int r = threadIdx.x; r < rows; r += SW * 32) stok[r] = __ldcg(a.tree_tok + r);
+  // the other tree arrays of the (at most SW) requests this CTA's rows belong
+  // to, for the acceptance of whichever of them completes here
+  const int b_lo = min(blockIdx.x * SW, rows - 1) / a.S;
+  const int b_hi = (min(blockIdx.x * SW + SW, rows) - 1) / a.S;
+  {
+    const int n_st = (b_hi - b_lo + 1) * a.S, r0 = b_lo * a.S;
+    for (int i = threadIdx.x; i < n_st; i += SW * 32) {
+      spar[i] = __ldcg(a.tree_parent + r0 + i);
+      spos[i] = __ldcg(a.tree_pos + r0 + i);
+      smask[i] = __ldcg(reinterpret_cast<const unsigned long long*>(a.tree_mask) + r0 + i);
+    }
+  }
 
   // 1. unit maxima; T0 = 8th largest lane maximum.  Eight distinct elements
   //    (one per lane holding such a maximum) reach T0, so every element of
@@ -205,9 +300,11 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
         }
       }
       if (!have_lw) writer_and_size();
+      const int nq = min(UB, nu - base);  // candidates in this batch (warp-uniform)
       int cnt = 0;
 #pragma unroll
       for (int q = 0; q < UB; ++q) {
+        if (q >= nq) break;
         mq[q] = sl[q] >= 0 ? v[q].ge_mask(T0) : 0u;
         cnt += __popc(mq[q]);
       }
@@ -222,6 +319,7 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
       int off = nc + inc - cnt;
 #pragma unroll
       for (int q = 0; q < UB; ++q) {
+        if (q >= nq) break;
         unsigned m = mq[q];
         while (m) {
           const int e = __ffs(m) - 1;
@@ -275,7 +373,8 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
   if (t == nv - 1) {
     if (lane == 0) a.req_ticket[b] = 0;
     __syncwarp();
-    accept_request(a, b, lane, stok);
+    const int o = (b - b_lo) * a.S;
+    accept_staged(a, b, lane, stok, spar + o, spos + o, smask + o);
   }
 }
 
