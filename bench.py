@@ -26,6 +26,7 @@ import platform
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -50,6 +51,7 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--scan-kernel", type=int, default=0, help="verify scan (graft_config.scan_kernel); 0 = automatic")
     return p.parse_args()
 
 
@@ -116,7 +118,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples go to $GRAFT_CLOCKS_DIR (kept) or the temp directory
+        d = os.environ.get("GRAFT_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
@@ -208,7 +212,8 @@ def run_graft(args, ws, rank, local):
     w = W.WORKLOADS[args.workload]
     if rank:
         w = w.scaled(seed=w.seed + 1000 * rank)
-    eng = g.Graft(g.graft_default_config(w.V, w.B, w.mode, w.dtype, budget=w.budget, max_draft_nodes=w.draft_nodes))
+    eng = g.Graft(g.graft_default_config(w.V, w.B, w.mode, w.dtype, budget=w.budget, max_draft_nodes=w.draft_nodes,
+                                         scan_kernel=args.scan_kernel))
     stream = torch.cuda.Stream(dev)
     loop = DeviceLoop(w, eng, device=dev, stream=stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)

@@ -11,8 +11,6 @@
 // writes C[its token] when no later row in (request, slot) order carries the
 // same token, and the warp that completes the last valid row of a request
 // (atomic ticket) runs its greedy acceptance.
-#include <climits>
-
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -27,68 +25,7 @@ constexpr int ECAP = 192;          // candidate elements per row
 constexpr int UCAP = 2 * (CCAP - ECAP);  // candidate units per row (int ids after the keys)
 constexpr int UB = 16;             // candidate units loaded at once per lane
 
-template <int DT>
-__device__ __noinline__ u64 exact_row(const uint4* rowv, int64_t nslot, const char* rowp, int tail, int lane) {
-  constexpr int EPL = Vec16<DT>::EPL;
-  u64 prev = ~0ull, out = 0ull;
-  for (int r = 0; r < K; ++r) {
-    u64 best = 0ull;
-    for (int64_t s = lane; s < nslot; s += 32) {
-      Vec16<DT> v;
-      v.r = __ldcg(rowv + s);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const u64 key = make_key(v.elem(e), (int32_t)(s * EPL + e));
-        if (key < prev && key > best) best = key;
-      }
-    }
-    if (lane < tail) {
-      const int32_t id = (int32_t)(nslot * EPL + lane);
-      const u64 key = make_key(load_scalar<DT>(rowp, id), id);
-      if (key < prev && key > best) best = key;
-    }
-    best = warp_max_u64(best);
-    if (lane == r) out = best;
-    prev = best;
-  }
-  return out;
-}
-
 constexpr int SW = 4;  // pass-2 warps per CTA
-
-// Value of the 8th largest of the 32 lanes' x: seven rounds remove the
-// current maximum (one lane each, the lowest on ties), the eighth reads it.
-// x must not be NaN.
-__device__ __forceinline__ float eighth_of_lanes(float x, int lane) {
-  int32_t k = ord_int(x);
-  int32_t m = 0;
-#pragma unroll
-  for (int r = 0; r < K; ++r) {
-    m = __reduce_max_sync(FULL, k);
-    if (r < K - 1) {
-      const unsigned owner = __ffs(__ballot_sync(FULL, k == m)) - 1;
-      if (lane == (int)owner) k = INT_MIN;
-    }
-  }
-  return from_ord_int(m);
-}
-
-// *p += 1 with acquire-release semantics at GPU scope; returns the old value.
-__device__ __forceinline__ int ticket_acq_rel(int32_t* p) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
-  return old;
-}
-
-// Number of valid slots (0 <= token < V) of request b, from the shared tree
-// tokens (one warp).
-__device__ __forceinline__ int request_valid(const VerifyArgs& a, const int32_t* stok, int b, int lane) {
-  const int base = b * a.S;
-  bool v0 = false, v1 = false;
-  if (lane < a.S) { const int32_t t = stok[base + lane]; v0 = t >= 0 && t < a.g.V; }
-  if (lane + 32 < a.S) { const int32_t t = stok[base + lane + 32]; v1 = t >= 0 && t < a.g.V; }
-  return __popc(__ballot_sync(FULL, v0)) + __popc(__ballot_sync(FULL, v1));
-}
 
 // Greedy acceptance of request b (one warp) from tree arrays staged in shared
 // memory (sp/spos/smask indexed by slot): match(i) = slot i is valid and is the

@@ -191,7 +191,7 @@ def test_lockstep_warmup_small(wid):
 @pytest.mark.slow
 @pytest.mark.parametrize("wid,steps", [(0, 100), (1, 6), (2, 3), (4, 2)])
 def test_lockstep_full_size(wid, steps):
-    """Full BASELINE sizes, the launch configuration the benchmark times."""
+    """The five workloads at full size, in the launch configuration the benchmark times."""
     w = W.WORKLOADS[wid]
     lockstep(w, steps, warm=(w.warm == "rollouts"), check_rows=4)
 
