@@ -143,8 +143,12 @@ int check_cfg(const graft_config* c, graft_handle* h) {
     for (int k = 0; k < 3; ++k)
       if (c->ckpt_draft[k] < 0 || c->ckpt_draft[k] > c->budget || c->ckpt_depth[k] < 0)
         return fail(h, GRAFT_EINVAL, "checkpoint %d: draft slots must be in [0, budget], depth >= 0", k);
-  if (c->tpl_depth < 1 || c->tpl_depth > 16 || c->tpl_width < 1 || c->tpl_width > graft::K)
-    return fail(h, GRAFT_EINVAL, "template depth must be in [1, 16] and width in [1, 8]");
+  if (c->tpl_depth < 1 || c->tpl_depth > 16 || c->tpl_width < 1 || c->tpl_width > 64)
+    return fail(h, GRAFT_EINVAL, "template depth must be in [1, 16] and width in [1, 64]");
+  if (c->ablation < 0 || c->ablation > 2 || (c->ablation != 0 && c->mode != GRAFT_MODE_CHECKPOINT))
+    return fail(h, GRAFT_EINVAL, "ablation must be 0, or 1 / 2 in checkpoint mode");
+  if (c->ablation == 2 && (c->fixed_draft < 0 || c->fixed_draft > c->budget))
+    return fail(h, GRAFT_EINVAL, "fixed_draft must be in [0, budget]");
   const int maxn = c->mode == GRAFT_MODE_TAIL ? c->budget : graft::MAX_DRAFT;
   if (c->max_draft_nodes < 0 || c->max_draft_nodes > maxn)
     return fail(h, GRAFT_EINVAL, "max_draft_nodes must be in [0, %d]", maxn);
@@ -197,6 +201,8 @@ void graft_default_config(graft_config* c, int32_t vocab, int32_t max_batch, int
   c->tail_thr = 0.4f;
   c->max_draft_nodes = mode == GRAFT_MODE_TAIL ? 16 : 184;
   c->scan_kernel = 0;
+  c->ablation = 0;
+  c->fixed_draft = 40;
 }
 
 int graft_init(const graft_config* cfg, graft_handle** out) {
@@ -320,6 +326,8 @@ int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
   }
   a.static_thr = c.static_thr;
   a.tail_thr = c.tail_thr;
+  a.ablation = c.ablation;
+  a.fixed_draft = c.fixed_draft;
   a.root_tok = d_root_tok; a.draft_tok = d_draft_tok; a.draft_parent = d_draft_parent; a.draft_aux = d_draft_aux;
   a.C = h->C;
   a.tpl.parent = h->tpl;

@@ -156,7 +156,11 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
 
     // ---- checkpoints: best path confidence of layers 0, 1, 5 ---------------
     int D = a.budget, cut = INT_MAX;
-    if (a.mode == GRAFT_MODE_CHECKPOINT) {
+    if (a.mode == GRAFT_MODE_CHECKPOINT && a.ablation == 2) {
+      // ablation without adaptive pruning (section 五): the same split every step
+      D = a.fixed_draft;
+      R = a.budget - D;
+    } else if (a.mode == GRAFT_MODE_CHECKPOINT) {
       if (t < nn) {
 #pragma unroll
         for (int k = 0; k < 3; ++k)
@@ -173,6 +177,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
           break;
         }
       }
+      if (a.ablation == 1) R = 0;  // ablation without retrieval (section 五): pruned slots stay empty
     }
 
     // ---- keep the top-D candidates by (confidence desc, index asc) --------

@@ -29,6 +29,7 @@ struct AssembleArgs {
   float ckpt_thr[3];
   int32_t ckpt_draft[3];
   float static_thr, tail_thr;
+  int32_t ablation, fixed_draft;
   const int32_t* root_tok;
   const int32_t* draft_tok;
   const int16_t* draft_parent;

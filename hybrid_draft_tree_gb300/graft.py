@@ -40,7 +40,7 @@ class graft_config(ctypes.Structure):
                 ("ckpt_depth", ctypes.c_int32 * 3), ("ckpt_thr", ctypes.c_float * 3),
                 ("ckpt_draft", ctypes.c_int32 * 3), ("tpl_depth", ctypes.c_int32), ("tpl_width", ctypes.c_int32),
                 ("static_thr", ctypes.c_float), ("tail_thr", ctypes.c_float), ("max_draft_nodes", ctypes.c_int32),
-                ("scan_kernel", ctypes.c_int32)]
+                ("scan_kernel", ctypes.c_int32), ("ablation", ctypes.c_int32), ("fixed_draft", ctypes.c_int32)]
 
 
 _lib = None

@@ -78,7 +78,7 @@ typedef struct {
   float ckpt_thr[3];      /* fire when the layer's best path confidence < thr (0.30, 0.20, 0.10) */
   int32_t ckpt_draft[3];  /* draft slots kept when that checkpoint fires (8, 24, 40); retrieval gets the rest */
   int32_t tpl_depth;      /* retrieval template depth (8) */
-  int32_t tpl_width;      /* template root width; rank-r node fan-out max(1, width >> r) (8) */
+  int32_t tpl_width;      /* template root width; rank-r node fan-out max(1, width >> r), at most 8 (8) */
   float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15) */
   float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4) */
   int32_t max_draft_nodes;/* largest draft tree (<= 256) or block (<= budget) per request */
@@ -86,6 +86,12 @@ typedef struct {
                              single-pass), 1 = single-pass with a shared running top-8,
                              2 = TMA-pipelined (aligned rows of >= 32 KB only), 3 = two-pass
                              (unit maxima, then per-row selection; aligned rows only) */
+  int32_t ablation;       /* checkpoint mode only (article §五 ablations; 0 elsewhere):
+                             0 = Graft, 1 = confidence pruning without retrieval (the freed
+                             slots stay empty), 2 = fixed split (no checkpoints: the top
+                             fixed_draft nodes of the whole tree plus budget - fixed_draft
+                             retrieval slots, every step) */
+  int32_t fixed_draft;    /* draft slots of the fixed split, in [0, budget] (40) */
 } graft_config;
 
 /* Fill *cfg with the paper's defaults for `mode` and vocabulary V. */

@@ -41,7 +41,7 @@ class Params(ctypes.Structure):
                 ("ckpt_depth", ctypes.c_int32 * 3), ("ckpt_thr", ctypes.c_float * 3),
                 ("ckpt_draft", ctypes.c_int32 * 3), ("tpl_depth", ctypes.c_int32),
                 ("tpl_width", ctypes.c_int32), ("static_thr", ctypes.c_float),
-                ("tail_thr", ctypes.c_float)]
+                ("tail_thr", ctypes.c_float), ("ablation", ctypes.c_int32), ("fixed_draft", ctypes.c_int32)]
 
 
 _lib = None
@@ -69,7 +69,8 @@ def _check(rc: int, what: str):
 
 
 def make_params(V, budget=60, mode=MODE_CHECKPOINT, ckpt_depth=(0, 1, 5), ckpt_thr=(0.30, 0.20, 0.10),
-                ckpt_draft=(8, 24, 40), tpl_depth=8, tpl_width=8, static_thr=0.15, tail_thr=0.4):
+                ckpt_draft=(8, 24, 40), tpl_depth=8, tpl_width=8, static_thr=0.15, tail_thr=0.4, ablation=0,
+                fixed_draft=40):
     p = Params()
     p.V, p.K, p.budget, p.S, p.mode = V, K, budget, budget + 1, mode
     for i in range(3):
@@ -78,6 +79,7 @@ def make_params(V, budget=60, mode=MODE_CHECKPOINT, ckpt_depth=(0, 1, 5), ckpt_t
         p.ckpt_draft[i] = ckpt_draft[i]
     p.tpl_depth, p.tpl_width = tpl_depth, tpl_width
     p.static_thr, p.tail_thr = static_thr, tail_thr
+    p.ablation, p.fixed_draft = ablation, fixed_draft
     return p
 
 

@@ -62,6 +62,8 @@ typedef struct {
   int32_t ckpt_draft[3];
   int32_t tpl_depth, tpl_width;
   float static_thr, tail_thr;
+  int32_t ablation;     /* checkpoint mode [P2 §五]: 0 Graft, 1 pruning without retrieval, 2 fixed split */
+  int32_t fixed_draft;  /* draft slots of the fixed split (ablation 2) */
 } or_params;
 
 enum { OR_OK = 0, OR_EINVAL = -1, OR_EDATA = -4 };
@@ -203,6 +205,8 @@ int or_assemble_checkpoint(const or_params* P, int32_t root_tok, int32_t n, cons
                            const int16_t* dpar, const float* dprob, const int32_t* C,
                            int32_t* tok, int32_t* par, int32_t* pos, uint64_t* mask, int32_t* info) {
   if (n < 0 || n > OR_MAXN || P->S > OR_MAXS || P->S != P->budget + 1) return OR_EINVAL;
+  if (P->ablation < 0 || P->ablation > 2 || (P->ablation == 2 && (P->fixed_draft < 0 || P->fixed_draft > P->budget)))
+    return OR_EINVAL;
   if (!check_tok(root_tok, P->V)) return OR_EDATA;
   for (int32_t i = 0; i < n; ++i) if (!check_tok(dtok[i], P->V)) return OR_EDATA;
   float conf[OR_MAXN]; int32_t depth[OR_MAXN];
@@ -212,11 +216,20 @@ int or_assemble_checkpoint(const or_params* P, int32_t root_tok, int32_t n, cons
   /* Gear 1: checkpoints in order; the first whose best path confidence is
    * below its threshold fires and fixes the (draft, retrieval) split. */
   int32_t fired = -1, D = P->budget, R = 0, cut = 1 << 30;
-  for (int k = 0; k < 3; ++k) {
-    int32_t d = P->ckpt_depth[k];
-    int any = 0; float best = 0.f;
-    for (int32_t i = 0; i < n; ++i) if (depth[i] == d) { if (!any || conf[i] > best) best = conf[i]; any = 1; }
-    if (any && best < P->ckpt_thr[k]) { fired = d; D = P->ckpt_draft[k]; R = P->budget - D; cut = d; break; }
+  if (P->ablation == 2) {
+    /* [P2 §五] ablation without adaptive pruning: the same (draft, retrieval)
+     * split every step, whatever the confidences; the top-D nodes of the
+     * whole tree are kept. */
+    D = P->fixed_draft; R = P->budget - D;
+  } else {
+    for (int k = 0; k < 3; ++k) {
+      int32_t d = P->ckpt_depth[k];
+      int any = 0; float best = 0.f;
+      for (int32_t i = 0; i < n; ++i) if (depth[i] == d) { if (!any || conf[i] > best) best = conf[i]; any = 1; }
+      if (any && best < P->ckpt_thr[k]) { fired = d; D = P->ckpt_draft[k]; R = P->budget - D; cut = d; break; }
+    }
+    /* [P2 §五] ablation without retrieval: the pruned slots stay empty. */
+    if (P->ablation == 1) R = 0;
   }
 
   /* Keep the top-D draft nodes of layers <= cut by confidence. */
@@ -275,6 +288,8 @@ int or_assemble_static(const or_params* P, int32_t root_tok, int32_t n, const in
                        const int16_t* dpar, const float* dprob, const int32_t* C,
                        int32_t* tok, int32_t* par, int32_t* pos, uint64_t* mask, int32_t* info) {
   if (n < 0 || n > OR_MAXN || P->S > OR_MAXS || P->S != P->budget + 1) return OR_EINVAL;
+  if (P->ablation < 0 || P->ablation > 2 || (P->ablation == 2 && (P->fixed_draft < 0 || P->fixed_draft > P->budget)))
+    return OR_EINVAL;
   if (!check_tok(root_tok, P->V)) return OR_EDATA;
   for (int32_t i = 0; i < n; ++i) if (!check_tok(dtok[i], P->V)) return OR_EDATA;
   float conf[OR_MAXN]; int32_t depth[OR_MAXN];

@@ -36,15 +36,36 @@ def test_library_loads_and_exports_every_declared_symbol():
 def test_config_struct_layout_and_defaults():
     import hybrid_draft_tree_gb300 as g
     cfg = g.graft_default_config(151936, 16, g.GRAFT_MODE_STATIC, g.GRAFT_BF16)
-    assert ctypes.sizeof(cfg) == 4 * 21
+    assert ctypes.sizeof(cfg) == 4 * 23
     assert (cfg.vocab, cfg.topk, cfg.budget, cfg.max_batch) == (151936, 8, 60, 16)
     assert list(cfg.ckpt_depth) == [0, 1, 5]
     assert [round(x, 6) for x in cfg.ckpt_thr] == [0.3, 0.2, 0.1]
     assert list(cfg.ckpt_draft) == [8, 24, 40]
     assert (cfg.tpl_depth, cfg.tpl_width) == (8, 8)
     assert abs(cfg.static_thr - 0.15) < 1e-7 and abs(cfg.tail_thr - 0.4) < 1e-7
+    assert (cfg.scan_kernel, cfg.ablation, cfg.fixed_draft) == (0, 0, 40)
     tail = g.graft_default_config(151936, 64, g.GRAFT_MODE_TAIL, g.GRAFT_BF16)
     assert tail.budget == 16 and tail.max_draft_nodes == 16
+
+
+def test_config_struct_matches_the_c_header(tmp_path):
+    """The binding's graft_config has the header's size and field offsets."""
+    import shutil
+    import subprocess
+    import hybrid_draft_tree_gb300 as g
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    names = [f[0] for f in g.graft.graft_config._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stddef.h>\n#include <stdio.h>\n#include \"graft.h\"\nint main(void) {\n"
+                   "  printf(\"%zu\\n\", sizeof(graft_config));\n" +
+                   "".join(f"  printf(\"%zu\\n\", offsetof(graft_config, {n}));\n" for n in names) + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", os.path.join(root, "include"), str(src), "-o", str(exe)])
+    out = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert out[0] == ctypes.sizeof(g.graft.graft_config)
+    assert out[1:] == [getattr(g.graft.graft_config, n).offset for n in names]
 
 
 def test_init_without_gpu_fails_cleanly():

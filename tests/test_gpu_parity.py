@@ -61,7 +61,8 @@ def lockstep(w, steps, warm=False, check_rows=0, stats=None, **cfg):
     from workloads.device_loop import DeviceLoop
     g = engine_for(w, **cfg)
     loop = DeviceLoop(w, g)
-    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
+    shared = {k: v for k, v in cfg.items() if k in ("tpl_depth", "tpl_width", "ablation", "fixed_draft")}
+    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode, **shared)
     C = oracle.new_matrix(w.V)
     if warm:
         toks_d, logits_d, (toks, rk, pl, bi) = loop.warm_inputs_device()
@@ -177,6 +178,19 @@ def test_verify_scan_kernels(scan_kernel, dtype, V, pad, fn):
     stride), heavy ties, all-equal rows (candidate overflow)."""
     fns = {"normal": _normal, "ties": _ties, "constant": _constant}
     _verify_case(V, dtype, 61, 3, fns[fn], stride_pad=pad, seed=V + pad, scan_kernel=scan_kernel)
+
+
+@pytest.mark.parametrize("cfg", [dict(ablation=1), dict(ablation=2, fixed_draft=40), dict(ablation=2, fixed_draft=0),
+                                 dict(ablation=2, fixed_draft=60), dict(tpl_depth=2), dict(tpl_depth=12),
+                                 dict(tpl_width=4), dict(tpl_width=16), dict(tpl_depth=10, tpl_width=16)])
+def test_lockstep_ablations_and_templates(cfg):
+    """The section 五 ablations (no retrieval, fixed split) and other
+    template depths and widths, closed loop against the oracle."""
+    w = W.WORKLOADS[0].scaled(V=3000, B=3, draft_sigma=0.75)
+    stats = []
+    lockstep(w, 12, stats=stats, **cfg)
+    if cfg.get("fixed_draft", 1) > 0:    # with no draft slots and a cold matrix nothing is accepted
+        assert any(a > 0 for _, a in stats)
 
 
 @pytest.mark.parametrize("wid", [1, 3])
@@ -469,9 +483,11 @@ def test_invalid_arguments_are_rejected():
     eng = g_.Graft(g_.graft_default_config(100, 2, 0, W.BF16))
     with pytest.raises(g_.GraftError):
         eng.verify_update(3, None, None, None, None, torch.empty((1, 100), device="cuda"), None, None)  # batch > max
-    bad = g_.graft_default_config(100, 2, 0, W.BF16, topk=4)
-    with pytest.raises(g_.GraftError):
-        g_.Graft(bad)
+    for mode, kw in ((0, dict(topk=4)), (1, dict(ablation=1)), (2, dict(ablation=2)), (0, dict(ablation=3)),
+                     (0, dict(ablation=2, fixed_draft=61)), (0, dict(tpl_width=65)), (0, dict(tpl_depth=17)),
+                     (0, dict(scan_kernel=5))):
+        with pytest.raises(g_.GraftError):
+            g_.Graft(g_.graft_default_config(100, 2, mode, W.BF16, **kw))
 
 
 def test_profile_api_reports_each_kernel():

@@ -3,8 +3,9 @@ brute force on tiny inputs, closed forms, the pages' budget table, and the
 pages' invariants (losslessness, the superset / monotonicity argument).
 
 Sources: popular-science article on arXiv 2605.20104, sections 二 (three
-gears), 三 (monotonicity and superset argument), 四 (static trees), 六
-(warm-up), 七 (Graft-TAIL); Hugging Face paper page 2605.20104, abstract.
+gears), 三 (monotonicity and superset argument), 四 (static trees), 五
+(ablations), 六 (warm-up), 七 (Graft-TAIL); Hugging Face paper page
+2605.20104, abstract.
 """
 import itertools
 import math
@@ -199,6 +200,63 @@ def test_checkpoint_firing_and_budget_table():
         assert tr.info[1] == min(D, avail[d])
         assert tr.info[2] == R                                      # all retrieval realised
         assert tr.info[3] == 1 + tr.info[1] + tr.info[2] <= 61
+
+
+def test_template_width_above_eight_and_deep_chains():
+    # width 16: the anchor's ranks are capped at the matrix row's 8; rank-r
+    # nodes have min(8, max(1, 16 >> r)) children: 8+8+4+2+1+1+1+1 = 26
+    par, rank, dep = oracle.template(60, depth=2, width=16)
+    assert len(par) == 8 + 26
+    # depth 12: the 12 rank-0 chain entries (rank sum 0) come first
+    par, rank, dep = oracle.template(20, depth=12, width=8)
+    assert list(dep[:12]) == list(range(1, 13)) and not rank[:12].any()
+    assert list(par[:12]) == [-1] + list(range(11))
+
+
+# ----------------------------------------------------------------------------- ablations (section 五)
+def test_no_retrieval_ablation_is_the_pruned_tree():
+    """Pruning without retrieval: the same tree as Graft with nothing to
+    retrieve (the pruned slots stay empty), whatever the matrix holds."""
+    V = 1000
+    full = oracle.new_matrix(V)
+    full[:, :] = (np.arange(V)[:, None] * 7 + np.arange(8)[None, :]) % V
+    for probs in ([0.25, 1, 1, 1, 1, 1], [0.5, 0.3, 1, 1, 1, 1], [0.9, 0.5, 0.5, 0.5, 0.6, 0.6], [0.9] * 6):
+        tok, par, prob = _layered_tree(probs)
+        a = oracle.assemble(oracle.make_params(V, ablation=1), 5, tok, prob, full, par)
+        b = oracle.assemble(oracle.make_params(V), 5, tok, prob, oracle.new_matrix(V), par)
+        for x, y in ((a.tok, b.tok), (a.par, b.par), (a.pos, b.pos), (a.mask, b.mask), (a.info, b.info)):
+            assert np.array_equal(x, y)
+        assert a.info[2] == 0
+
+
+@pytest.mark.parametrize("D", [0, 8, 40, 60])
+def test_fixed_split_keeps_the_top_d_of_the_whole_tree(D):
+    """No adaptive pruning: the top-D nodes of the whole tree by path
+    confidence (ties: lower index), then budget - D retrieval slots, every
+    step; no checkpoint is reported."""
+    V = 500
+    h = W.Harness(W.WORKLOADS[0].scaled(V=V, draft_sigma=0.75))
+    root, prev, ctx = h.init_state()
+    C = oracle.new_matrix(V)
+    C[:, :] = (np.arange(V)[:, None] * 3 + np.arange(8)[None, :] * 5 + 1) % V
+    for step in range(6):
+        tok, par, prob = h.draft(step, root, prev)
+        tok, par, prob = tok[0], par[0], prob[0]
+        conf = np.zeros(len(tok), np.float32)
+        for i in range(len(tok)):                       # fp32 product, root first
+            conf[i] = prob[i] if par[i] < 0 else np.float32(conf[par[i]] * prob[i])
+        kept = np.sort(np.lexsort((np.arange(len(tok)), -conf.astype(np.float64)))[:D])
+        tr = oracle.assemble(oracle.make_params(V, ablation=2, fixed_draft=D), int(root[0]), tok, prob, C, par)
+        assert tr.info[0] == -1 and tr.info[1] == D
+        assert list(tr.tok[1:1 + D]) == list(tok[kept])
+        assert tr.info[2] == 60 - D                     # the full matrix realises every entry
+
+
+@pytest.mark.parametrize("ablation", [1, 2])
+def test_ablations_are_lossless(ablation):
+    w = W.WORKLOADS[0].scaled(V=600, B=1, draft_sigma=0.75)
+    emitted, accs, _ = _run_loop(w, 10, ablation=ablation)
+    assert emitted[0] == _greedy(w, 0, len(emitted[0]))
 
 
 def test_empty_matrix_gives_pruned_only_tree():
@@ -408,9 +466,9 @@ def test_pad_rows_are_not_read():
 
 
 # ----------------------------------------------------------------------------- closed loop invariants
-def _run_loop(w, steps, C=None, retrieval=True):
+def _run_loop(w, steps, C=None, retrieval=True, **params):
     h = W.Harness(w)
-    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
+    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode, **params)
     C = oracle.new_matrix(w.V) if C is None else C
     root, prev, ctx = h.init_state()
     emitted = [[] for _ in range(w.B)]
