@@ -303,20 +303,12 @@ int graft_warmup(graft_handle* h, const int32_t* d_tokens, const void* d_logits,
   return GRAFT_OK;
 }
 
-int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
-                   const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes, int32_t* d_tree_tok,
-                   int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info, void* stream) {
-  if (!h) return GRAFT_EINVAL;
-  h->last_launches = 0;
+}  // extern "C"
+
+namespace {
+
+graft::AssembleArgs assemble_args(const graft_handle* h, int32_t batch, int32_t draft_nodes) {
   const graft_config& c = h->cfg;
-  if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
-  if (draft_nodes < 0 || draft_nodes > c.max_draft_nodes)
-    return fail(h, GRAFT_EINVAL, "draft_nodes %d outside [0, %d]", draft_nodes, c.max_draft_nodes);
-  if (batch == 0) return GRAFT_OK;
-  if (!d_root_tok || !d_tree_tok || !d_tree_parent || !d_tree_pos || !d_tree_mask || !d_info)
-    return fail(h, GRAFT_EINVAL, "null pointer");
-  if (draft_nodes > 0 && (!d_draft_tok || !d_draft_aux || (c.mode != GRAFT_MODE_TAIL && !d_draft_parent)))
-    return fail(h, GRAFT_EINVAL, "null draft pointer");
   graft::AssembleArgs a{};
   a.mode = c.mode; a.V = c.vocab; a.budget = c.budget; a.S = h->S; a.n = draft_nodes; a.batch = batch;
   for (int k = 0; k < 3; ++k) {
@@ -328,15 +320,36 @@ int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
   a.tail_thr = c.tail_thr;
   a.ablation = c.ablation;
   a.fixed_draft = c.fixed_draft;
-  a.root_tok = d_root_tok; a.draft_tok = d_draft_tok; a.draft_parent = d_draft_parent; a.draft_aux = d_draft_aux;
   a.C = h->C;
   a.tpl.parent = h->tpl;
   a.tpl.rank = h->tpl + h->tpl_len;
   a.tpl.depth = h->tpl + 2 * h->tpl_len;
   a.tpl.len = h->tpl_len;
+  a.err = h->err;
+  return a;
+}
+
+int assemble_impl(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                  const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes,
+                  const int32_t* d_event, const int32_t* d_retrieved, int32_t* d_tree_tok, int8_t* d_tree_parent,
+                  int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info, void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  h->last_launches = 0;
+  const graft_config& c = h->cfg;
+  if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
+  if (draft_nodes < 0 || draft_nodes > c.max_draft_nodes)
+    return fail(h, GRAFT_EINVAL, "draft_nodes %d outside [0, %d]", draft_nodes, c.max_draft_nodes);
+  if (batch == 0) return GRAFT_OK;
+  if (!d_root_tok || !d_tree_tok || !d_tree_parent || !d_tree_pos || !d_tree_mask || !d_info)
+    return fail(h, GRAFT_EINVAL, "null pointer");
+  if (draft_nodes > 0 && (!d_draft_tok || !d_draft_aux || (c.mode != GRAFT_MODE_TAIL && !d_draft_parent)))
+    return fail(h, GRAFT_EINVAL, "null draft pointer");
+  graft::AssembleArgs a = assemble_args(h, batch, draft_nodes);
+  a.root_tok = d_root_tok; a.draft_tok = d_draft_tok; a.draft_parent = d_draft_parent; a.draft_aux = d_draft_aux;
+  a.event_in = d_event;
+  a.rtok_in = d_retrieved;
   a.tree_tok = d_tree_tok; a.tree_parent = d_tree_parent; a.tree_pos = d_tree_pos; a.tree_mask = d_tree_mask;
   a.info = d_info;
-  a.err = h->err;
   cudaError_t e;
   {
     ProfScope ps(h, (cudaStream_t)stream, "k_assemble");
@@ -345,6 +358,75 @@ int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_assemble launch");
   h->last_launches = 1;
   return GRAFT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                   const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes, int32_t* d_tree_tok,
+                   int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info, void* stream) {
+  return assemble_impl(h, batch, d_root_tok, d_draft_tok, d_draft_parent, d_draft_aux, draft_nodes, nullptr, nullptr,
+                       d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, stream);
+}
+
+int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, const float* d_draft_prob,
+                int32_t draft_nodes, int32_t layer, int32_t* d_event, void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  h->last_launches = 0;
+  const graft_config& c = h->cfg;
+  if (c.mode != GRAFT_MODE_CHECKPOINT) return fail(h, GRAFT_EINVAL, "graft_check needs checkpoint mode");
+  if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
+  if (draft_nodes < 0 || draft_nodes > c.max_draft_nodes)
+    return fail(h, GRAFT_EINVAL, "draft_nodes %d outside [0, %d]", draft_nodes, c.max_draft_nodes);
+  if (layer < 0) return fail(h, GRAFT_EINVAL, "layer must be >= 0");
+  if (batch == 0) return GRAFT_OK;
+  if (!d_event || (draft_nodes > 0 && (!d_draft_parent || !d_draft_prob))) return fail(h, GRAFT_EINVAL, "null pointer");
+  if (c.ablation == 2) return GRAFT_OK;  // the fixed split has no checkpoints
+  graft::AssembleArgs a = assemble_args(h, batch, draft_nodes);
+  a.draft_parent = d_draft_parent; a.draft_aux = d_draft_prob; a.layer = layer;
+  cudaError_t e;
+  {
+    ProfScope ps(h, (cudaStream_t)stream, "k_check");
+    e = graft::launch_check(a, d_event, (cudaStream_t)stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_check launch");
+  h->last_launches = 1;
+  return GRAFT_OK;
+}
+
+int graft_retrieve(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_event,
+                   int32_t* d_retrieved, void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  h->last_launches = 0;
+  const graft_config& c = h->cfg;
+  if (c.mode != GRAFT_MODE_CHECKPOINT) return fail(h, GRAFT_EINVAL, "graft_retrieve needs checkpoint mode");
+  if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
+  if (batch == 0) return GRAFT_OK;
+  if (!d_root_tok || !d_event || !d_retrieved) return fail(h, GRAFT_EINVAL, "null pointer");
+  graft::AssembleArgs a = assemble_args(h, batch, 0);
+  a.root_tok = d_root_tok;
+  cudaError_t e;
+  {
+    ProfScope ps(h, (cudaStream_t)stream, "k_retrieve");
+    e = graft::launch_retrieve(a, d_event, d_retrieved, (cudaStream_t)stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_retrieve launch");
+  h->last_launches = 1;
+  return GRAFT_OK;
+}
+
+int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                          const int16_t* d_draft_parent, const float* d_draft_prob, int32_t draft_nodes,
+                          const int32_t* d_event, const int32_t* d_retrieved, int32_t* d_tree_tok,
+                          int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info,
+                          void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  if (h->cfg.mode != GRAFT_MODE_CHECKPOINT) return fail(h, GRAFT_EINVAL, "graft_assemble_staged needs checkpoint mode");
+  if (batch > 0 && (!d_event || !d_retrieved)) return fail(h, GRAFT_EINVAL, "null pointer");
+  return assemble_impl(h, batch, d_root_tok, d_draft_tok, d_draft_parent, d_draft_prob, draft_nodes, d_event,
+                       d_retrieved, d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, stream);
 }
 
 int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,

@@ -37,6 +37,63 @@ __device__ __forceinline__ int block_excl_count(bool v, int* s_warp, int& total)
   return base + pre;
 }
 
+// Path confidences conf(n) = conf(parent) * p(n) (fp32, root first) and
+// layer depths of draft nodes 0..nn-1, for the whole CTA (every thread calls;
+// thread t owns node t).  s_depth[t] must be -1 for t < nn on entry.  Each node
+// walks up to WALK ancestors and multiplies their probabilities root first:
+// the same products, in the same order, as computing one layer after the
+// other.  Trees deeper than WALK take the layer-by-layer passes.  -0 (a -0.0
+// probability) is stored as +0: keys and maxima use the bits, and the two
+// compare equal as values.  Returns node t's depth (-1 for t >= nn).
+__device__ int block_path_conf(int nn, int t, float prob, const int32_t* s_par, const float* s_prob, float* s_conf,
+                               int32_t* s_depth) {
+  int my_depth = -1;
+  bool deep = false;
+  if (t < nn) {
+    float pr[WALK];  // pr[i]: probability of the ancestor i levels up (pr[0]: this node)
+    int p = t, d = 0;
+#pragma unroll
+    for (int i = 0; i < WALK; ++i) {
+      const bool in = p >= 0;
+      const int q = in ? p : 0;
+      pr[i] = in ? s_prob[q] : 1.f;
+      d += in;
+      p = in ? s_par[q] : -1;
+    }
+    deep = p >= 0;
+    if (!deep) {
+      float c = 0.f;
+#pragma unroll
+      for (int k = 0; k < WALK; ++k) {
+        const int i = WALK - 1 - k;
+        const float x = (i == d - 1) ? pr[i] : __fmul_rn(c, pr[i]);
+        c = (i < d) ? (x == 0.f ? 0.f : x) : c;
+      }
+      s_conf[t] = c;
+      my_depth = d - 1;
+    }
+  }
+  // (uniform: every thread takes the passes or none does)
+  const bool layered = __syncthreads_or(deep);
+  if (layered) my_depth = -1;
+  for (int pass = 0; layered && pass <= nn; ++pass) {
+    float nc = 0.f;
+    int nd = -1;
+    if (t < nn && my_depth < 0) {
+      const int p = s_par[t];
+      if (p < 0) { nc = prob; nd = 0; }
+      else {
+        const int dp = s_depth[p];
+        if (dp >= 0) { nc = __fmul_rn(s_conf[p], prob); nd = dp + 1; }
+      }
+    }
+    __syncthreads();
+    if (nd >= 0) { s_conf[t] = nc == 0.f ? 0.f : nc; s_depth[t] = nd; my_depth = nd; }
+    if (!__syncthreads_or(t < nn && my_depth < 0)) break;
+  }
+  return my_depth;
+}
+
 __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   const int b = blockIdx.x;
   const int t = threadIdx.x;
@@ -103,55 +160,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
 
   if (a.mode != GRAFT_MODE_TAIL) {
     // ---- path confidence, root to leaf (gear 1) ---------------------------
-    // Each node walks up to WALK ancestors and multiplies their probabilities
-    // root first: the same fp32 products, in the same order, as computing one
-    // layer after the other.  Trees deeper than WALK take the layer passes.
-    int my_depth = -1;
-    bool deep = false;
-    if (t < nn) {
-      float pr[WALK];  // pr[i]: probability of the ancestor i levels up (pr[0]: this node)
-      int p = t, d = 0;
-#pragma unroll
-      for (int i = 0; i < WALK; ++i) {
-        const bool in = p >= 0;
-        const int q = in ? p : 0;
-        pr[i] = in ? s_prob[q] : 1.f;
-        d += in;
-        p = in ? s_par[q] : -1;
-      }
-      deep = p >= 0;
-      if (!deep) {
-        float c = 0.f;
-#pragma unroll
-        for (int k = 0; k < WALK; ++k) {
-          const int i = WALK - 1 - k;
-          const float x = (i == d - 1) ? pr[i] : __fmul_rn(c, pr[i]);
-          c = (i < d) ? (x == 0.f ? 0.f : x) : c;  // -0 is stored as +0, as below
-        }
-        s_conf[t] = c;
-        my_depth = d - 1;
-      }
-    }
-    // (uniform: every thread takes the passes or none does)
-    const bool layered = __syncthreads_or(deep);
-    if (layered) my_depth = -1;
-    for (int pass = 0; layered && pass <= nn; ++pass) {
-      float nc = 0.f;
-      int nd = -1;
-      if (t < nn && my_depth < 0) {
-        const int p = s_par[t];
-        if (p < 0) { nc = prob; nd = 0; }
-        else {
-          const int dp = s_depth[p];
-          if (dp >= 0) { nc = __fmul_rn(s_conf[p], prob); nd = dp + 1; }
-        }
-      }
-      __syncthreads();
-      // -0 (a -0.0 probability) is stored as +0: keys and maxima below use the
-      // bits, and the two compare equal as values
-      if (nd >= 0) { s_conf[t] = nc == 0.f ? 0.f : nc; s_depth[t] = nd; my_depth = nd; }
-      if (!__syncthreads_or(t < nn && my_depth < 0)) break;
-    }
+    const int my_depth = block_path_conf(nn, t, prob, s_par, s_prob, s_conf, s_depth);
     if (t < nn) atomicMax(&s_maxdepth, my_depth);
 
     // ---- checkpoints: best path confidence of layers 0, 1, 5 ---------------
@@ -161,7 +170,15 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
       D = a.fixed_draft;
       R = a.budget - D;
     } else if (a.mode == GRAFT_MODE_CHECKPOINT) {
-      if (t < nn) {
+      if (a.event_in) {
+        // incremental drafting: graft_check already evaluated the checkpoints
+        // as the layers were drafted; its verdict stands for itself
+        // (a request with bad input degrades to its root, as in graft_assemble)
+        if (t < 3) s_best[t] = (!bad && a.event_in[b] == a.ckpt_depth[t]) ? 0 : -1;
+        if (t == 0 && !bad && a.event_in[b] >= 0 && a.event_in[b] != a.ckpt_depth[0] &&
+            a.event_in[b] != a.ckpt_depth[1] && a.event_in[b] != a.ckpt_depth[2])
+          raise_err(a.err, GRAFT_ERR_TREE);  // not a checkpoint depth: treated as no firing
+      } else if (t < nn) {
 #pragma unroll
         for (int k = 0; k < 3; ++k)
           if (my_depth == a.ckpt_depth[k]) atomicMax(&s_best[k], __float_as_int(s_conf[t]));  // conf >= 0
@@ -169,7 +186,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
       __syncthreads();
       for (int k = 0; k < 3; ++k) {
         const int bi = s_best[k];
-        if (bi >= 0 && __int_as_float(bi) < a.ckpt_thr[k]) {
+        if (a.event_in ? bi == 0 : (bi >= 0 && __int_as_float(bi) < a.ckpt_thr[k])) {
           event = a.ckpt_depth[k];
           D = min(max(a.ckpt_draft[k], 0), a.budget);
           R = a.budget - D;
@@ -299,6 +316,16 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
     const int jr = mine ? a.tpl.rank[j] : 0;
     int maxd = 0;
     for (int q = 0; q < R; ++q) maxd = max(maxd, a.tpl.depth[q]);
+    if (a.rtok_in) {
+      // incremental drafting: graft_retrieve gathered the entries already
+      if (mine) {
+        int32_t tk = a.rtok_in[(int64_t)b * a.budget + j];
+        if (tk < -1 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); tk = -1; }
+        s_rtok[j] = tk;
+      }
+      __syncthreads();
+      maxd = 0;
+    }
     for (int level = 1; level <= maxd; ++level) {
       if (mine && jd == level) {
         const int32_t ptok = (jq < 0) ? anchor_tok : s_rtok[jq];
@@ -353,7 +380,103 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   }
 }
 
+// ---- incremental drafting: checkpoint verdicts and early retrieval ---------------
+// graft_check: for each request whose event is still -1, evaluate (in order)
+// the checkpoints whose layer is complete (depth <= a.layer) on the draft so
+// far; the first whose best path confidence is below its threshold fires and
+// its depth becomes the request's event.  One CTA per request.
+__global__ __launch_bounds__(AT) void k_check(AssembleArgs a, int32_t* event) {
+  const int b = blockIdx.x, t = threadIdx.x, n = a.n;
+  __shared__ int32_t s_par[MAX_DRAFT];
+  __shared__ float s_prob[MAX_DRAFT];
+  __shared__ float s_conf[MAX_DRAFT];
+  __shared__ int32_t s_depth[MAX_DRAFT];
+  __shared__ int s_bad, s_best[3];
+  if (t == 0) s_bad = 0;
+  if (t < 3) s_best[t] = -1;
+  __syncthreads();
+  float prob = 0.f;
+  if (t < n) {
+    const int64_t k = (int64_t)b * n + t;
+    const int p = a.draft_parent[k];
+    prob = a.draft_aux[k];
+    s_par[t] = p;
+    s_prob[t] = prob;
+    s_depth[t] = -1;
+    if (p < -1 || p >= t) { raise_err(a.err, GRAFT_ERR_TREE); s_bad = 1; }
+    if (!(prob >= 0.f && prob <= 1.f)) { raise_err(a.err, GRAFT_ERR_NAN); s_bad = 1; }
+  }
+  __syncthreads();
+  const int nn = s_bad ? 0 : n;  // bad input: nothing fires (assemble degrades the request)
+  const int my_depth = block_path_conf(nn, t, prob, s_par, s_prob, s_conf, s_depth);
+  if (t < nn) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      if (my_depth == a.ckpt_depth[k] && a.ckpt_depth[k] <= a.layer) atomicMax(&s_best[k], __float_as_int(s_conf[t]));
+  }
+  __syncthreads();
+  if (t == 0 && event[b] < 0) {
+    for (int k = 0; k < 3; ++k) {
+      const int bi = s_best[k];
+      if (bi >= 0 && __int_as_float(bi) < a.ckpt_thr[k]) { event[b] = a.ckpt_depth[k]; break; }
+    }
+  }
+}
+
+// Retrieval slots of a request: budget - D(fired checkpoint), 0 when nothing
+// fired or without retrieval, budget - fixed_draft under the fixed split.
+__device__ __forceinline__ int retrieval_slots(const AssembleArgs& a, int ev) {
+  if (a.ablation == 2) return a.budget - a.fixed_draft;
+  if (a.ablation == 1 || ev < 0) return 0;
+  for (int k = 0; k < 3; ++k)
+    if (ev == a.ckpt_depth[k]) return a.budget - min(max(a.ckpt_draft[k], 0), a.budget);
+  return 0;
+}
+
+// graft_retrieve: the retrieval subtree of every request that fired, gathered
+// along the template from the matrix (gear 2), anchored at the root, in
+// template order: out[b][j] = token of entry j, or -1 when the entry is not
+// realised or beyond the request's retrieval slots.  One CTA per request.
+__global__ __launch_bounds__(MAX_S) void k_retrieve(AssembleArgs a, const int32_t* event, int32_t* out) {
+  const int b = blockIdx.x, j = threadIdx.x;
+  __shared__ int32_t s_rtok[MAX_S];
+  const uint64_t keep = l2_keep_policy();
+  const int32_t root = a.root_tok[b];
+  const bool root_ok = root >= 0 && root < a.V;
+  const int R = root_ok ? min(retrieval_slots(a, event[b]), a.tpl.len) : 0;
+  const bool mine = j < R;
+  const int jd = mine ? a.tpl.depth[j] : 0;
+  const int jq = mine ? a.tpl.parent[j] : -1;
+  const int jr = mine ? a.tpl.rank[j] : 0;
+  s_rtok[j] = -1;
+  int maxd = 0;
+  for (int q = 0; q < R; ++q) maxd = max(maxd, a.tpl.depth[q]);
+  __syncthreads();
+  for (int level = 1; level <= maxd; ++level) {
+    if (mine && jd == level) {
+      const int32_t ptok = (jq < 0) ? root : s_rtok[jq];
+      int32_t tk = -1;
+      if (ptok >= 0 && ptok < a.V) {
+        tk = ld_keep(a.C + (int64_t)ptok * K + jr, keep);
+        if (tk < -1 || tk >= a.V) { raise_err(a.err, GRAFT_ERR_TOKEN); tk = -1; }
+      }
+      s_rtok[j] = tk;
+    }
+    __syncthreads();
+  }
+  if (j < a.budget) out[(int64_t)b * a.budget + j] = mine ? s_rtok[j] : -1;
+}
+
 }  // namespace
+
+cudaError_t launch_check(const AssembleArgs& a, int32_t* event, cudaStream_t s) {
+  k_check<<<a.batch, AT, 0, s>>>(a, event);
+  return cudaGetLastError();
+}
+cudaError_t launch_retrieve(const AssembleArgs& a, const int32_t* event, int32_t* out, cudaStream_t s) {
+  k_retrieve<<<a.batch, MAX_S, 0, s>>>(a, event, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s) {
   k_assemble<<<a.batch, AT, 0, s>>>(a);

@@ -30,6 +30,9 @@ struct AssembleArgs {
   int32_t ckpt_draft[3];
   float static_thr, tail_thr;
   int32_t ablation, fixed_draft;
+  int32_t layer;              // graft_check: deepest complete draft layer
+  const int32_t* event_in;    // graft_assemble_staged: checkpoint verdicts, or nullptr
+  const int32_t* rtok_in;     // graft_assemble_staged: gathered retrieval entries [batch][budget], or nullptr
   const int32_t* root_tok;
   const int32_t* draft_tok;
   const int16_t* draft_parent;
@@ -136,6 +139,8 @@ __device__ __forceinline__ void st_keep(uint64_t* ptr, uint64_t v, uint64_t pol)
 
 // launchers (return cudaGetLastError())
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s);
+cudaError_t launch_check(const AssembleArgs& a, int32_t* event, cudaStream_t s);
+cudaError_t launch_retrieve(const AssembleArgs& a, const int32_t* event, int32_t* out, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
 int verify_ctas_per_sm();
 int verify_max_rows(int grid);

@@ -25,7 +25,7 @@ K = 8
 EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup", "graft_assemble",
            "graft_verify_update", "graft_get_matrix", "graft_set_matrix", "graft_matrix_device_ptr",
            "graft_sync", "graft_last_error", "graft_last_launch_count", "graft_verify_update_noalloc",
-           "graft_profile_enable", "graft_profile_read")
+           "graft_profile_enable", "graft_profile_read", "graft_check", "graft_retrieve", "graft_assemble_staged")
 
 
 class GraftError(RuntimeError):
@@ -68,6 +68,9 @@ def load(build_if_missing: bool = True):
     L.graft_warmup.argtypes = [vp, vp, vp, i64, i64, vp]
     L.graft_assemble.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
     L.graft_verify_update.argtypes = [vp, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp]
+    L.graft_check.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp]
+    L.graft_retrieve.argtypes = [vp, i32, vp, vp, vp, vp]
+    L.graft_assemble_staged.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     L.graft_get_matrix.argtypes = [vp, vp, vp]
     L.graft_set_matrix.argtypes = [vp, vp, vp]
     L.graft_matrix_device_ptr.argtypes = [vp]
@@ -159,6 +162,24 @@ class Graft:
         self._check(self.L.graft_assemble(self.h, batch, _ptr(root_tok), _ptr(draft_tok), _ptr(draft_parent),
                                           _ptr(draft_aux), n, _ptr(tree_tok), _ptr(tree_parent), _ptr(tree_pos),
                                           _ptr(tree_mask), _ptr(info), _stream(stream)))
+
+    # incremental drafting (checkpoint mode): see graft_check in include/graft.h
+    def check(self, batch, draft_parent, draft_prob, layer, event, stream=None):
+        n = draft_parent.shape[-1]
+        self._check(self.L.graft_check(self.h, batch, _ptr(draft_parent), _ptr(draft_prob), n, layer, _ptr(event),
+                                       _stream(stream)))
+
+    def retrieve(self, batch, root_tok, event, retrieved, stream=None):
+        self._check(self.L.graft_retrieve(self.h, batch, _ptr(root_tok), _ptr(event), _ptr(retrieved),
+                                          _stream(stream)))
+
+    def assemble_staged(self, batch, root_tok, draft_tok, draft_parent, draft_prob, event, retrieved, tree_tok,
+                        tree_parent, tree_pos, tree_mask, info, stream=None):
+        n = draft_tok.shape[-1]
+        self._check(self.L.graft_assemble_staged(self.h, batch, _ptr(root_tok), _ptr(draft_tok), _ptr(draft_parent),
+                                                 _ptr(draft_prob), n, _ptr(event), _ptr(retrieved), _ptr(tree_tok),
+                                                 _ptr(tree_parent), _ptr(tree_pos), _ptr(tree_mask), _ptr(info),
+                                                 _stream(stream)))
 
     def verify_update(self, batch, tree_tok, tree_parent, tree_pos, tree_mask, logits, accept_len, out_tokens,
                       stream=None):

@@ -138,6 +138,40 @@ int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
                    int32_t* d_tree_tok, int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask,
                    int32_t* d_info, void* stream);
 
+/* Incremental drafting (article §二 gears 1-2; checkpoint mode only).  The
+ * checkpoints exist to stop the drafter early, and the retrieval gather runs
+ * beside the drafter instead of after it.  A drafter that expands its tree
+ * layer by layer calls, per step:
+ *   1. d_event[b] = -1 for every request (caller-owned int32[batch]);
+ *   2. after completing layer L (nodes of layers <= L in BFS order, the same
+ *      arrays graft_assemble takes, draft_nodes of them per request):
+ *      graft_check(..., L, d_event) -- every checkpoint whose layer is <= L is
+ *      evaluated in order for requests whose event is still -1; the first
+ *      that fires writes its depth.  A request that fired stops growing: its
+ *      later layers are not drafted;
+ *   3. at any point after its last graft_check, possibly on another stream
+ *      while the drafter works on other requests: graft_retrieve(...) gathers
+ *      every fired request's retrieval entries from the matrix into
+ *      d_retrieved[b][budget] (template order, -1 = not realised);
+ *   4. graft_assemble_staged(...) with the final tree: the same outputs as
+ *      graft_assemble on that tree (checkpoints are not re-evaluated, entries
+ *      are not gathered again), at the cost of the flatten alone.
+ * The matrix must not change between steps 3 and 4 (graft_verify_update and
+ * graft_warmup write it).  Under the fixed-split ablation graft_check does
+ * nothing and graft_retrieve gathers budget - fixed_draft entries for every
+ * request.  All three are asynchronous on `stream`; argument errors return
+ * GRAFT_EINVAL at once (also in static and tail modes).  An event that is not
+ * a checkpoint depth counts as no firing and sets GRAFT_ERR_TREE. */
+int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, const float* d_draft_prob,
+                int32_t draft_nodes, int32_t layer, int32_t* d_event, void* stream);
+int graft_retrieve(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_event,
+                   int32_t* d_retrieved, void* stream);
+int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                          const int16_t* d_draft_parent, const float* d_draft_prob, int32_t draft_nodes,
+                          const int32_t* d_event, const int32_t* d_retrieved, int32_t* d_tree_tok,
+                          int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info,
+                          void* stream);
+
 /* Steps 4-5 (article §二 gear 3, §三): one streaming pass over the logits of
  * every valid slot (plus a re-read of the few 512-byte pieces of a row that
  * can hold its largest values) computes its top-8 (element 0 = the greedy

@@ -83,6 +83,25 @@ def make_params(V, budget=60, mode=MODE_CHECKPOINT, ckpt_depth=(0, 1, 5), ckpt_t
     return p
 
 
+def check_layer(P, par, prob, layer, event):
+    """Incremental checkpoint evaluation after layers 0..layer; returns the
+    (possibly updated) event of one request."""
+    par = np.ascontiguousarray(par, np.int16)
+    prob = np.ascontiguousarray(prob, np.float32)
+    ev = ctypes.c_int32(int(event))
+    _check(lib().or_check_layer(ctypes.byref(P), len(par), _p(par), _p(prob), layer, ctypes.byref(ev)),
+           "or_check_layer")
+    return ev.value
+
+
+def retrieve(P, root, event, C):
+    """Retrieval entries of one request in template order ([budget], -1 = none)."""
+    out = np.empty(P.budget, np.int32)
+    _check(lib().or_retrieve(ctypes.byref(P), int(root), int(event), _p(np.ascontiguousarray(C, np.int32)), _p(out)),
+           "or_retrieve")
+    return out
+
+
 def template(R, depth=8, width=8):
     """First R retrieval-template entries: (parent entry, rank, depth) arrays."""
     par = np.zeros(max(R, 1), np.int32)

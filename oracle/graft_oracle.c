@@ -273,6 +273,55 @@ int or_assemble_checkpoint(const or_params* P, int32_t root_tok, int32_t n, cons
 }
 
 /* ------------------------------------------------------------------------
+ * Incremental drafting, one request [P2 §二, gears 1 and 2]: the checkpoints
+ * are meant to stop the drafter, so they are evaluated as its layers complete,
+ * and the retrieval gather can run beside the drafter.
+ * or_check_layer: with layers 0..layer complete (the n nodes given), evaluate
+ * in order every checkpoint whose layer is <= `layer`, unless *event already
+ * holds a firing depth; the first that fires writes its depth to *event.
+ * ---------------------------------------------------------------------- */
+int or_check_layer(const or_params* P, int32_t n, const int16_t* dpar, const float* dprob, int32_t layer,
+                   int32_t* event) {
+  if (n < 0 || n > OR_MAXN || layer < 0) return OR_EINVAL;
+  if (P->ablation == 2 || *event >= 0) return OR_OK;   /* the fixed split has no checkpoints */
+  float conf[OR_MAXN]; int32_t depth[OR_MAXN];
+  int rc = or_path_conf(n, dpar, dprob, conf, depth);
+  if (rc) return rc;
+  for (int k = 0; k < 3; ++k) {
+    int32_t d = P->ckpt_depth[k];
+    if (d > layer) continue;
+    int any = 0; float best = 0.f;
+    for (int32_t i = 0; i < n; ++i) if (depth[i] == d) { if (!any || conf[i] > best) best = conf[i]; any = 1; }
+    if (any && best < P->ckpt_thr[k]) { *event = d; break; }
+  }
+  return OR_OK;
+}
+
+/* or_retrieve: the retrieval entries of one request in template order for
+ * the split its event fixes (gear 2: a pure gather C[parent token][rank]
+ * anchored at the root); out[j] = token, or -1 when entry j is not realised or
+ * j is past the request's retrieval slots.  out has budget entries. */
+int or_retrieve(const or_params* P, int32_t root_tok, int32_t event, const int32_t* C, int32_t* out) {
+  int32_t R = 0;
+  if (P->ablation == 2) R = P->budget - P->fixed_draft;
+  else if (P->ablation == 0 && event >= 0)
+    for (int k = 0; k < 3; ++k) if (P->ckpt_depth[k] == event) { R = P->budget - P->ckpt_draft[k]; break; }
+  for (int32_t j = 0; j < P->budget; ++j) out[j] = -1;
+  if (!check_tok(root_tok, P->V)) return OR_EDATA;
+  int32_t tp[OR_MAXTPL], tr[OR_MAXTPL], td[OR_MAXTPL];
+  int32_t nt = or_template(P->tpl_depth, P->tpl_width, R, tp, tr, td);
+  if (nt < 0) return OR_EINVAL;
+  for (int32_t j = 0; j < nt; ++j) {
+    int32_t ptok = tp[j] < 0 ? root_tok : out[tp[j]];
+    if (ptok < 0) continue;
+    int32_t t = C[(int64_t)ptok * OR_K + tr[j]];
+    if (t < -1 || t >= P->V) return OR_EDATA;
+    out[j] = t;
+  }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------
  * Static-tree mode, one request [P2 §四]: each request keeps a fixed number of
  * verify slots (the top-`budget` draft nodes by path confidence, plus the
  * root), and every kept node whose path confidence is below static_thr is

@@ -193,6 +193,58 @@ def test_lockstep_ablations_and_templates(cfg):
         assert any(a > 0 for _, a in stats)
 
 
+@pytest.mark.parametrize("cfg", [{}, dict(ablation=1), dict(ablation=2, fixed_draft=40), dict(tpl_depth=12)])
+def test_incremental_drafting_matches_assemble_and_oracle(cfg):
+    """Checkpoints evaluated layer by layer, the retrieval gathered on a
+    second stream, then the staged assembly: the same trees as graft_assemble
+    and as the oracle, closed loop (the matrix fills as the loop runs)."""
+    from workloads.device_loop import DeviceLoop
+    w = W.WORKLOADS[0].scaled(V=3000, B=4, draft_sigma=0.75)
+    g = engine_for(w, **cfg)
+    loop = DeviceLoop(w, g)
+    shared = {k: v for k, v in cfg.items() if k in ("tpl_depth", "tpl_width", "ablation", "fixed_draft")}
+    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode, **shared)
+    C = oracle.new_matrix(w.V)
+    side = torch.cuda.Stream()
+    fired = 0
+    for step in range(12):
+        tok, par, aux = loop.draft()
+        loop.assemble()
+        ref = [t.clone() for t in (loop.tok, loop.par, loop.pos, loop.mask, loop.info)]
+        loop.assemble_incremental(side)
+        for x, y in zip((loop.tok, loop.par, loop.pos, loop.mask, loop.info), ref):
+            assert torch.equal(x, y), step
+        ev_g = loop.event.cpu().numpy()
+        rt_g = loop.retrieved.cpu().numpy()
+        depth = np.zeros(w.draft_nodes, np.int32)
+        for i in range(w.draft_nodes):
+            depth[i] = 0 if par[0][i] < 0 else depth[par[0][i]] + 1
+        for b in range(w.B):
+            ev = -1
+            for L in range(int(depth.max()) + 1):
+                m = int((depth <= L).sum())
+                ev = oracle.check_layer(P, par[b][:m], aux[b][:m], L, ev)
+            assert ev_g[b] == ev, (step, b)
+            assert np.array_equal(rt_g[b], oracle.retrieve(P, loop.root_h[b], ev, C)), (step, b)
+            fired += ev >= 0
+        trees = [oracle.assemble(P, loop.root_h[b], tok[b], aux[b], C, par[b]) for b in range(w.B)]
+        assert_trees_equal(loop, trees, step)
+        loop.make_logits()
+        tt = np.stack([t.tok for t in trees])
+        pp = np.stack([t.par for t in trees]).astype(np.int8)
+        lg = loop.h.tree_logits(tt, pp, loop.ctx_h, loop.prev_h)
+        loop.verify_update()
+        for b in range(w.B):
+            acc, out, topk = oracle.verify(trees[b], lg[b], w.dtype)
+            oracle.update(C, trees[b], topk)
+        assert np.array_equal(g.get_matrix(), C), step
+        loop.advance()
+    assert g.sync() == 0
+    if cfg.get("ablation", 0) != 2:
+        assert fired > 0
+    g.close()
+
+
 @pytest.mark.parametrize("wid", [1, 3])
 def test_lockstep_warmup_small(wid):
     base = W.WORKLOADS[wid]
@@ -483,6 +535,13 @@ def test_invalid_arguments_are_rejected():
     eng = g_.Graft(g_.graft_default_config(100, 2, 0, W.BF16))
     with pytest.raises(g_.GraftError):
         eng.verify_update(3, None, None, None, None, torch.empty((1, 100), device="cuda"), None, None)  # batch > max
+    static = g_.Graft(g_.graft_default_config(100, 2, 1, W.BF16))
+    ev = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    with pytest.raises(g_.GraftError):            # incremental drafting is for checkpoint mode
+        static.check(2, torch.zeros((2, 4), dtype=torch.int16, device="cuda"),
+                     torch.ones((2, 4), device="cuda"), 0, ev)
+    with pytest.raises(g_.GraftError):
+        eng.check(2, torch.zeros((2, 4), dtype=torch.int16, device="cuda"), torch.ones((2, 4), device="cuda"), -1, ev)
     for mode, kw in ((0, dict(topk=4)), (1, dict(ablation=1)), (2, dict(ablation=2)), (0, dict(ablation=3)),
                      (0, dict(ablation=2, fixed_draft=61)), (0, dict(tpl_width=65)), (0, dict(tpl_depth=17)),
                      (0, dict(scan_kernel=5))):

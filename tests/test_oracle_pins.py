@@ -259,6 +259,64 @@ def test_ablations_are_lossless(ablation):
     assert emitted[0] == _greedy(w, 0, len(emitted[0]))
 
 
+# ----------------------------------------------------------------------------- incremental drafting
+def _np_conf(par, prob):
+    conf = np.zeros(len(par), np.float32)
+    depth = np.zeros(len(par), np.int32)
+    for i in range(len(par)):                       # fp32 product, root first
+        conf[i] = prob[i] if par[i] < 0 else np.float32(conf[par[i]] * prob[i])
+        depth[i] = 0 if par[i] < 0 else depth[par[i]] + 1
+    return conf, depth
+
+
+@pytest.mark.parametrize("sigma", [0.5, 0.75, 2.0])
+def test_incremental_checkpoints_match_brute_force(sigma):
+    """Checkpoints evaluated layer by layer as the drafter completes them:
+    the first checkpoint (in order 0, 1, 5) whose layer's best path
+    confidence is below its threshold fires, and its verdict never changes."""
+    V = 400
+    h = W.Harness(W.WORKLOADS[0].scaled(V=V, draft_sigma=sigma))
+    root, prev, ctx = h.init_state()
+    P = oracle.make_params(V)
+    for step in range(12):
+        tok, par, prob = h.draft(step, root, prev)
+        par, prob = par[0], prob[0]
+        conf, depth = _np_conf(par, prob)
+        expect = -1
+        for d, thr in zip((0, 1, 5), (0.30, 0.20, 0.10)):
+            layer = conf[depth == d]
+            if len(layer) and layer.max() < np.float32(thr):
+                expect = d
+                break
+        ev = -1
+        for L in range(6):
+            n = int((depth <= L).sum())
+            ev = oracle.check_layer(P, par[:n], prob[:n], L, ev)
+            if expect >= 0 and L >= expect:
+                assert ev == expect
+            elif L < (expect if expect >= 0 else 99):
+                assert ev == -1
+        assert ev == expect
+        assert oracle.assemble(P, int(root[0]), tok[0], prob, oracle.new_matrix(V), par).info[0] == expect
+
+
+def test_retrieve_is_the_template_gather_of_the_fired_split():
+    V = 64
+    C = ((np.arange(V)[:, None] * 3 + np.arange(8)[None, :] * 11) % V).astype(np.int32)
+    C[C[9, 0], 1] = -1                                # entry "01" is empty: its subtree is not realised
+    P = oracle.make_params(V)
+    for event, R in ((-1, 0), (0, 52), (1, 36), (5, 20)):
+        out = oracle.retrieve(P, 9, event, C)
+        tp, trk, td = oracle.template(R)
+        ent = []
+        for j in range(R):
+            ptok = 9 if tp[j] < 0 else ent[tp[j]]
+            ent.append(-1 if ptok < 0 else int(C[ptok, trk[j]]))
+        assert list(out[:R]) == ent and (out[R:] == -1).all()
+    assert (oracle.retrieve(oracle.make_params(V, ablation=1), 9, 0, C) == -1).all()
+    assert (oracle.retrieve(oracle.make_params(V, ablation=2, fixed_draft=50), 9, -1, C)[:10] != -1).any()
+
+
 def test_empty_matrix_gives_pruned_only_tree():
     V = 1000
     P = oracle.make_params(V)

@@ -65,6 +65,34 @@ class DeviceLoop:
         self.g.assemble(self.w.B, self.root, self.d_tok, par, self.d_aux, self.tok, self.par, self.pos, self.mask,
                         self.info, stream=self.stream)
 
+    def assemble_incremental(self, side_stream=None):
+        """The same step through the incremental-drafting calls: checkpoint
+        verdicts layer by layer on growing prefixes of this step's draft (as
+        a drafter would make them), the retrieval gather on `side_stream`, then
+        the staged assembly.  Leaves the verdicts in self.event and the
+        gathered entries in self.retrieved."""
+        torch = self.torch
+        B, n = self.w.B, self.w.draft_nodes
+        if not hasattr(self, "event"):
+            self.event = torch.empty((B,), dtype=torch.int32, device=self.device)
+            self.retrieved = torch.empty((B, self.w.budget), dtype=torch.int32, device=self.device)
+        par_h = self.host_draft[1][0]
+        depth = np.zeros(n, np.int32)
+        for i in range(n):
+            depth[i] = 0 if par_h[i] < 0 else depth[par_h[i]] + 1
+        with torch.cuda.stream(self.stream):
+            self.event.fill_(-1)
+            for L in range(int(depth.max()) + 1 if n else 0):
+                m = int((depth <= L).sum())          # BFS order: layers 0..L are a prefix
+                self.g.check(B, self.d_par[:, :m].contiguous(), self.d_aux[:, :m].contiguous(), L, self.event,
+                             stream=self.stream)
+        side = side_stream if side_stream is not None else self.stream
+        side.wait_stream(self.stream)
+        self.g.retrieve(B, self.root, self.event, self.retrieved, stream=side)
+        self.stream.wait_stream(side)
+        self.g.assemble_staged(B, self.root, self.d_tok, self.d_par, self.d_aux, self.event, self.retrieved, self.tok,
+                               self.par, self.pos, self.mask, self.info, stream=self.stream)
+
     def make_logits(self):
         s = self.stream.cuda_stream
         rk, pl, bi = self.ds.tree_rowparams(self.tok, self.par, self.ctx, self.prev, s)
