@@ -1,6 +1,8 @@
 // C ABI of libgraft: handle management, argument checking and launches.
 // The method (popular-science article on arXiv 2605.20104, section 二) is
 // described in include/graft.h; the kernels live in assemble.cu and scan.cu.
+#include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -389,7 +391,7 @@ int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, c
   cudaError_t e;
   {
     ProfScope ps(h, (cudaStream_t)stream, "k_check");
-    e = graft::launch_check(a, d_event, (cudaStream_t)stream);
+    e = graft::launch_check(a, d_event, nullptr, (cudaStream_t)stream);
   }
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_check launch");
   h->last_launches = 1;
@@ -427,6 +429,82 @@ int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_
   if (batch > 0 && (!d_event || !d_retrieved)) return fail(h, GRAFT_EINVAL, "null pointer");
   return assemble_impl(h, batch, d_root_tok, d_draft_tok, d_draft_parent, d_draft_prob, draft_nodes, d_event,
                        d_retrieved, d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, stream);
+}
+
+int graft_confidence(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, const float* d_draft_prob,
+                     int32_t draft_nodes, float* d_best, void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  h->last_launches = 0;
+  const graft_config& c = h->cfg;
+  if (c.mode == GRAFT_MODE_TAIL) return fail(h, GRAFT_EINVAL, "graft_confidence needs a draft tree");
+  if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
+  if (draft_nodes < 0 || draft_nodes > c.max_draft_nodes)
+    return fail(h, GRAFT_EINVAL, "draft_nodes %d outside [0, %d]", draft_nodes, c.max_draft_nodes);
+  if (batch == 0) return GRAFT_OK;
+  if (!d_best || (draft_nodes > 0 && (!d_draft_parent || !d_draft_prob))) return fail(h, GRAFT_EINVAL, "null pointer");
+  graft::AssembleArgs a = assemble_args(h, batch, draft_nodes);
+  a.draft_parent = d_draft_parent; a.draft_aux = d_draft_prob; a.layer = INT32_MAX;
+  cudaError_t e;
+  {
+    ProfScope ps(h, (cudaStream_t)stream, "k_check");
+    e = graft::launch_check(a, nullptr, d_best, (cudaStream_t)stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_confidence launch");
+  h->last_launches = 1;
+  return GRAFT_OK;
+}
+
+int graft_calibrate_thresholds(const float* best, int32_t n_rows, double quantile, float* thr_out) {
+  if (!best || !thr_out || n_rows < 0 || !(quantile > 0.0 && quantile <= 1.0)) return GRAFT_EINVAL;
+  for (int k = 0; k < 3; ++k) {
+    std::vector<float> v;
+    for (int32_t i = 0; i < n_rows; ++i) {
+      const float x = best[(int64_t)i * 3 + k];
+      if (x >= 0.f && x <= 1.f) v.push_back(x);  // -1 = the layer was empty
+    }
+    if (v.empty()) return GRAFT_EINVAL;
+    std::sort(v.begin(), v.end());
+    // nearest rank: the smallest sample value with at least `quantile` of the sample at or below it
+    // (1e-9 absorbs the rounding of q * n when it is an integer in exact arithmetic)
+    int64_t r = (int64_t)std::ceil(quantile * (double)v.size() - 1e-9);
+    if (r < 1) r = 1;
+    if (r > (int64_t)v.size()) r = (int64_t)v.size();
+    thr_out[k] = v[(size_t)(r - 1)];
+  }
+  return GRAFT_OK;
+}
+
+int graft_set_thresholds(graft_handle* h, const float* thr) {
+  if (!h || !thr) return GRAFT_EINVAL;
+  for (int k = 0; k < 3; ++k)
+    if (!(thr[k] >= 0.f && thr[k] <= 1.f)) return fail(h, GRAFT_EINVAL, "threshold %d must be in [0, 1]", k);
+  for (int k = 0; k < 3; ++k) h->cfg.ckpt_thr[k] = thr[k];
+  return GRAFT_OK;
+}
+
+int graft_coverage(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
+                   const int32_t* d_info, const void* d_logits, int64_t row_stride, float* d_gain, void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  h->last_launches = 0;
+  const graft_config& c = h->cfg;
+  if (c.mode == GRAFT_MODE_STATIC) return fail(h, GRAFT_EINVAL, "graft_coverage needs checkpoint or tail mode");
+  if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
+  if (batch == 0) return GRAFT_OK;
+  if (!d_tree_tok || !d_tree_parent || !d_info || !d_logits || !d_gain) return fail(h, GRAFT_EINVAL, "null pointer");
+  if (row_stride < c.vocab) return fail(h, GRAFT_EINVAL, "row_stride < vocab");
+  graft::VerifyArgs a{};
+  a.g.V = c.vocab;
+  a.g.stride = row_stride;
+  a.S = h->S; a.batch = batch; a.logits = d_logits;
+  a.tree_tok = d_tree_tok; a.tree_parent = d_tree_parent;
+  cudaError_t e;
+  {
+    ProfScope ps(h, (cudaStream_t)stream, "k_coverage");
+    e = graft::launch_coverage(a, d_info, d_gain, c.logits_dtype, (cudaStream_t)stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_coverage launch");
+  h->last_launches = 1;
+  return GRAFT_OK;
 }
 
 int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,

@@ -385,7 +385,9 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
 // the checkpoints whose layer is complete (depth <= a.layer) on the draft so
 // far; the first whose best path confidence is below its threshold fires and
 // its depth becomes the request's event.  One CTA per request.
-__global__ __launch_bounds__(AT) void k_check(AssembleArgs a, int32_t* event) {
+// With best_out set instead (graft_confidence), write the best path
+// confidence of each checkpoint layer, -1 for an empty layer.
+__global__ __launch_bounds__(AT) void k_check(AssembleArgs a, int32_t* event, float* best_out) {
   const int b = blockIdx.x, t = threadIdx.x, n = a.n;
   __shared__ int32_t s_par[MAX_DRAFT];
   __shared__ float s_prob[MAX_DRAFT];
@@ -415,6 +417,10 @@ __global__ __launch_bounds__(AT) void k_check(AssembleArgs a, int32_t* event) {
       if (my_depth == a.ckpt_depth[k] && a.ckpt_depth[k] <= a.layer) atomicMax(&s_best[k], __float_as_int(s_conf[t]));
   }
   __syncthreads();
+  if (best_out) {
+    if (t < 3) best_out[(int64_t)b * 3 + t] = s_best[t] >= 0 ? __int_as_float(s_best[t]) : -1.f;
+    return;
+  }
   if (t == 0 && event[b] < 0) {
     for (int k = 0; k < 3; ++k) {
       const int bi = s_best[k];
@@ -469,8 +475,8 @@ __global__ __launch_bounds__(MAX_S) void k_retrieve(AssembleArgs a, const int32_
 
 }  // namespace
 
-cudaError_t launch_check(const AssembleArgs& a, int32_t* event, cudaStream_t s) {
-  k_check<<<a.batch, AT, 0, s>>>(a, event);
+cudaError_t launch_check(const AssembleArgs& a, int32_t* event, float* best_out, cudaStream_t s) {
+  k_check<<<a.batch, AT, 0, s>>>(a, event, best_out);
   return cudaGetLastError();
 }
 cudaError_t launch_retrieve(const AssembleArgs& a, const int32_t* event, int32_t* out, cudaStream_t s) {

@@ -139,7 +139,8 @@ __device__ __forceinline__ void st_keep(uint64_t* ptr, uint64_t v, uint64_t pol)
 
 // launchers (return cudaGetLastError())
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s);
-cudaError_t launch_check(const AssembleArgs& a, int32_t* event, cudaStream_t s);
+cudaError_t launch_check(const AssembleArgs& a, int32_t* event, float* best_out, cudaStream_t s);
+cudaError_t launch_coverage(const VerifyArgs& a, const int32_t* info, float* gain, int dtype, cudaStream_t s);
 cudaError_t launch_retrieve(const AssembleArgs& a, const int32_t* event, int32_t* out, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
 int verify_ctas_per_sm();

@@ -25,7 +25,20 @@ K = 8
 EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup", "graft_assemble",
            "graft_verify_update", "graft_get_matrix", "graft_set_matrix", "graft_matrix_device_ptr",
            "graft_sync", "graft_last_error", "graft_last_launch_count", "graft_verify_update_noalloc",
-           "graft_profile_enable", "graft_profile_read", "graft_check", "graft_retrieve", "graft_assemble_staged")
+           "graft_profile_enable", "graft_profile_read", "graft_check", "graft_retrieve", "graft_assemble_staged",
+           "graft_confidence", "graft_calibrate_thresholds", "graft_set_thresholds", "graft_coverage")
+
+
+def calibrate_thresholds(best: np.ndarray, quantile: float) -> np.ndarray:
+    """Nearest-rank `quantile` of each checkpoint's best path confidences
+    (best: [n, 3], -1 = empty layer), computed by the library (host code)."""
+    best = np.ascontiguousarray(best, np.float32)
+    out = np.zeros(3, np.float32)
+    rc = load().graft_calibrate_thresholds(best.ctypes.data_as(vp), best.shape[0], ctypes.c_double(quantile),
+                                           out.ctypes.data_as(vp))
+    if rc != 0:
+        raise GraftError(rc, "graft_calibrate_thresholds")
+    return out
 
 
 class GraftError(RuntimeError):
@@ -71,6 +84,10 @@ def load(build_if_missing: bool = True):
     L.graft_check.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp]
     L.graft_retrieve.argtypes = [vp, i32, vp, vp, vp, vp]
     L.graft_assemble_staged.argtypes = [vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.graft_confidence.argtypes = [vp, i32, vp, vp, i32, vp, vp]
+    L.graft_calibrate_thresholds.argtypes = [vp, i32, ctypes.c_double, vp]
+    L.graft_set_thresholds.argtypes = [vp, vp]
+    L.graft_coverage.argtypes = [vp, i32, vp, vp, vp, vp, i64, vp, vp]
     L.graft_get_matrix.argtypes = [vp, vp, vp]
     L.graft_set_matrix.argtypes = [vp, vp, vp]
     L.graft_matrix_device_ptr.argtypes = [vp]
@@ -180,6 +197,20 @@ class Graft:
                                                  _ptr(draft_prob), n, _ptr(event), _ptr(retrieved), _ptr(tree_tok),
                                                  _ptr(tree_parent), _ptr(tree_pos), _ptr(tree_mask), _ptr(info),
                                                  _stream(stream)))
+
+    # threshold calibration and the coverage diagnostic
+    def confidence(self, batch, draft_parent, draft_prob, best, stream=None):
+        n = draft_parent.shape[-1]
+        self._check(self.L.graft_confidence(self.h, batch, _ptr(draft_parent), _ptr(draft_prob), n, _ptr(best),
+                                            _stream(stream)))
+
+    def set_thresholds(self, thr):
+        t = (ctypes.c_float * 3)(*[float(x) for x in thr])
+        self._check(self.L.graft_set_thresholds(self.h, t))
+
+    def coverage(self, batch, tree_tok, tree_parent, info, logits, gain, stream=None):
+        self._check(self.L.graft_coverage(self.h, batch, _ptr(tree_tok), _ptr(tree_parent), _ptr(info), _ptr(logits),
+                                          logits.stride(-2), _ptr(gain), _stream(stream)))
 
     def verify_update(self, batch, tree_tok, tree_parent, tree_pos, tree_mask, logits, accept_len, out_tokens,
                       stream=None):

@@ -172,6 +172,33 @@ int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_
                           int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info,
                           void* stream);
 
+/* Threshold calibration (article §二: the checkpoint thresholds are set from
+ * the distribution of path confidences seen during warm-up).
+ * graft_confidence: d_best[b][k] = best path confidence of request b's draft
+ *   nodes at checkpoint layer ckpt_depth[k] (-1 when that layer is empty);
+ *   checkpoint and static modes.  Asynchronous on `stream`.
+ * graft_calibrate_thresholds (host only, no handle): thr_out[k] = the
+ *   nearest-rank `quantile` (in (0, 1]) of the non-negative best[i][k],
+ *   i < n_rows: the smallest sample value with at least that fraction of the
+ *   sample at or below it.  GRAFT_EINVAL if a checkpoint has no sample.
+ * graft_set_thresholds: replace the handle's ckpt_thr (each in [0, 1]); later
+ *   calls use them. */
+int graft_confidence(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, const float* d_draft_prob,
+                     int32_t draft_nodes, float* d_best, void* stream);
+int graft_calibrate_thresholds(const float* best, int32_t n_rows, double quantile, float* thr_out);
+int graft_set_thresholds(graft_handle* h, const float* thr);
+
+/* Coverage gain of the retrieval graft (article §三), a diagnostic; checkpoint
+ * and tail modes.  For request b, with the tree and info record graft_assemble
+ * wrote and the target's logits of that tree (as graft_verify_update takes
+ * them): every retrieved slot whose parent is a kept slot (the root, or the
+ * last kept block token) carries a boundary candidate, new unless a kept draft
+ * child of the same parent has the same token; d_gain[b] = the sum over the
+ * new candidates of softmax(parent's row)[token], in fp32.  Reads one logits
+ * row per boundary parent.  Asynchronous on `stream`. */
+int graft_coverage(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
+                   const int32_t* d_info, const void* d_logits, int64_t row_stride, float* d_gain, void* stream);
+
 /* Steps 4-5 (article §二 gear 3, §三): one streaming pass over the logits of
  * every valid slot (plus a re-read of the few 512-byte pieces of a row that
  * can hold its largest values) computes its top-8 (element 0 = the greedy

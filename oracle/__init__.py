@@ -102,6 +102,36 @@ def retrieve(P, root, event, C):
     return out
 
 
+def coverage(tree, info, rows, dtype):
+    """Coverage gain of the retrieval graft (article section 三), fp64: the
+    target probability mass that the new candidates at the prune boundary add.
+    Retrieved slots follow the kept draft slots (checkpoint and tail modes);
+    a retrieved slot whose parent is a kept slot is a boundary candidate, new
+    unless a kept draft child of that parent has the same token; the gain is
+    the sum of softmax(parent's row)[token] over the new candidates.
+    rows: [S, V] logits of the tree (float32, or bf16 bit patterns)."""
+    n_draft, n_retr = int(info[1]), int(info[2])
+    r0, r1 = 1 + n_draft, 1 + n_draft + n_retr
+    vals = np.asarray(rows)
+    if dtype == BF16:
+        vals = (vals.astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+    vals = vals.astype(np.float64)
+    gain = 0.0
+    for p in range(r0):
+        kids = [j for j in range(r0, r1) if tree.par[j] == p]
+        if not kids:
+            continue
+        x = vals[p]
+        m = x.max()
+        z = np.exp(x - m).sum()
+        drafted = {int(tree.tok[q]) for q in range(1, r0) if tree.par[q] == p}
+        for j in kids:
+            t = int(tree.tok[j])
+            if t not in drafted:
+                gain += np.exp(x[t] - m) / z
+    return gain
+
+
 def template(R, depth=8, width=8):
     """First R retrieval-template entries: (parent entry, rank, depth) arrays."""
     par = np.zeros(max(R, 1), np.int32)

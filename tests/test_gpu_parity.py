@@ -245,6 +245,90 @@ def test_incremental_drafting_matches_assemble_and_oracle(cfg):
     g.close()
 
 
+def _np_layer_best(par, prob):
+    conf = np.zeros(len(par), np.float32)
+    depth = np.zeros(len(par), np.int32)
+    for i in range(len(par)):                       # fp32 product, root first
+        conf[i] = prob[i] if par[i] < 0 else np.float32(conf[par[i]] * prob[i])
+        depth[i] = 0 if par[i] < 0 else depth[par[i]] + 1
+    return np.array([conf[depth == d].max() if (depth == d).any() else -1.0 for d in (0, 1, 5)], np.float32)
+
+
+def test_confidence_and_calibrated_thresholds():
+    """graft_confidence returns each checkpoint layer's best fp32 path
+    confidence; thresholds calibrated from those over warm-up steps then
+    drive the checkpoints exactly as in the oracle with the same thresholds."""
+    from workloads.device_loop import DeviceLoop
+    w = W.WORKLOADS[0].scaled(V=3000, B=4, draft_sigma=0.75)
+    g_ = G()
+    eng = engine_for(w)
+    loop = DeviceLoop(w, eng)
+    best = torch.empty((w.B, 3), dtype=torch.float32, device="cuda")
+    samples = []
+    for step in range(6):
+        tok, par, aux = loop.draft()
+        eng.confidence(w.B, loop.d_par, loop.d_aux, best)
+        got = best.cpu().numpy()
+        for b in range(w.B):
+            assert np.array_equal(got[b], _np_layer_best(par[b], aux[b])), (step, b)
+        samples.append(got)
+        loop.assemble(); loop.make_logits(); loop.verify_update(); loop.advance()
+    thr = g_.calibrate_thresholds(np.concatenate(samples), 0.4)
+    eng.set_thresholds(thr)
+    P = oracle.make_params(w.V, ckpt_thr=tuple(float(x) for x in thr))
+    C = eng.get_matrix()
+    fired = 0
+    for step in range(8):
+        tok, par, aux = loop.draft()
+        loop.assemble()
+        trees = [oracle.assemble(P, loop.root_h[b], tok[b], aux[b], C, par[b]) for b in range(w.B)]
+        assert_trees_equal(loop, trees, step)
+        fired += sum(int(t.info[0] >= 0) for t in trees)
+        loop.make_logits()
+        tt = np.stack([t.tok for t in trees])
+        pp = np.stack([t.par for t in trees]).astype(np.int8)
+        lg = loop.h.tree_logits(tt, pp, loop.ctx_h, loop.prev_h)
+        loop.verify_update()
+        for b in range(w.B):
+            acc, out, topk = oracle.verify(trees[b], lg[b], w.dtype)
+            oracle.update(C, trees[b], topk)
+        loop.advance()
+    assert fired > 0
+    with pytest.raises(g_.GraftError):
+        eng.set_thresholds([0.5, 1.5, 0.1])
+    eng.close()
+
+
+@pytest.mark.parametrize("wid,B", [(0, 3), (4, 8)])
+def test_coverage_gain_matches_oracle(wid, B):
+    """The coverage diagnostic against the oracle's fp64 value (fp32 softmax
+    over one row: relative 1e-4, absolute 1e-7)."""
+    from workloads.device_loop import DeviceLoop
+    w = W.WORKLOADS[wid].scaled(V=5000, B=B, draft_sigma=0.75)
+    eng = engine_for(w)
+    loop = DeviceLoop(w, eng)
+    gain = torch.empty((B,), dtype=torch.float32, device="cuda")
+    seen = 0
+    for step in range(10):
+        loop.draft()
+        loop.assemble()
+        loop.make_logits()
+        eng.coverage(B, loop.tok, loop.par, loop.info, loop.logits, gain)
+        got = gain.cpu().numpy()
+        toks, pars, info = loop.tok.cpu().numpy(), loop.par.cpu().numpy(), loop.info.cpu().numpy()
+        rows = loop.logits.view(torch.int16 if w.dtype else torch.int32).cpu().numpy().reshape(B, w.S, -1)
+        for b in range(B):
+            t = oracle.Tree(w.S)
+            t.tok[:], t.par[:] = toks[b], pars[b].astype(np.int32)
+            exp = oracle.coverage(t, info[b], rows[b].view(np.uint16) if w.dtype else rows[b].view(np.float32), w.dtype)
+            assert abs(got[b] - exp) <= 1e-4 * exp + 1e-7, (step, b, got[b], exp)
+            seen += exp > 0
+        loop.verify_update()
+        loop.advance()
+    assert seen > 0
+    eng.close()
+
+
 @pytest.mark.parametrize("wid", [1, 3])
 def test_lockstep_warmup_small(wid):
     base = W.WORKLOADS[wid]

@@ -317,6 +317,38 @@ def test_retrieve_is_the_template_gather_of_the_fired_split():
     assert (oracle.retrieve(oracle.make_params(V, ablation=2, fixed_draft=50), 9, -1, C)[:10] != -1).any()
 
 
+# ----------------------------------------------------------------------------- coverage gain (section 三)
+def _coverage_case():
+    """Root 0 with kept draft children 10, 11 (slots 1, 2) and retrieved
+    children 11, 12, 13 (slots 3-5, 11 duplicating a draft token) plus a
+    retrieved grandchild 14 (slot 6, not at the boundary)."""
+    t = oracle.Tree(8)
+    t.tok[:7] = [0, 10, 11, 11, 12, 13, 14]
+    t.par[:7] = [-1, 0, 0, 0, 0, 0, 3]
+    t.info[:] = [0, 2, 4, 7]
+    return t
+
+
+def test_coverage_of_a_uniform_row_counts_new_candidates():
+    t = _coverage_case()
+    V = 40
+    rows = np.zeros((8, V), np.float32)
+    assert abs(oracle.coverage(t, t.info, rows, oracle.F32) - 2 / V) < 1e-15   # 12 and 13 are new; 11 is not
+
+
+def test_coverage_is_the_mass_of_the_new_tokens():
+    t = _coverage_case()
+    V = 40
+    rows = np.full((8, V), -np.inf, np.float32)
+    rows[0, 12] = 3.0
+    assert oracle.coverage(t, t.info, rows, oracle.F32) == 1.0          # all the mass on a new candidate
+    rows[0, 12], rows[0, 11] = -np.inf, 3.0
+    assert oracle.coverage(t, t.info, rows, oracle.F32) == 0.0          # all of it on a drafted token
+    rows[0, :] = np.log(np.arange(1, V + 1, dtype=np.float32))           # p(v) = (v + 1) / sum
+    expect = (13 + 14) / (V * (V + 1) / 2)
+    assert abs(oracle.coverage(t, t.info, rows, oracle.F32) - expect) < 1e-6 * expect   # fp32 logs of 1..V
+
+
 def test_empty_matrix_gives_pruned_only_tree():
     V = 1000
     P = oracle.make_params(V)
