@@ -507,9 +507,26 @@ int graft_coverage(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, co
   return GRAFT_OK;
 }
 
-int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
-                        const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
-                        int64_t row_stride, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int launch_sample_step(graft_handle* h, const graft::VerifyArgs& a, void* stream) {
+  cudaError_t e;
+  {
+    ProfScope ps(h, (cudaStream_t)stream, "k_sample");
+    e = graft::launch_sample(a, h->cfg.logits_dtype, (cudaStream_t)stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update_sample launch");
+  h->last_launches += 1;
+  return GRAFT_OK;
+}
+
+// Greedy (sample = false) or stochastic verification, and the update.
+int verify_impl(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
+                const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits, int64_t row_stride,
+                int32_t* d_accept_len, int32_t* d_out_tokens, bool sample, float temperature,
+                const float* d_u_accept, const float* d_u_resid, void* stream) {
   if (!h) return GRAFT_EINVAL;
   h->last_launches = 0;
   const graft_config& c = h->cfg;
@@ -526,6 +543,9 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
   a.accept_len = d_accept_len; a.out_tokens = d_out_tokens;
   a.part = h->part; a.row_ticket = h->row_ticket; a.req_ticket = h->req_ticket; a.topk = h->topk;
   a.winner = h->winner; a.err = h->err; a.row_nseg = h->row_nseg;
+  a.sample = sample ? 1 : 0;
+  a.inv_temp = sample ? 1.f / temperature : 1.f;
+  a.u_accept = d_u_accept; a.u_resid = d_u_resid;
   const bool tma_fits = h->tma_ready && a.g.vec && a.g.row_vec_bytes >= graft::TMA_CHUNK &&
                         a.g.cpr <= graft::MAX_SPLIT && rows <= graft::verify_tma_max_rows(h->num_sms);
   a.upr = (int32_t)((a.g.nslot + 31) / 32);
@@ -552,7 +572,7 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update two-pass launch");
     h->last_launches = 2;
-    return GRAFT_OK;
+    return sample ? launch_sample_step(h, a, stream) : GRAFT_OK;
   }
   {
     ProfScope ps(h, (cudaStream_t)stream, use_tma ? "k_verify_tma" : "k_verify");
@@ -566,8 +586,32 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
   }
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update finish launch");
   h->last_launches = 2;
-  return GRAFT_OK;
+  return sample ? launch_sample_step(h, a, stream) : GRAFT_OK;
 }
+
+}  // namespace
+
+extern "C" {
+
+int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
+                        const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
+                        int64_t row_stride, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream) {
+  return verify_impl(h, batch, d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_logits, row_stride, d_accept_len,
+                     d_out_tokens, false, 1.f, nullptr, nullptr, stream);
+}
+
+int graft_verify_update_sample(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
+                               const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
+                               int64_t row_stride, float temperature, const float* d_u_accept,
+                               const float* d_u_resid, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream) {
+  if (!h) return GRAFT_EINVAL;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return fail(h, GRAFT_EINVAL, "temperature must be > 0");
+  if (batch > 0 && (!d_u_accept || !d_u_resid)) return fail(h, GRAFT_EINVAL, "null pointer");
+  return verify_impl(h, batch, d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_logits, row_stride, d_accept_len,
+                     d_out_tokens, true, temperature, d_u_accept, d_u_resid, stream);
+}
+
+
 
 int graft_get_matrix(graft_handle* h, int32_t* host_out, void* stream) {
   if (!h || !host_out) return fail(h, GRAFT_EINVAL, "null pointer");

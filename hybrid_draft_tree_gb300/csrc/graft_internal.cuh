@@ -73,6 +73,10 @@ struct VerifyArgs {
   unsigned long long* part;   // [rows][MAX_SPLIT][K] partial top-8 keys
   int32_t* row_ticket;        // [rows]
   int32_t* req_ticket;        // [batch]
+  int32_t sample;             // 1: acceptance by stochastic verification (k_sample), not greedy
+  float inv_temp;             // stochastic verification: 1 / temperature
+  const float* u_accept;      // stochastic verification: [batch][S] uniforms, one per candidate slot
+  const float* u_resid;       // stochastic verification: [batch] uniforms for the final draw
   int32_t* topk;              // [rows][K] staged top-8 ids
   int32_t* winner;            // [V] last-writer key (row + 1), 0 = none
   int32_t* row_nseg;          // [rows] number of partial top-8s the scan wrote for the row
@@ -82,13 +86,6 @@ struct VerifyArgs {
   uint32_t* err;
 };
 
-struct ScatterArgs {
-  int32_t rows, V;
-  const int32_t* tree_tok;
-  const int32_t* topk;
-  int32_t* winner;
-  int32_t* C;
-};
 
 struct WarmArgs {
   ScanGeom g;
@@ -141,6 +138,7 @@ __device__ __forceinline__ void st_keep(uint64_t* ptr, uint64_t v, uint64_t pol)
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t s);
 cudaError_t launch_check(const AssembleArgs& a, int32_t* event, float* best_out, cudaStream_t s);
 cudaError_t launch_coverage(const VerifyArgs& a, const int32_t* info, float* gain, int dtype, cudaStream_t s);
+cudaError_t launch_sample(const VerifyArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_retrieve(const AssembleArgs& a, const int32_t* event, int32_t* out, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
 int verify_ctas_per_sm();
@@ -149,7 +147,6 @@ cudaError_t prepare_verify_tma();
 cudaError_t launch_verify_tma(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
 size_t verify_tma_smem_bytes();
 int verify_tma_max_rows(int grid);
-cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s);
 cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s);
 cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
 cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s);

@@ -518,7 +518,7 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
     if (lane < K) a.topk[(size_t)row * K + lane] = key_id(keys[h]);
   }
   __syncthreads();
-  if (warp == 0) accept_request(a, b, lane);
+  if (warp == 0 && !a.sample) accept_request(a, b, lane);  // stochastic verification accepts in k_sample
 #pragma unroll
   for (int h = 0; h < (MAX_S + FW - 1) / FW; ++h) {
     const int i = warp + h * FW;
@@ -530,25 +530,6 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
     for (int r = row + 1 + lane; r < rows; r += 32) later |= (a.tree_tok[r] == t);
     const int32_t id = key_id(keys[h]);
     if (!__any_sync(FULL, later) && lane < K) st_keep(C + (size_t)t * K + lane, id, keep);
-  }
-}
-
-// ---- last-writer scatter into the matrix -------------------------------------
-constexpr int XT = 1024;
-__global__ __launch_bounds__(XT) void k_scatter(ScatterArgs a) {
-  for (int r = threadIdx.x; r < a.rows; r += XT) {
-    const int32_t t = a.tree_tok[r];
-    if (t >= 0 && t < a.V && a.winner[t] == r + 1) {
-      const int4* src = reinterpret_cast<const int4*>(a.topk + (size_t)r * K);
-      int4* dst = reinterpret_cast<int4*>(a.C + (size_t)t * K);
-      dst[0] = src[0];
-      dst[1] = src[1];
-    }
-  }
-  __syncthreads();
-  for (int r = threadIdx.x; r < a.rows; r += XT) {
-    const int32_t t = a.tree_tok[r];
-    if (t >= 0 && t < a.V) a.winner[t] = 0;
   }
 }
 
@@ -618,10 +599,6 @@ cudaError_t launch_verify(const VerifyArgs& a, int dtype, int grid, cudaStream_t
 }
 cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
   k_finish<<<a.batch, FT, 0, s>>>(a, C);
-  return cudaGetLastError();
-}
-cudaError_t launch_scatter(const ScatterArgs& a, cudaStream_t s) {
-  k_scatter<<<1, XT, 0, s>>>(a);
   return cudaGetLastError();
 }
 cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s) {

@@ -245,68 +245,6 @@ static __device__ void accept_request(const VerifyArgs& a, int b, int lane, cons
   }
 }
 
-// ---- row and request completion (one warp) ---------------------------------------
-// Stage the row's top-8, claim its token's matrix row (largest row index wins:
-// the last writer in (request, slot) order), and run acceptance if this row
-// completes its request (atomic ticket over the request's valid rows).
-static __device__ void finish_row(const VerifyArgs& a, int row, u64 key, int lane) {
-  if (lane < K) a.topk[(size_t)row * K + lane] = key_id(key);
-  const int32_t tok = a.tree_tok[row];
-  if (lane == 0) atomicMax(&a.winner[tok], row + 1);
-  __threadfence();
-  __syncwarp();
-  const int S = a.S;
-  const int b = row / S;
-  const size_t base = (size_t)b * S;
-  bool v0 = false, v1 = false;
-  if (lane < S) { const int32_t t = a.tree_tok[base + lane]; v0 = t >= 0 && t < a.g.V; }
-  if (lane + 32 < S) { const int32_t t = a.tree_tok[base + lane + 32]; v1 = t >= 0 && t < a.g.V; }
-  const int nv = __popc(__ballot_sync(FULL, v0)) + __popc(__ballot_sync(FULL, v1));
-  int t = 0;
-  if (lane == 0) t = atomicAdd(&a.req_ticket[b], 1);
-  t = __shfl_sync(FULL, t, 0);
-  if (t == nv - 1) {
-    if (lane == 0) a.req_ticket[b] = 0;
-    __threadfence();
-    accept_request(a, b, lane);
-  }
-}
-
-// A CTA's top-8 of one row segment: write it as partial `seg` of `nseg`; the
-// last of the row's CTAs merges the partials and finishes the row.
-static __device__ __noinline__ void finish_segment_warp(const VerifyArgs& a, int row, u64 key, int seg, int nseg, int lane) {
-  bool fin = true;
-  if (nseg > 1) {
-    if (lane < K) a.part[((size_t)row * MAX_SPLIT + seg) * K + lane] = key;
-    __threadfence();
-    __syncwarp();
-    int t = 0;
-    if (lane == 0) t = atomicAdd(&a.row_ticket[row], 1);
-    t = __shfl_sync(FULL, t, 0);
-    fin = (t == nseg - 1);
-    if (fin) {
-      if (lane == 0) a.row_ticket[row] = 0;
-      __threadfence();
-      key = warp_merge_global(a.part + (size_t)row * MAX_SPLIT * K, nseg * K, lane);
-    }
-  }
-  if (fin) finish_row(a, row, key, lane);
-}
-
-// Requests with no valid slot have no row to finish them: one warp of CTA c
-// checks requests c, c + G, ... and writes their empty result (accept length
-// 0, no tokens).
-static __device__ __noinline__ void finish_empty_requests(const VerifyArgs& a, int c, int G, int lane) {
-  const int S = a.S;
-  for (int b = c; b < a.batch; b += G) {
-    const size_t base = (size_t)b * S;
-    bool v0 = false, v1 = false;
-    if (lane < S) { const int32_t t = a.tree_tok[base + lane]; v0 = t >= 0 && t < a.g.V; }
-    if (lane + 32 < S) { const int32_t t = a.tree_tok[base + lane + 32]; v1 = t >= 0 && t < a.g.V; }
-    if (!__any_sync(FULL, v0 || v1)) accept_request(a, b, lane);
-  }
-}
-
 // ---- pieces shared by the row-selection kernels ------------------------------------
 template <int DT>
 static __device__ __noinline__ u64 exact_row(const uint4* rowv, int64_t nslot, const char* rowp, int tail, int lane) {

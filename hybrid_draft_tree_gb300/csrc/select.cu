@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
   }
   __syncthreads();
   // requests with no valid slot have no row to finish them
-  if (warp == 0)
+  if (warp == 0 && !a.sample)
     for (int b = blockIdx.x; b < a.batch; b += gridDim.x)
       if (request_valid(a, stok, b, lane) == 0) accept_request(a, b, lane, stok);
   if (!live) return;
@@ -301,7 +301,9 @@ __global__ void __launch_bounds__(SW * 32) k_select(VerifyArgs a, int32_t* C) {
 
   // 6. the warp that completes the request's last valid row runs acceptance:
   //    the warp's writes are released by lane 0's ticket increment, and the
-  //    last incrementer acquires every other row's
+  //    last incrementer acquires every other row's (stochastic verification
+  //    accepts in its own kernel)
+  if (a.sample) return;
   __syncwarp();
   const int b = row / a.S;
   int t = 0;

@@ -26,7 +26,8 @@ EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup"
            "graft_verify_update", "graft_get_matrix", "graft_set_matrix", "graft_matrix_device_ptr",
            "graft_sync", "graft_last_error", "graft_last_launch_count", "graft_verify_update_noalloc",
            "graft_profile_enable", "graft_profile_read", "graft_check", "graft_retrieve", "graft_assemble_staged",
-           "graft_confidence", "graft_calibrate_thresholds", "graft_set_thresholds", "graft_coverage")
+           "graft_confidence", "graft_calibrate_thresholds", "graft_set_thresholds", "graft_coverage",
+           "graft_verify_update_sample")
 
 
 def calibrate_thresholds(best: np.ndarray, quantile: float) -> np.ndarray:
@@ -88,6 +89,7 @@ def load(build_if_missing: bool = True):
     L.graft_calibrate_thresholds.argtypes = [vp, i32, ctypes.c_double, vp]
     L.graft_set_thresholds.argtypes = [vp, vp]
     L.graft_coverage.argtypes = [vp, i32, vp, vp, vp, vp, i64, vp, vp]
+    L.graft_verify_update_sample.argtypes = [vp, i32, vp, vp, vp, vp, vp, i64, ctypes.c_float, vp, vp, vp, vp, vp]
     L.graft_get_matrix.argtypes = [vp, vp, vp]
     L.graft_set_matrix.argtypes = [vp, vp, vp]
     L.graft_matrix_device_ptr.argtypes = [vp]
@@ -219,6 +221,14 @@ class Graft:
         self._check(self.L.graft_verify_update(self.h, batch, _ptr(tree_tok), _ptr(tree_parent), _ptr(tree_pos),
                                                _ptr(tree_mask), _ptr(logits), stride, _ptr(accept_len),
                                                _ptr(out_tokens), _stream(stream)))
+
+    def verify_update_sample(self, batch, tree_tok, tree_parent, tree_pos, tree_mask, logits, temperature, u_accept,
+                             u_resid, accept_len, out_tokens, stream=None):
+        stride = logits.stride(-2)
+        self._check(self.L.graft_verify_update_sample(self.h, batch, _ptr(tree_tok), _ptr(tree_parent), _ptr(tree_pos),
+                                                      _ptr(tree_mask), _ptr(logits), stride, ctypes.c_float(temperature),
+                                                      _ptr(u_accept), _ptr(u_resid), _ptr(accept_len),
+                                                      _ptr(out_tokens), _stream(stream)))
 
     def get_matrix(self, stream=None) -> np.ndarray:
         out = np.empty((self.cfg.vocab, K), np.int32)

@@ -217,6 +217,28 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
                         const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
                         int64_t row_stride, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream);
 
+/* Stochastic variant of graft_verify_update (article §二 third gear: the
+ * output distribution equals sampling from the target at `temperature`).
+ * The top-8 of every valid row and the matrix update are those of
+ * graft_verify_update; acceptance instead walks the tree from the root: at
+ * node n with p = softmax(row_n / temperature), n's children are tested in
+ * slot order, child c accepted when d_u_accept[b][c] * rem < p(token of c),
+ * rem being the mass of the tokens not yet rejected at n (a repeated token
+ * has none left); acceptance descends into c.  When every child of n is
+ * rejected, or n is a leaf, the final token is the first v (in id order)
+ * whose cumulative mass among the unrejected tokens exceeds
+ * d_u_resid[b] * their total.  Every emitted token is so distributed exactly
+ * as the target's p, whatever the candidates.
+ *   d_u_accept  DEVICE float [batch][S], uniforms in [0, 1), one per slot
+ *   d_u_resid   DEVICE float [batch], uniforms in [0, 1)
+ *   d_accept_len[b] = accepted path length; d_out_tokens[b] = path tokens,
+ *   then the final token, then -1s.  Probabilities are computed in fp32.
+ * Asynchronous; GRAFT_EINVAL for a temperature that is not finite and > 0. */
+int graft_verify_update_sample(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
+                               const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
+                               int64_t row_stride, float temperature, const float* d_u_accept,
+                               const float* d_u_resid, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream);
+
 /* Allocation-free variant of graft_verify_update.  It has no counterpart in
  * the paper: it is an integration entry point for callers that cannot call
  * cudaMalloc, such as an engine that records its decode step into a CUDA

@@ -201,6 +201,64 @@ def verify(tree: Tree, logits: np.ndarray, dtype: int):
     return int(acc[0]), out, topk
 
 
+def verify_sample(tree: Tree, logits: np.ndarray, dtype: int, inv_temp: float, u: np.ndarray, u_res: float):
+    """Lossless stochastic verification of one request (article section 二
+    third gear: the output distribution equals sampling from the target), in
+    fp64.  The candidates are deterministic (draft top-k and retrieved
+    tokens), so they are tested one by one: at node n with target
+    distribution p = softmax(row_n * inv_temp), child c (slot order) is
+    accepted when u[c] * rem < p(tok_c), rem being the mass not yet rejected
+    at n; a rejected token's mass leaves rem (a repeated token has none
+    left).  On acceptance the walk descends into c.  When every child is
+    rejected (or n is a leaf) the last token is drawn from p restricted to
+    the unrejected tokens: the first v whose cumulative mass exceeds
+    u_res * (their total).  Each token so emitted is distributed exactly as p.
+    Returns (accept_len, emitted [S] padded with -1, smallest decision margin
+    relative to the mass compared against)."""
+    S = len(tree.tok)
+    vals = np.asarray(logits)
+    if dtype == BF16:
+        vals = (vals.astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+    vals = vals.astype(np.float64)
+    out = np.full(S, -1, np.int32)
+    if tree.tok[0] < 0:
+        return 0, out, np.inf
+    node, length, margin = 0, 0, np.inf
+    while True:
+        x = vals[node]
+        w = np.exp((x - x.max()) * inv_temp)
+        p = w / w.sum()
+        rem, rejected, acc = 1.0, set(), -1
+        for j in range(node + 1, S):
+            tk = int(tree.tok[j])
+            if tree.par[j] != node or tk < 0 or tk in rejected:
+                continue
+            margin = min(margin, abs(u[j] * rem - p[tk]) / max(p[tk], 1e-300))
+            if u[j] * rem < p[tk]:
+                acc = j
+                break
+            rem -= p[tk]
+            rejected.add(tk)
+        if acc >= 0:
+            out[length] = tree.tok[acc]
+            length += 1
+            node = acc
+            continue
+        w2 = w.copy()
+        w2[list(rejected)] = 0.0
+        cum = np.cumsum(w2)
+        if cum[-1] <= 0.0:                       # every token with mass was rejected: undefined
+            out[length] = len(cum) - 1
+            return length, out, 0.0
+        target = u_res * cum[-1]
+        v = int(np.searchsorted(cum, target, side="right"))
+        v = min(v, len(cum) - 1)
+        lo = cum[v - 1] if v > 0 else 0.0
+        margin = min(margin, min(target - lo, cum[v] - target) / cum[-1])
+        out[length] = v
+        return length, out, margin
+
+
 def update(C: np.ndarray, tree: Tree, topk: np.ndarray):
     _check(lib().or_update(_p(C), C.shape[0], len(tree.tok), _p(tree.tok),
                            _p(np.ascontiguousarray(topk, np.int32))), "or_update")

@@ -329,6 +329,56 @@ def test_coverage_gain_matches_oracle(wid, B):
     eng.close()
 
 
+@pytest.mark.parametrize("wid,B,temp", [(0, 4, 1.0), (0, 4, 0.7), (2, 4, 1.0), (4, 8, 1.5)])
+def test_stochastic_verification_matches_oracle(wid, B, temp):
+    """Sampling acceptance against the oracle's fp64 walk on the same
+    uniforms, closed loop.  Where a decision of the oracle lies within 2e-5
+    (relative) of its threshold, fp32 and fp64 may take either side (the
+    kernel's sums of exp over a row carry ~1e-6 relative error), so only
+    requests whose every decision is clear are compared; the matrix update
+    is the greedy one and is compared always."""
+    from workloads.device_loop import DeviceLoop
+    w = W.WORKLOADS[wid].scaled(V=5000, B=B, draft_sigma=0.75, bias=12.0)   # a confident target: paths get accepted
+    eng = engine_for(w)
+    loop = DeviceLoop(w, eng)
+    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
+    C = oracle.new_matrix(w.V)
+    rng = np.random.default_rng(wid * 10 + int(temp * 10))
+    compared = total = accepted = 0
+    for step in range(10):
+        tok, par, aux = loop.draft()
+        loop.assemble()
+        trees = [oracle.assemble(P, loop.root_h[b], tok[b], aux[b], C, None if par is None else par[b])
+                 for b in range(w.B)]
+        assert_trees_equal(loop, trees, step)
+        loop.make_logits()
+        tt = np.stack([t.tok for t in trees])
+        pp = np.stack([t.par for t in trees]).astype(np.int8)
+        lg = loop.h.tree_logits(tt, pp, loop.ctx_h, loop.prev_h)
+        u = rng.random((w.B, w.S)).astype(np.float32)
+        ur = rng.random(w.B).astype(np.float32)
+        eng.verify_update_sample(w.B, loop.tok, loop.par, loop.pos, loop.mask, loop.logits, temp,
+                                 torch.from_numpy(u).cuda(), torch.from_numpy(ur).cuda(), loop.accept_len,
+                                 loop.out_tokens)
+        acc_g = loop.accept_len.cpu().numpy()
+        out_g = loop.out_tokens.cpu().numpy()
+        for b in range(w.B):
+            acc, out, margin = oracle.verify_sample(trees[b], lg[b], w.dtype, 1.0 / temp, u[b].astype(np.float64),
+                                                    float(ur[b]))
+            total += 1
+            if margin > 2e-5:
+                compared += 1
+                assert acc_g[b] == acc and np.array_equal(out_g[b], out), (step, b, acc_g[b], acc, out_g[b], out)
+                accepted += acc
+            _, _, topk = oracle.verify(trees[b], lg[b], w.dtype)
+            oracle.update(C, trees[b], topk)
+        assert np.array_equal(eng.get_matrix(), C), step
+        loop.advance()
+    assert eng.sync() == 0
+    assert compared >= 0.5 * total and accepted > 0, (compared, total, accepted)
+    eng.close()
+
+
 @pytest.mark.parametrize("wid", [1, 3])
 def test_lockstep_warmup_small(wid):
     base = W.WORKLOADS[wid]

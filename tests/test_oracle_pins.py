@@ -349,6 +349,68 @@ def test_coverage_is_the_mass_of_the_new_tokens():
     assert abs(oracle.coverage(t, t.info, rows, oracle.F32) - expect) < 1e-6 * expect   # fp32 logs of 1..V
 
 
+# ----------------------------------------------------------------------------- stochastic verification
+def _sample_tree():
+    """Root (token 0) with children 2, 4, 2 (slots 1-3, a repeated token) and
+    a grandchild 5 under slot 1 (slot 4)."""
+    t = oracle.Tree(6)
+    t.tok[:5] = [0, 2, 4, 2, 5]
+    t.par[:5] = [-1, 0, 0, 0, 1]
+    return t
+
+
+def test_stochastic_verification_is_lossless():
+    """Each emitted token is distributed as the target's softmax: the first
+    as p(root row), the second, after the first was slot 1's token, as
+    p(slot 1's row) -- Monte Carlo over seeded uniforms, 5-sigma bounds."""
+    rng = np.random.default_rng(7)
+    V = 6
+    rows = rng.normal(0, 1, (6, V)).astype(np.float32)
+    rows[0, 2] += 1.0
+    t = _sample_tree()
+    p0 = np.exp(rows[0].astype(np.float64) - rows[0].max()); p0 /= p0.sum()
+    p1 = np.exp(rows[1].astype(np.float64) - rows[1].max()); p1 /= p1.sum()
+    N = 20000
+    first = np.zeros(V)
+    second = np.zeros(V)
+    n_after_2 = 0
+    for _ in range(N):
+        u = rng.random(6)
+        acc, out, _ = oracle.verify_sample(t, rows, oracle.F32, 1.0, u, rng.random())
+        first[out[0]] += 1
+        if out[0] == 2 and acc >= 1:
+            second[out[1]] += 1
+            n_after_2 += 1
+    for v in range(V):
+        assert abs(first[v] / N - p0[v]) < 5 * np.sqrt(p0[v] * (1 - p0[v]) / N) + 1e-3, (v, first[v] / N, p0[v])
+    # slot 1 (token 2) is tested before slot 3 (also 2), so an accepted 2 always descends into slot 1
+    for v in range(V):
+        m = n_after_2
+        assert abs(second[v] / m - p1[v]) < 5 * np.sqrt(p1[v] * (1 - p1[v]) / m) + 2e-3, (v, second[v] / m, p1[v])
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_stochastic_verification_at_low_temperature_is_greedy(seed):
+    """As the temperature goes to 0 the target puts all its mass on the
+    argmax, and on trees without repeated sibling tokens the walk accepts
+    exactly the greedy path and emits the greedy bonus token."""
+    rng = np.random.default_rng(seed)
+    S, V = 16, 12
+    rows = rng.normal(0, 1, (S, V)).astype(np.float32)
+    t = oracle.Tree(S)
+    t.tok[0], t.par[0] = 0, -1
+    used = {}
+    for i in range(1, S):
+        p = int(rng.integers(0, i))
+        cand = [v for v in range(V) if v not in used.setdefault(p, set())]
+        tk = int(np.argmax(rows[p])) if rng.random() < 0.5 and np.argmax(rows[p]) in cand else int(rng.choice(cand))
+        used[p].add(tk)
+        t.tok[i], t.par[i] = tk, p
+    acc_g, out_g, _ = oracle.verify(t, rows, oracle.F32)
+    acc_s, out_s, _ = oracle.verify_sample(t, rows, oracle.F32, 1e4, rng.random(S) * 0.999, 0.5)
+    assert acc_s == acc_g and np.array_equal(out_s, out_g)
+
+
 def test_empty_matrix_gives_pruned_only_tree():
     V = 1000
     P = oracle.make_params(V)
