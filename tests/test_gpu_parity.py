@@ -618,6 +618,13 @@ def test_verify_unaligned_rows(dtype, pad, off):
 
 
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_verify_beyond_the_two_pass_row_limit(dtype):
+    """More verified rows than the two-pass scan takes (4096): the automatic
+    choice falls back to the single-pass scan; same results."""
+    _verify_case(1024, dtype, 61, 72, _normal, seed=5)          # 72 x 61 = 4392 rows
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
 @pytest.mark.parametrize("fn", [_ties, _constant])
 def test_verify_ties_and_candidate_overflow(dtype, fn):
     """Heavy ties and all-equal rows (more candidates than the list holds:
