@@ -1,6 +1,9 @@
 // C ABI of libgraft: handle management, argument checking and launches.
 // The method (popular-science article on arXiv 2605.20104, section 二) is
-// described in include/graft.h; the kernels live in assemble.cu and scan.cu.
+// described in include/graft.h; the kernels live in assemble.cu (assembly,
+// incremental drafting, confidences), umax.cu + select.cu (the default verify
+// scan), scan.cu (single-pass scan, finishing, warm-up), scan_tma.cu,
+// sample.cu (stochastic verification), coverage.cu and noalloc.cu.
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>

@@ -1,4 +1,4 @@
-// Streaming kernels of graft_verify_update and graft_warmup.
+// Single-pass verify scan, its finishing kernel, and the warm-up kernels.
 //
 // The hot loop of a Graft step is the read of every verified slot's logits
 // row (popular-science article on arXiv 2605.20104, section 二 third gear:
@@ -7,8 +7,18 @@
 // Greedy verification needs each row's argmax and the update needs its
 // top-8, so one pass computes the top-8 and element 0 serves as the argmax.
 //
-// Per CTA and round every thread holds NV 16-byte vectors in registers (all
-// loads in flight at once), then
+// The default path for 16-byte aligned rows is the two-pass scan (umax.cu,
+// select.cu).  This file holds the single-pass scan, taken for rows that are
+// not 16-byte aligned, for more rows than the two-pass scan takes, and by the
+// allocation-free entry point: k_verify streams equal contiguous slices of
+// the valid rows, keeps a lock-free running top-8 per row segment in shared
+// memory, and hands each segment's top-8 to k_finish (one CTA per request),
+// which merges a row's partials, runs the acceptance walk on bit masks and
+// writes the matrix rows (the last writer wins).
+//
+// The warm-up kernels load the matrix from the last occurrence of each token;
+// their row selection (scan_range) is CTA-wide: per round every thread holds
+// NV 16-byte vectors (all loads in flight), then
 //   pass 1: per-thread max -> per-warp max; T = min over the 8 warp maxima is
 //           a value that at least 8 elements of the round reach, and the 8th
 //           best value seen by the CTA so far is another; the larger of the
@@ -17,10 +27,7 @@
 //           candidate list; warp 0 merges them into the running top-8 with a
 //           32-lane bitonic sort on 64-bit keys (value desc, id asc).
 // If the candidate list overflows (e.g. a row of equal values) the CTA falls
-// back to an exact 8-round selection over its registers.
-// A row split over several CTAs hands partial top-8s to the last CTA of the
-// row (atomic ticket, no waiting); the last row of a request runs the
-// acceptance walk on bit masks.  Nothing ever spins.
+// back to an exact 8-round selection over its registers.  Nothing ever spins.
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
