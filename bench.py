@@ -191,6 +191,13 @@ def traffic_record(kernel):
     return rec
 
 
+def workload_config(w, ws):
+    """The `config` object of both arms' JSON lines: what the workload is."""
+    return {"workload": w.name, "vocab": w.V, "batch": w.B, "slots_per_request": w.S, "draft_sigma": w.draft_sigma,
+            "mode": ["checkpoint", "static", "tail"][w.mode], "logits_bytes_per_step": w.logits_bytes_per_step(),
+            "parallelism": "replicas" if ws > 1 else "single"}
+
+
 def max_over_ranks(x: float, device=None) -> float:
     """Largest value of x over all ranks (the job's time is its slowest rank's)."""
     import torch
@@ -334,13 +341,10 @@ def run_graft(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "vocab": w.V, "batch": w.B, "slots_per_request": w.S,
-                   "draft_sigma": w.draft_sigma,
-                   "mode": ["checkpoint", "static", "tail"][w.mode],
-                   "logits_bytes_per_step": w.logits_bytes_per_step(),
-                   "l2": "flushed before each graft call (256 MB written, then read back); logits 296.6 MB > L2",
-                   "timed": "assemble + verify_update per step (CUDA events on the library stream)",
-                   "parallelism": "replicas" if ws > 1 else "single"},
+        "config": workload_config(w, ws),
+        "timing": {"l2": "flushed before each graft call (256 MB written, then read back); logits "
+                         f"{w.logits_bytes_per_step() / 1e6:.1f} MB per step",
+                   "timed": "assemble + verify_update per step (CUDA events on the library stream)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": tr["bytes_per_launch"] if tr else None,
                      "peak_source": f"{peak_kind} hbm_gbs (of measured)", "kernel": dominant,
@@ -466,6 +470,8 @@ def main():
             torch.cuda.set_device(local)
         torch.distributed.init_process_group(backend)
     w = W.WORKLOADS[args.workload]
+    if args.draft_sigma is not None:
+        w = w.scaled(draft_sigma=args.draft_sigma)
     if args.impl == "reference":
         if rank != 0:
             return
@@ -479,7 +485,7 @@ def main():
                "warmup": args.warmup, "ms_per_step": round(1e3 / v, 3), "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
                "data": "synthetic", "impl": "reference",
-               "config": {"workload": w.name, "vocab": w.V, "batch": w.B, "slots_per_request": w.S},
+               "config": workload_config(w, ws),
                "cpu_baseline": {"value": round(v, 5), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
                                 "cpu": cpu_model()},
                "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
