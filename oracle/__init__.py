@@ -2,9 +2,15 @@
 
 A ctypes front-end for ``graft_oracle.c``, the plain single-threaded CPU
 restatement of one Graft decode step (arXiv 2605.20104; the Hugging Face
-paper page's abstract and the popular-science article's sections 二, 四, 六 and
-七).  Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
-baseline may import this package; the CUDA library never does.
+paper page's abstract and the popular-science article's sections 二 to 七),
+plus two fp64 numpy restatements written here: the coverage gain (section
+三) and lossless stochastic verification (section 二, third gear).  Only the
+test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU baseline may
+import this package; the CUDA library never does.
+
+Parity unpinned beyond their stated rules (the pages give no procedure): the
+coverage gain's boundary and novelty rule, and the stochastic walk's order of
+candidates; the tests pin each by closed forms, Monte Carlo and limits.
 
 All arrays are numpy.  Nothing here touches a GPU.
 """

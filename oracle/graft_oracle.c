@@ -24,6 +24,8 @@
  *        update the matrix row of every verified position, accepted or not.
  *        Section 四 (batched serving): fixed verify slots per request, low
  *        confidence draft nodes replaced in place by retrieval nodes.
+ *        Section 五 (ablations): pruning without retrieval, and a fixed
+ *        draft/retrieval split instead of the confidence checkpoints.
  *        Section 六: warm-up writes target distributions into the matrix.
  *        Section 七 (Graft-TAIL): keep a block draft's confident prefix and
  *        replace the low-confidence tail with retrieval at equal budget.
@@ -40,6 +42,12 @@
  *   is root, kept draft (BFS), realised retrieval (template order); argmax
  *   and top-k ties go to the lower token id, -0 equals +0, NaN is an error;
  *   the last writer in (request, slot) order wins a matrix row.
+ *
+ * Parity unpinned: the pages fix no value or rule to check the following
+ * against, so the tests pin the rule stated here and its invariants instead
+ * of an external value: the template's order (or_template), the static
+ * mode's replacement rank among replaced siblings, and the fixed split's
+ * ratio in the ablation (a parameter).
  *
  * Floating point: path confidences are fp32 products taken root to leaf (the
  * same precision as the CUDA kernels, because they decide which nodes are
