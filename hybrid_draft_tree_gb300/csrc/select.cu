@@ -25,7 +25,7 @@ constexpr int ECAP = 192;          // candidate elements per row
 constexpr int UCAP = 2 * (CCAP - ECAP);  // candidate units per row (int ids after the keys)
 constexpr int UB = 16;             // candidate units loaded at once per lane
 
-constexpr int SW = 4;  // pass-2 warps per CTA
+constexpr int SW = 8;  // pass-2 warps per CTA
 
 // Greedy acceptance of request b (one warp) from tree arrays staged in shared
 // memory (sp/spos/smask indexed by slot): match(i) = slot i is valid and is the

@@ -21,7 +21,7 @@ using namespace scan;
 constexpr int UT = 256;            // threads per CTA
 constexpr int UMAXROWS = 192;      // rows one CTA's slice may touch
 constexpr int UW = UT / 32;
-constexpr int UNV = 4;             // units (one 16-byte load per lane each) per warp iteration
+constexpr int UNV = 8;             // units (one 16-byte load per lane each) per warp iteration
 
 __device__ __forceinline__ uint4 neg_inf_vec(int dt) {
   const uint32_t w = dt == GRAFT_BF16 ? 0xFF80FF80u : 0xFF800000u;
