@@ -722,6 +722,54 @@ def test_invalid_arguments_are_rejected():
             g_.Graft(g_.graft_default_config(100, 2, mode, W.BF16, **kw))
 
 
+def test_step_replays_from_a_cuda_graph():
+    """assemble + verify_update (with the dependent launch of pass 2) are
+    captured into a CUDA graph and replayed: the same trees, acceptance and
+    matrix as the same calls made directly on an identical handle."""
+    from workloads.device_loop import DeviceLoop
+    w = W.WORKLOADS[2].scaled(V=40000, B=4)
+    eager = engine_for(w)
+    graphed = engine_for(w)
+    loop = DeviceLoop(w, eager)
+    for _ in range(3):                                 # fill the matrix a little
+        loop.step()
+    graphed.set_matrix(eager.get_matrix())
+    loop.draft()
+    side = torch.cuda.Stream()
+    outs = {}
+    for name, eng in (("eager", eager), ("graph", graphed)):
+        bufs = [torch.empty_like(t) for t in (loop.tok, loop.par, loop.pos, loop.mask, loop.info)]
+        acc = torch.empty_like(loop.accept_len)
+        out = torch.empty_like(loop.out_tokens)
+        par = loop.d_par
+
+        def step():
+            eng.assemble(w.B, loop.root, loop.d_tok, par, loop.d_aux, *bufs, stream=torch.cuda.current_stream())
+            eng.verify_update(w.B, bufs[0], bufs[1], bufs[2], bufs[3], loop.logits, acc, out,
+                              stream=torch.cuda.current_stream())
+        if name == "graph":
+            with torch.cuda.stream(side):
+                step()                                 # first call on the stream: nothing new is set up in capture
+            side.synchronize()
+            graphed.set_matrix(eager_matrix_before)
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_, stream=side):
+                step()
+            g_.replay()
+        else:
+            eager_matrix_before = eager.get_matrix()
+            loop.assemble()                            # logits of this step's tree (same tree as both will build)
+            loop.make_logits()
+            step()
+        torch.cuda.synchronize()
+        outs[name] = [t.clone() for t in bufs] + [acc.clone(), out.clone(), torch.from_numpy(eng.get_matrix())]
+    for x, y in zip(outs["eager"], outs["graph"]):
+        assert torch.equal(x, y)
+    assert eager.sync() == 0 and graphed.sync() == 0
+    eager.close()
+    graphed.close()
+
+
 def test_profile_api_reports_each_kernel():
     """Tracing: every kernel of a step is bracketed by events and reported."""
     from workloads.device_loop import DeviceLoop
