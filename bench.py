@@ -52,6 +52,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--scan-kernel", type=int, default=0, help="verify scan (graft_config.scan_kernel); 0 = automatic")
+    p.add_argument("--next-rows", action="store_true",
+                   help="also time the stochastic step and the confidence / coverage calls (JSON key next_rows)")
+    p.add_argument("--sample-temperature", type=float, default=1.0)
     p.add_argument("--draft-sigma", type=float, default=None,
                    help="sibling-logit scale of the synthetic drafter (default: the workload's)")
     return p.parse_args()
@@ -332,6 +335,7 @@ def run_graft(args, ws, rank, local):
     # the checkpoints are evaluated as the layers are drafted and the
     # retrieval is gathered beside the drafter
     incremental = run_incremental(w, eng, loop, stream, flush_l2) if w.mode == W.MODE_CHECKPOINT else None
+    next_rows = run_next_rows(args, w, eng, loop, stream, flush_l2) if args.next_rows else None
 
     # e2e through the C ABI from pinned host buffers
     e2e = run_e2e(args, w, eng, loop, stream, dev)
@@ -358,10 +362,71 @@ def run_graft(args, ws, rank, local):
         "gpu_launches": launches,
         "breakdown_ms": {"assemble": round(statistics.mean(t_asm), 5), "verify_update": round(statistics.mean(t_ver), 5)},
         "incremental": incremental,
+        "next_rows": next_rows,
         "stats": {"mean_accepted_tokens_per_step": round(mat, 4), "valid_rows_per_step": statistics.mean(valid_rows),
                   "wall_s": round(wall, 2)},
     }
     return out
+
+
+def run_next_rows(args, w, eng, loop, stream, flush_l2, steps=50):
+    """Timings of the calls beyond the greedy step, on this workload: the
+    stochastic step (assemble + verify_update_sample, events around the two
+    calls, L2 flushed before each) with its per-kernel times, and the traced
+    kernels of the confidence (tree modes) and coverage (checkpoint and tail
+    modes) calls."""
+    import torch
+    dev = stream.device
+    B, S = w.B, w.S
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    u = torch.empty((B, S), dtype=torch.float32, device=dev)
+    ur = torch.empty((B,), dtype=torch.float32, device=dev)
+    best = torch.empty((B, 3), dtype=torch.float32, device=dev)
+    gain = torch.empty((B,), dtype=torch.float32, device=dev)
+    temp = args.sample_temperature
+    ms_asm, ms_ver, acc = [], [], []
+    kern = {}
+    for k in range(steps + 3):
+        trace = k >= 3 and k % 2 == 1                   # alternate traced and untimed-by-events steps
+        eng.profile_enable(trace)
+        eng.profile_read()
+        loop.draft()
+        with torch.cuda.stream(stream):
+            u.uniform_(generator=gen)
+            ur.uniform_(generator=gen)
+            flush_l2()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        loop.assemble()
+        e[1].record(stream)
+        if w.mode != W.MODE_TAIL:
+            eng.confidence(B, loop.d_par, loop.d_aux, best, stream=stream)
+        loop.make_logits()
+        if w.mode != W.MODE_STATIC:
+            eng.coverage(B, loop.tok, loop.par, loop.info, loop.logits, gain, stream=stream)
+        with torch.cuda.stream(stream):
+            flush_l2()
+        e[2].record(stream)
+        eng.verify_update_sample(B, loop.tok, loop.par, loop.pos, loop.mask, loop.logits, temp, u, ur,
+                                 loop.accept_len, loop.out_tokens, stream=stream)
+        e[3].record(stream)
+        loop.advance()
+        if k >= 3:
+            if trace:
+                for name, ms in eng.profile_read():
+                    kern.setdefault(name, []).append(ms)
+            else:
+                ms_asm.append(e[0].elapsed_time(e[1]))
+                ms_ver.append(e[2].elapsed_time(e[3]))
+                acc.append(float(loop.accept_len.float().mean().item()))
+    eng.profile_enable(False)
+    step_ms = statistics.mean(ms_asm) + statistics.mean(ms_ver)
+    return {"stochastic_step": {"steps_per_s": round(1e3 / step_ms, 1), "ms_per_step": round(step_ms, 5),
+                                "temperature": temp, "mean_accept_len": round(statistics.mean(acc), 3)},
+            "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in sorted(kern.items())},
+            "note": "stochastic step = assemble + verify_update_sample (CUDA events, L2 flushed before each); "
+                    "kernels from alternate steps with tracing on; k_check here is graft_confidence"}
 
 
 def run_incremental(w, eng, loop, stream, flush_l2, steps=30):

@@ -496,8 +496,7 @@ int graft_coverage(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, co
   if (!d_tree_tok || !d_tree_parent || !d_info || !d_logits || !d_gain) return fail(h, GRAFT_EINVAL, "null pointer");
   if (row_stride < c.vocab) return fail(h, GRAFT_EINVAL, "row_stride < vocab");
   graft::VerifyArgs a{};
-  a.g.V = c.vocab;
-  a.g.stride = row_stride;
+  a.g = scan_geom(h, d_logits, row_stride, (int64_t)batch * h->S, h->scan_ctas_target);  // 16-byte loads when aligned
   a.S = h->S; a.batch = batch; a.logits = d_logits;
   a.tree_tok = d_tree_tok; a.tree_parent = d_tree_parent;
   cudaError_t e;

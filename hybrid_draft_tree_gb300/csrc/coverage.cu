@@ -8,62 +8,29 @@
 // a boundary candidate; its token is new unless a kept draft child of the same
 // parent carries it.  The gain is the sum, over the new tokens, of their
 // softmax probability in the parent's logits row.  A diagnostic off the hot
-// path: one CTA per request streams each boundary parent's row once.
+// path: one CTA per request streams each boundary parent's row once
+// (row_softmax.cuh).
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
+#include "row_softmax.cuh"
 #include "scan_common.cuh"
 
 namespace graft {
 namespace {
 using namespace scan;
+using namespace softmax;
 
 constexpr int CT = 256;
 
-// CTA-wide (max, sum of exp(x - max)) of one logits row.
-template <int DT>
-__device__ void row_lse(const char* rowp, int V, float* s_m, float* s_s, float& m_out, float& s_out) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  float m = -INFINITY, sum = 0.f;
-  for (int v = t; v < V; v += CT) {
-    const float x = load_scalar<DT>(rowp, v);
-    if (x > m) {
-      sum = sum * expf(m - x) + 1.f;
-      m = x;
-    } else if (x != -INFINITY) {
-      sum += expf(x - m);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(FULL, m, o), s2 = __shfl_xor_sync(FULL, sum, o);
-    const float mm = fmaxf(m, m2);
-    sum = (mm == -INFINITY) ? 0.f : sum * expf(m - mm) + s2 * expf(m2 - mm);
-    m = mm;
-  }
-  if (lane == 0) { s_m[warp] = m; s_s[warp] = sum; }
-  __syncthreads();
-  if (t == 0) {
-    float M = -INFINITY, Ssum = 0.f;
-    for (int w = 0; w < CT / 32; ++w) {
-      const float mm = fmaxf(M, s_m[w]);
-      Ssum = (mm == -INFINITY) ? 0.f : Ssum * expf(M - mm) + s_s[w] * expf(s_m[w] - mm);
-      M = mm;
-    }
-    s_m[0] = M;
-    s_s[0] = Ssum;
-  }
-  __syncthreads();
-  m_out = s_m[0];
-  s_out = s_s[0];
-  __syncthreads();
-}
+constexpr float LOG2E = 1.4426950408889634f;
 
 template <int DT>
 __global__ __launch_bounds__(CT) void k_coverage(VerifyArgs a, const int32_t* info, float* gain) {
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
-  __shared__ float s_m[CT / 32], s_s[CT / 32];
+  __shared__ RowStats<CT> st;
   __shared__ int32_t s_tok[MAX_S], s_par[MAX_S];
+  __shared__ float s_x[MAX_S];  // a boundary candidate's logit in its parent's row, by slot
   const int b = blockIdx.x, t = threadIdx.x, S = a.S;
   const int n_draft = info[(int64_t)b * 4 + 1], n_retr = info[(int64_t)b * 4 + 2];
   const int r0 = min(max(1 + n_draft, 1), S), r1 = min(r0 + max(n_retr, 0), S);
@@ -79,15 +46,17 @@ __global__ __launch_bounds__(CT) void k_coverage(VerifyArgs a, const int32_t* in
     for (int j = r0; j < r1; ++j) has |= s_par[j] == p;
     if (!has || s_tok[p] < 0 || s_tok[p] >= a.g.V) continue;  // (uniform: shared values)
     const char* rowp = reinterpret_cast<const char*>(a.logits) + ((size_t)b * S + p) * (size_t)a.g.stride * ES;
-    float M, Z;
-    row_lse<DT>(rowp, a.g.V, s_m, s_s, M, Z);
+    if (t >= r0 && t < r1 && s_par[t] == p && s_tok[t] >= 0 && s_tok[t] < a.g.V)
+      s_x[t] = load_scalar<DT>(rowp, s_tok[t]);  // fetched beside the row pass
+    row_stats<DT, CT>(rowp, a.g.V, a.g.vec != 0, LOG2E, st);
+    const float M = st.M, Z = st.W;
     if (t == 0 && Z > 0.f) {
       for (int j = r0; j < r1; ++j) {
         const int32_t tk = s_tok[j];
         if (s_par[j] != p || tk < 0 || tk >= a.g.V) continue;
         bool dup = false;  // a kept draft child of p with the same token is not new
         for (int q = 1; q < r0; ++q) dup |= s_par[q] == p && s_tok[q] == tk;
-        if (!dup) total += expf(load_scalar<DT>(rowp, tk) - M) / Z;
+        if (!dup) total += exp2f((s_x[j] - M) * LOG2E) / Z;
       }
     }
   }
