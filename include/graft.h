@@ -15,9 +15,15 @@
  *      path, ties to the lower token id);
  *   5. the online update: every verified position, accepted or rejected,
  *      overwrites C[its token] with the top-8 of its logits row.
+ * Around the step: warm-up of the matrix, incremental drafting (checkpoint
+ * verdicts as the drafter's layers complete, the retrieval gathered beside
+ * the drafter), the ablations without retrieval or with a fixed split,
+ * threshold calibration, the coverage-gain diagnostic, and lossless
+ * stochastic verification at a temperature.
  * Sources: Hugging Face paper page 2605.20104 (abstract); popular-science
- * article on the paper, section 二 (the three gears: steps 1-5), section 四
- * (static-tree batched mode), section 六 (warm-up), section 七 (Graft-TAIL).
+ * article on the paper, section 二 (the three gears: steps 1-5), section 三
+ * (superset argument, coverage gain), section 四 (static-tree batched mode),
+ * section 五 (ablations), section 六 (warm-up), section 七 (Graft-TAIL).
  *
  * Conventions (all entry points):
  *   - Pointers named d_* are DEVICE pointers owned by the caller; they must
