@@ -21,7 +21,7 @@ namespace {
 using namespace scan;
 using namespace softmax;
 
-constexpr int CT = 256;
+constexpr int CT = 1024;  // threads per CTA: one row per CTA, so memory parallelism comes from the threads
 
 constexpr float LOG2E = 1.4426950408889634f;
 

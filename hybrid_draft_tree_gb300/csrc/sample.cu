@@ -29,7 +29,7 @@ namespace {
 using namespace scan;
 using namespace softmax;
 
-constexpr int PT = 256;
+constexpr int PT = 1024;  // threads per CTA: one row per CTA, so memory parallelism comes from the threads
 constexpr float LOG2E = 1.4426950408889634f;
 
 template <int DT>
