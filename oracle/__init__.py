@@ -12,7 +12,9 @@ Parity unpinned beyond their stated rules (the pages give no procedure): the
 coverage gain's boundary and novelty rule, and the stochastic walk's order of
 candidates; the tests pin each by closed forms, Monte Carlo and limits.
 
-All arrays are numpy.  Nothing here touches a GPU.
+All arrays are numpy.  Nothing here touches a GPU.  ``GRAFT_ORACLE_LIB``, when
+set, names a prebuilt copy of the oracle library to load instead of building
+this one (the mutation tests point it at copies with a planted mistake).
 """
 from __future__ import annotations
 
@@ -56,7 +58,7 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
+        _lib = ctypes.CDLL(os.environ.get("GRAFT_ORACLE_LIB") or build())
     return _lib
 
 

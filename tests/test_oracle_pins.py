@@ -288,14 +288,17 @@ def test_incremental_checkpoints_match_brute_force(sigma):
             if len(layer) and layer.max() < np.float32(thr):
                 expect = d
                 break
-        ev = -1
+        ev = ev_full = -1
         for L in range(6):
             n = int((depth <= L).sum())
             ev = oracle.check_layer(P, par[:n], prob[:n], L, ev)
+            # the whole tree given early: layers past L are present but their
+            # checkpoints are not evaluated yet
+            ev_full = oracle.check_layer(P, par, prob, L, ev_full)
             if expect >= 0 and L >= expect:
-                assert ev == expect
+                assert ev == expect and ev_full == expect
             elif L < (expect if expect >= 0 else 99):
-                assert ev == -1
+                assert ev == -1 and ev_full == -1
         assert ev == expect
         assert oracle.assemble(P, int(root[0]), tok[0], prob, oracle.new_matrix(V), par).info[0] == expect
 
@@ -319,27 +322,52 @@ def test_retrieve_is_the_template_gather_of_the_fired_split():
 
 # ----------------------------------------------------------------------------- coverage gain (section 三)
 def _coverage_case():
-    """Root 0 with kept draft children 10, 11 (slots 1, 2) and retrieved
-    children 11, 12, 13 (slots 3-5, 11 duplicating a draft token) plus a
-    retrieved grandchild 14 (slot 6, not at the boundary)."""
-    t = oracle.Tree(8)
-    t.tok[:7] = [0, 10, 11, 11, 12, 13, 14]
-    t.par[:7] = [-1, 0, 0, 0, 0, 0, 3]
-    t.info[:] = [0, 2, 4, 7]
+    """Root 0 with kept draft children 10, 11 (slots 1, 2) and a kept draft
+    grandchild 12 under slot 1 (slot 3); retrieved children 11, 12, 13 of the
+    root (slots 4-6: 11 duplicates a drafted sibling, 12 only a drafted token
+    elsewhere in the tree) plus a retrieved grandchild 14 (slot 7, not at the
+    boundary)."""
+    t = oracle.Tree(9)
+    t.tok[:8] = [0, 10, 11, 12, 11, 12, 13, 14]
+    t.par[:8] = [-1, 0, 0, 1, 0, 0, 0, 4]
+    t.info[:] = [0, 3, 4, 8]
     return t
 
 
 def test_coverage_of_a_uniform_row_counts_new_candidates():
     t = _coverage_case()
     V = 40
-    rows = np.zeros((8, V), np.float32)
+    rows = np.zeros((9, V), np.float32)
     assert abs(oracle.coverage(t, t.info, rows, oracle.F32) - 2 / V) < 1e-15   # 12 and 13 are new; 11 is not
+
+
+# bfloat16 bit patterns of small integers (sign, 8 exponent bits with bias
+# 127, 7 fraction bits): 0 -> 0x0000, 1 -> 0x3F80, 2 -> 0x4000, 3 -> 0x4040,
+# 4 -> 0x4080, 5 -> 0x40A0, -1 -> 0xBF80, -2 -> 0xC000.
+BF16_OF_INT = {0: 0x0000, 1: 0x3F80, 2: 0x4000, 3: 0x4040, 4: 0x4080, 5: 0x40A0, -1: 0xBF80, -2: 0xC000}
+
+
+def _int_rows_both(shape, seed):
+    """Integer logits in [-2, 5] as float32 and as bf16 bit patterns."""
+    ints = np.random.default_rng(seed).integers(-2, 6, shape)
+    bits = np.vectorize(BF16_OF_INT.get)(ints).astype(np.uint16)
+    return ints.astype(np.float32), bits
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_coverage_of_bf16_rows_equals_their_values(seed):
+    t = _coverage_case()
+    f32, bits = _int_rows_both((9, 24), seed)
+    x = f32[0].astype(np.float64)
+    p = np.exp(x) / np.exp(x).sum()
+    assert abs(oracle.coverage(t, t.info, bits, oracle.BF16) - (p[12] + p[13])) < 1e-12
+    assert oracle.coverage(t, t.info, bits, oracle.BF16) == oracle.coverage(t, t.info, f32, oracle.F32)
 
 
 def test_coverage_is_the_mass_of_the_new_tokens():
     t = _coverage_case()
     V = 40
-    rows = np.full((8, V), -np.inf, np.float32)
+    rows = np.full((9, V), -np.inf, np.float32)
     rows[0, 12] = 3.0
     assert oracle.coverage(t, t.info, rows, oracle.F32) == 1.0          # all the mass on a new candidate
     rows[0, 12], rows[0, 11] = -np.inf, 3.0
@@ -387,6 +415,19 @@ def test_stochastic_verification_is_lossless():
     for v in range(V):
         m = n_after_2
         assert abs(second[v] / m - p1[v]) < 5 * np.sqrt(p1[v] * (1 - p1[v]) / m) + 2e-3, (v, second[v] / m, p1[v])
+
+
+def test_stochastic_verification_of_bf16_rows_equals_their_values():
+    """bf16 rows holding small integers walk exactly as the same values in
+    float32 (whose walk the Monte Carlo pin above ties to the target)."""
+    f32, bits = _int_rows_both((6, 8), 3)
+    t = _sample_tree()
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        u, ur = rng.random(6), rng.random()
+        a32, o32, _ = oracle.verify_sample(t, f32, oracle.F32, 0.7, u, ur)
+        a16, o16, _ = oracle.verify_sample(t, bits, oracle.BF16, 0.7, u, ur)
+        assert a32 == a16 and np.array_equal(o32, o16)
 
 
 @pytest.mark.parametrize("seed", range(10))
