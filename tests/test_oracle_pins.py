@@ -202,6 +202,30 @@ def test_checkpoint_firing_and_budget_table():
         assert tr.info[3] == 1 + tr.info[1] + tr.info[2] <= 61
 
 
+def _brute_force_template(depth, width):
+    """Every rank path of the template by exhaustive product over ranks,
+    kept when each step obeys the fan-out (anchor: min(8, width); after rank
+    r: min(8, max(1, width >> r))), in the order (rank sum, depth, path)."""
+    paths = []
+    for d in range(1, depth + 1):
+        for p in itertools.product(range(8), repeat=d):
+            if p[0] >= min(8, width):
+                continue
+            if all(b < min(8, max(1, width >> a)) for a, b in zip(p, p[1:])):
+                paths.append(p)
+    return sorted(paths, key=lambda p: (sum(p), len(p), p))
+
+
+@pytest.mark.parametrize("depth", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("width", [1, 2, 3, 4, 8, 16])
+def test_template_equals_brute_force_enumeration(depth, width):
+    want = _brute_force_template(depth, width)
+    for R in sorted({1, 7, 20, 52, min(len(want), 256)}):
+        par, rank, dep = oracle.template(R, depth=depth, width=width)
+        assert _paths(par, rank) == want[:R], (depth, width, R)
+        assert list(dep) == [len(p) for p in want[:R]]
+
+
 def test_template_width_above_eight_and_deep_chains():
     # width 16: the anchor's ranks are capped at the matrix row's 8; rank-r
     # nodes have min(8, max(1, 16 >> r)) children: 8+8+4+2+1+1+1+1 = 26
