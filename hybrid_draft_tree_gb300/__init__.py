@@ -5,8 +5,8 @@ ABI in include/graft.h); ``graft`` is its thin ctypes binding.
 """
 from .graft import (EXPORTS, GRAFT_BF16, GRAFT_F32, GRAFT_MODE_CHECKPOINT, GRAFT_MODE_STATIC, GRAFT_MODE_TAIL, Graft,
                     GraftError, TreeBuffers, calibrate_thresholds, graft_config, graft_default_config, library_path,
-                    load)
+                    load, template)
 
 __all__ = ["EXPORTS", "GRAFT_BF16", "GRAFT_F32", "GRAFT_MODE_CHECKPOINT", "GRAFT_MODE_STATIC", "GRAFT_MODE_TAIL",
            "Graft", "GraftError", "TreeBuffers", "calibrate_thresholds", "graft_config", "graft_default_config",
-           "library_path", "load"]
+           "library_path", "load", "template"]

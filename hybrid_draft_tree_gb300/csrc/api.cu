@@ -457,6 +457,24 @@ int graft_confidence(graft_handle* h, int32_t batch, const int16_t* d_draft_pare
   return GRAFT_OK;
 }
 
+int graft_template(int32_t depth, int32_t width, int32_t len, int32_t* parent_out, int32_t* rank_out,
+                   int32_t* depth_out) {
+  if (depth < 1 || depth > 16 || width < 1 || width > 64 || len < 0 || len > 65536) return GRAFT_EINVAL;
+  if (len > 0 && (!parent_out || !rank_out || !depth_out)) return GRAFT_EINVAL;
+  std::vector<int32_t> tp, tr, td;
+  try {
+    build_template(depth, width, len, tp, tr, td);
+  } catch (...) {
+    return GRAFT_ENOMEM;
+  }
+  for (size_t j = 0; j < tp.size(); ++j) {
+    parent_out[j] = tp[j];
+    rank_out[j] = tr[j];
+    depth_out[j] = td[j];
+  }
+  return (int)tp.size();
+}
+
 int graft_calibrate_thresholds(const float* best, int32_t n_rows, double quantile, float* thr_out) {
   if (!best || !thr_out || n_rows < 0 || !(quantile > 0.0 && quantile <= 1.0)) return GRAFT_EINVAL;
   for (int k = 0; k < 3; ++k) {

@@ -27,7 +27,7 @@ EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup"
            "graft_sync", "graft_last_error", "graft_last_launch_count", "graft_verify_update_noalloc",
            "graft_profile_enable", "graft_profile_read", "graft_check", "graft_retrieve", "graft_assemble_staged",
            "graft_confidence", "graft_calibrate_thresholds", "graft_set_thresholds", "graft_coverage",
-           "graft_verify_update_sample")
+           "graft_verify_update_sample", "graft_template")
 
 
 def calibrate_thresholds(best: np.ndarray, quantile: float) -> np.ndarray:
@@ -40,6 +40,18 @@ def calibrate_thresholds(best: np.ndarray, quantile: float) -> np.ndarray:
     if rc != 0:
         raise GraftError(rc, "graft_calibrate_thresholds")
     return out
+
+
+def template(depth: int = 8, width: int = 8, length: int = 60):
+    """The first `length` retrieval-template entries the library uses for
+    (depth, width), computed by the library (host code): arrays of the parent
+    entry (-1 = the anchor), the rank (matrix column) and the depth."""
+    par, rank, dep = (np.zeros(max(length, 1), np.int32) for _ in range(3))
+    n = load().graft_template(depth, width, length, par.ctypes.data_as(vp), rank.ctypes.data_as(vp),
+                              dep.ctypes.data_as(vp))
+    if n < 0:
+        raise GraftError(n, "graft_template")
+    return par[:n].copy(), rank[:n].copy(), dep[:n].copy()
 
 
 class GraftError(RuntimeError):
@@ -88,6 +100,7 @@ def load(build_if_missing: bool = True):
     L.graft_confidence.argtypes = [vp, i32, vp, vp, i32, vp, vp]
     L.graft_calibrate_thresholds.argtypes = [vp, i32, ctypes.c_double, vp]
     L.graft_set_thresholds.argtypes = [vp, vp]
+    L.graft_template.argtypes = [i32, i32, i32, vp, vp, vp]
     L.graft_coverage.argtypes = [vp, i32, vp, vp, vp, vp, i64, vp, vp]
     L.graft_verify_update_sample.argtypes = [vp, i32, vp, vp, vp, vp, vp, i64, ctypes.c_float, vp, vp, vp, vp, vp]
     L.graft_get_matrix.argtypes = [vp, vp, vp]

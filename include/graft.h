@@ -54,7 +54,7 @@ typedef struct graft_handle graft_handle;
 typedef enum {
   GRAFT_OK = 0,
   GRAFT_EINVAL = -1,   /* bad argument; nothing was queued */
-  GRAFT_ENOMEM = -2,   /* device allocation failed (graft_init only) */
+  GRAFT_ENOMEM = -2,   /* allocation failed (graft_init; graft_template on the host) */
   GRAFT_ECUDA = -3,    /* a CUDA call failed */
   GRAFT_EDEVICE = -4   /* a kernel flagged bad data (see graft_sync) */
 } graft_status;
@@ -172,6 +172,22 @@ int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, c
                 int32_t draft_nodes, int32_t layer, int32_t* d_event, void* stream);
 int graft_retrieve(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_event,
                    int32_t* d_retrieved, void* stream);
+
+/* The retrieval template (article §二, second gear: rank paths below the
+ * anchor; the rank-r successor of a node has max(1, width >> r) children of
+ * its own, the anchor min(8, width); depth <= `depth`; entries in increasing
+ * (rank sum, depth, rank path) order).  Host only, no handle, no GPU: writes
+ * the first min(len, template size) entries -- the template graft_init builds
+ * from tpl_depth / tpl_width, of which a split with R retrieval slots uses
+ * the first R -- as parent_out[j] (index of the parent entry, -1 = the
+ * anchor), rank_out[j] (the matrix column the entry gathers, 0..7) and
+ * depth_out[j] (1 = a child of the anchor).  Entry j is d_retrieved[b][j] of
+ * graft_retrieve.  The caller owns the three arrays (len int32 each; they may
+ * be null when len is 0).  Returns the number of entries written, or
+ * GRAFT_EINVAL for depth outside [1, 16], width outside [1, 64], len outside
+ * [0, 65536] or a null array. */
+int graft_template(int32_t depth, int32_t width, int32_t len, int32_t* parent_out, int32_t* rank_out,
+                   int32_t* depth_out);
 int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
                           const int16_t* d_draft_parent, const float* d_draft_prob, int32_t draft_nodes,
                           const int32_t* d_event, const int32_t* d_retrieved, int32_t* d_tree_tok,
