@@ -1,11 +1,13 @@
 """Host-side logic of the benchmark, on the CPU: the roofline's traffic
 record is used only while the kernel's source is unchanged, the peak comes
 from the measured file when present, and both arms describe the workload
-with the same config object."""
+with the same config object; the oracle arm's launch at N = 2."""
 import hashlib
 import importlib.util
 import json
 import os
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -51,3 +53,27 @@ def test_both_arms_share_the_workload_config():
     assert cfg["workload"] == w.name and cfg["vocab"] == 151936 and cfg["batch"] == 16
     assert cfg["slots_per_request"] == 61 and cfg["logits_bytes_per_step"] == 16 * 61 * 151936 * 2
     assert b.workload_config(w, 4)["parallelism"] == "replicas"
+
+
+def test_reference_arm_under_torchrun_world_size_2():
+    """The oracle arm launched like the GPU arm at N = 2 (torchrun, gloo on
+    the host): rank 0 alone prints one JSON line, every rank exits 0."""
+    import socket
+    import subprocess
+    import sys
+    pytest.importorskip("torch")
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
+                        "reference", "--gpus", "2", "--steps", "1", "--warmup", "0"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["steps"] == 1
+    assert out["value"] > 0 and out["cpu_baseline"]["kind"] == "oracle"
+    assert out["cpu_baseline"]["value"] == out["value"] == out["e2e"]["value"]
+    assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["d2h_bytes_per_step"] == 0
