@@ -3,7 +3,11 @@
 Argument marshalling only: every step of the Graft hot path runs in the CUDA
 kernels of libgraft.so.  Device buffers are torch CUDA tensors (their
 data_ptr is passed through); the stream is torch's current stream unless one
-is given.  There is no CPU fallback: if the library is missing or no CUDA
+is given.  Before a pointer is passed, its tensor is checked against what the
+C ABI expects of that buffer (CUDA memory, element type, contiguous layout,
+enough elements for the batch), because the library cannot see a tensor's
+size or memory kind: a violation raises GraftError(GRAFT_EINVAL) and nothing
+is queued.  There is no CPU fallback: if the library is missing or no CUDA
 device is present, these calls raise.
 """
 from __future__ import annotations
@@ -131,6 +135,57 @@ def _ptr(t):
     return vp(t.data_ptr())
 
 
+def _dtypes(*names):
+    import torch
+    return tuple(getattr(torch, n) for n in names if hasattr(torch, n))
+
+
+def _on_device(t) -> bool:
+    return bool(t.is_cuda)
+
+
+def _buf(t, name, dtypes, numel):
+    """Pointer to a caller's device buffer of at least `numel` elements of
+    one of `dtypes`, laid out contiguously.  None passes through as a null
+    pointer (the library decides where one is allowed)."""
+    if t is None:
+        return None
+    if not hasattr(t, "data_ptr") or not hasattr(t, "is_cuda"):
+        raise GraftError(GRAFT_EINVAL, f"{name}: expected a torch tensor, got {type(t).__name__}")
+    if t.dtype not in dtypes:
+        raise GraftError(GRAFT_EINVAL, f"{name}: dtype {t.dtype}, expected {' or '.join(map(str, dtypes))}")
+    if not t.is_contiguous():
+        raise GraftError(GRAFT_EINVAL, f"{name}: must be contiguous")
+    if t.numel() < numel:
+        raise GraftError(GRAFT_EINVAL, f"{name}: {t.numel()} elements, the call needs {numel}")
+    if not _on_device(t):
+        raise GraftError(GRAFT_EINVAL, f"{name}: expected a CUDA tensor (device buffer), got {t.device}")
+    return vp(t.data_ptr())
+
+
+def _rows(t, name, dtype, rows, vocab):
+    """(pointer, row stride) of logits rows: rows of >= `vocab` unit-stride
+    elements at one common stride (any leading shape that merges into one row
+    dimension), at least `rows` of them."""
+    if t is None:
+        return None, vocab
+    if not hasattr(t, "data_ptr") or not hasattr(t, "is_cuda"):
+        raise GraftError(GRAFT_EINVAL, f"{name}: expected a torch tensor, got {type(t).__name__}")
+    if t.dtype != dtype:
+        raise GraftError(GRAFT_EINVAL, f"{name}: dtype {t.dtype}, the handle's logits are {dtype}")
+    if t.dim() < 2 or t.stride(-1) != 1 or t.shape[-1] < vocab:
+        raise GraftError(GRAFT_EINVAL, f"{name}: expected rows [..., >= {vocab}] with unit stride in the last dim")
+    try:
+        t2 = t.view(-1, t.shape[-1])
+    except RuntimeError:
+        raise GraftError(GRAFT_EINVAL, f"{name}: the leading dims do not merge into rows at one stride") from None
+    if t2.shape[0] < rows:
+        raise GraftError(GRAFT_EINVAL, f"{name}: {t2.shape[0]} rows, the call needs {rows}")
+    if not _on_device(t):
+        raise GraftError(GRAFT_EINVAL, f"{name}: expected a CUDA tensor (device buffer), got {t.device}")
+    return vp(t.data_ptr()), (t2.stride(0) if t2.shape[0] > 1 else max(t2.stride(0), t.shape[-1]))
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -182,41 +237,71 @@ class Graft:
             pass
 
     # --- entry points (same names as the C ABI, without the prefix) ---------------
+    def _logits_dtype(self):
+        import torch
+        return torch.bfloat16 if self.cfg.logits_dtype == GRAFT_BF16 else torch.float32
+
+    def _tree(self, batch, tree_tok, tree_parent, tree_pos, tree_mask):
+        n = max(batch, 0) * self.S
+        return (_buf(tree_tok, "tree_tok", _dtypes("int32"), n), _buf(tree_parent, "tree_parent", _dtypes("int8"), n),
+                _buf(tree_pos, "tree_pos", _dtypes("int32"), n),
+                _buf(tree_mask, "tree_mask", _dtypes("int64", "uint64"), n))
+
+    def _draft(self, batch, draft_tok, draft_parent, draft_aux, n):
+        m = max(batch, 0) * n
+        return (_buf(draft_tok, "draft_tok", _dtypes("int32"), m), _buf(draft_parent, "draft_parent", _dtypes("int16"), m),
+                _buf(draft_aux, "draft_prob", _dtypes("float32"), m))
+
     def warmup(self, tokens, logits, stream=None):
         """tokens: int32 [N] CUDA; logits: [N, >=V] CUDA (bf16 or float32)."""
         n = tokens.numel()
-        self._check(self.L.graft_warmup(self.h, _ptr(tokens), _ptr(logits), n, logits.stride(0) if n else self.cfg.vocab,
-                                        _stream(stream)))
+        pt = _buf(tokens, "tokens", _dtypes("int32"), n)
+        pl, stride = _rows(logits, "logits", self._logits_dtype(), n, self.cfg.vocab)
+        self._check(self.L.graft_warmup(self.h, pt, pl, n, stride if n else self.cfg.vocab, _stream(stream)))
 
     def assemble(self, batch, root_tok, draft_tok, draft_parent, draft_aux, tree_tok, tree_parent, tree_pos, tree_mask,
                  info, stream=None):
         n = draft_tok.shape[-1]
-        self._check(self.L.graft_assemble(self.h, batch, _ptr(root_tok), _ptr(draft_tok), _ptr(draft_parent),
-                                          _ptr(draft_aux), n, _ptr(tree_tok), _ptr(tree_parent), _ptr(tree_pos),
-                                          _ptr(tree_mask), _ptr(info), _stream(stream)))
+        args = (_buf(root_tok, "root_tok", _dtypes("int32"), max(batch, 0)),
+                *self._draft(batch, draft_tok, draft_parent, draft_aux, n),
+                *self._tree(batch, tree_tok, tree_parent, tree_pos, tree_mask),
+                _buf(info, "info", _dtypes("int32"), max(batch, 0) * 4))
+        self._check(self.L.graft_assemble(self.h, batch, *args[:4], n, *args[4:], _stream(stream)))
 
     # incremental drafting (checkpoint mode): see graft_check in include/graft.h
     def check(self, batch, draft_parent, draft_prob, layer, event, stream=None):
         n = draft_parent.shape[-1]
-        self._check(self.L.graft_check(self.h, batch, _ptr(draft_parent), _ptr(draft_prob), n, layer, _ptr(event),
-                                       _stream(stream)))
+        m = max(batch, 0) * n
+        self._check(self.L.graft_check(self.h, batch, _buf(draft_parent, "draft_parent", _dtypes("int16"), m),
+                                       _buf(draft_prob, "draft_prob", _dtypes("float32"), m), n, layer,
+                                       _buf(event, "event", _dtypes("int32"), max(batch, 0)), _stream(stream)))
 
     def retrieve(self, batch, root_tok, event, retrieved, stream=None):
-        self._check(self.L.graft_retrieve(self.h, batch, _ptr(root_tok), _ptr(event), _ptr(retrieved),
+        b = max(batch, 0)
+        self._check(self.L.graft_retrieve(self.h, batch, _buf(root_tok, "root_tok", _dtypes("int32"), b),
+                                          _buf(event, "event", _dtypes("int32"), b),
+                                          _buf(retrieved, "retrieved", _dtypes("int32"), b * self.cfg.budget),
                                           _stream(stream)))
 
     def assemble_staged(self, batch, root_tok, draft_tok, draft_parent, draft_prob, event, retrieved, tree_tok,
                         tree_parent, tree_pos, tree_mask, info, stream=None):
         n = draft_tok.shape[-1]
-        self._check(self.L.graft_assemble_staged(self.h, batch, _ptr(root_tok), _ptr(draft_tok), _ptr(draft_parent),
-                                                 _ptr(draft_prob), n, _ptr(event), _ptr(retrieved), _ptr(tree_tok),
-                                                 _ptr(tree_parent), _ptr(tree_pos), _ptr(tree_mask), _ptr(info),
-                                                 _stream(stream)))
+        b = max(batch, 0)
+        args = (_buf(root_tok, "root_tok", _dtypes("int32"), b),
+                *self._draft(batch, draft_tok, draft_parent, draft_prob, n),
+                _buf(event, "event", _dtypes("int32"), b),
+                _buf(retrieved, "retrieved", _dtypes("int32"), b * self.cfg.budget),
+                *self._tree(batch, tree_tok, tree_parent, tree_pos, tree_mask),
+                _buf(info, "info", _dtypes("int32"), b * 4))
+        self._check(self.L.graft_assemble_staged(self.h, batch, *args[:4], n, *args[4:], _stream(stream)))
 
     # threshold calibration and the coverage diagnostic
     def confidence(self, batch, draft_parent, draft_prob, best, stream=None):
         n = draft_parent.shape[-1]
-        self._check(self.L.graft_confidence(self.h, batch, _ptr(draft_parent), _ptr(draft_prob), n, _ptr(best),
+        m = max(batch, 0) * n
+        self._check(self.L.graft_confidence(self.h, batch, _buf(draft_parent, "draft_parent", _dtypes("int16"), m),
+                                            _buf(draft_prob, "draft_prob", _dtypes("float32"), m), n,
+                                            _buf(best, "best", _dtypes("float32"), max(batch, 0) * 3),
                                             _stream(stream)))
 
     def set_thresholds(self, thr):
@@ -224,24 +309,35 @@ class Graft:
         self._check(self.L.graft_set_thresholds(self.h, t))
 
     def coverage(self, batch, tree_tok, tree_parent, info, logits, gain, stream=None):
-        self._check(self.L.graft_coverage(self.h, batch, _ptr(tree_tok), _ptr(tree_parent), _ptr(info), _ptr(logits),
-                                          logits.stride(-2), _ptr(gain), _stream(stream)))
+        b = max(batch, 0)
+        pl, stride = _rows(logits, "logits", self._logits_dtype(), b * self.S, self.cfg.vocab)
+        self._check(self.L.graft_coverage(self.h, batch, _buf(tree_tok, "tree_tok", _dtypes("int32"), b * self.S),
+                                          _buf(tree_parent, "tree_parent", _dtypes("int8"), b * self.S),
+                                          _buf(info, "info", _dtypes("int32"), b * 4), pl, stride,
+                                          _buf(gain, "gain", _dtypes("float32"), b), _stream(stream)))
 
     def verify_update(self, batch, tree_tok, tree_parent, tree_pos, tree_mask, logits, accept_len, out_tokens,
                       stream=None):
-        """logits: [batch*S, >=V] rows (any leading shape; the last dim's stride is 1)."""
-        stride = logits.stride(-2)
-        self._check(self.L.graft_verify_update(self.h, batch, _ptr(tree_tok), _ptr(tree_parent), _ptr(tree_pos),
-                                               _ptr(tree_mask), _ptr(logits), stride, _ptr(accept_len),
-                                               _ptr(out_tokens), _stream(stream)))
+        """logits: [batch*S, >=V] rows (any leading shape that merges into rows; the last dim's stride is 1)."""
+        b = max(batch, 0)
+        tree = self._tree(batch, tree_tok, tree_parent, tree_pos, tree_mask)
+        pl, stride = _rows(logits, "logits", self._logits_dtype(), b * self.S, self.cfg.vocab)
+        self._check(self.L.graft_verify_update(self.h, batch, *tree, pl, stride,
+                                               _buf(accept_len, "accept_len", _dtypes("int32"), b),
+                                               _buf(out_tokens, "out_tokens", _dtypes("int32"), b * self.S),
+                                               _stream(stream)))
 
     def verify_update_sample(self, batch, tree_tok, tree_parent, tree_pos, tree_mask, logits, temperature, u_accept,
                              u_resid, accept_len, out_tokens, stream=None):
-        stride = logits.stride(-2)
-        self._check(self.L.graft_verify_update_sample(self.h, batch, _ptr(tree_tok), _ptr(tree_parent), _ptr(tree_pos),
-                                                      _ptr(tree_mask), _ptr(logits), stride, ctypes.c_float(temperature),
-                                                      _ptr(u_accept), _ptr(u_resid), _ptr(accept_len),
-                                                      _ptr(out_tokens), _stream(stream)))
+        b = max(batch, 0)
+        tree = self._tree(batch, tree_tok, tree_parent, tree_pos, tree_mask)
+        pl, stride = _rows(logits, "logits", self._logits_dtype(), b * self.S, self.cfg.vocab)
+        self._check(self.L.graft_verify_update_sample(self.h, batch, *tree, pl, stride, ctypes.c_float(temperature),
+                                                      _buf(u_accept, "u_accept", _dtypes("float32"), b * self.S),
+                                                      _buf(u_resid, "u_resid", _dtypes("float32"), b),
+                                                      _buf(accept_len, "accept_len", _dtypes("int32"), b),
+                                                      _buf(out_tokens, "out_tokens", _dtypes("int32"), b * self.S),
+                                                      _stream(stream)))
 
     def get_matrix(self, stream=None) -> np.ndarray:
         out = np.empty((self.cfg.vocab, K), np.int32)
