@@ -212,6 +212,41 @@ def max_over_ranks(x: float, device=None) -> float:
     return float(t.item())
 
 
+def winner_slot(tok, par, accept_len, out_tokens) -> int:
+    """Slot of a request's deepest accepted node, recovered from the step's
+    outputs: the lowest slot at depth accept_len whose root path carries the
+    emitted tokens (verification breaks depth ties toward the lower slot).
+    Parents precede children in the flattened tree.  -1 for an empty tree."""
+    S = len(tok)
+    if S == 0 or tok[0] < 0:
+        return -1
+    depth = np.full(S, -1, np.int64)
+    depth[0] = 0
+    for i in range(1, S):
+        p = int(par[i])
+        if tok[i] < 0 or p < 0 or p >= i or depth[p] < 0:
+            continue
+        d = depth[p] + 1
+        if d <= accept_len and tok[i] == out_tokens[d - 1]:
+            depth[i] = d
+    hits = np.flatnonzero(depth == accept_len)
+    return int(hits[0]) if len(hits) else -1
+
+
+def retrieval_hits(mode, tok, par, info, accept_len, out_tokens):
+    """Per request: 1 when the deepest accepted node is a retrieved one, else
+    0 (None in static mode, whose in-place replacements the outputs do not
+    identify).  Checkpoint and tail trees hold their retrieved nodes after the
+    kept draft nodes: slots 1 + info[b][1] .. info[b][3] - 1."""
+    if mode == W.MODE_STATIC:
+        return None
+    hits = []
+    for b in range(len(accept_len)):
+        ws_ = winner_slot(tok[b], par[b], int(accept_len[b]), out_tokens[b])
+        hits.append(int(accept_len[b] > 0 and ws_ >= 1 + int(info[b][1])))
+    return hits
+
+
 def run_graft(args, ws, rank, local):
     import torch
     import hybrid_draft_tree_gb300 as g
@@ -272,11 +307,16 @@ def run_graft(args, ws, rank, local):
         valid = int((loop.tok >= 0).sum().item())
         acc = loop.accept_len.cpu().numpy()
         info = loop.info.cpu().numpy()
+        try:
+            hit = retrieval_hits(w.mode, loop.tok.cpu().numpy(), loop.par.cpu().numpy(), info, acc,
+                                 loop.out_tokens.cpu().numpy())
+        except Exception:                                # a statistic only: never costs the measurement
+            hit = None
         loop.pull_state()
         if ev is not None and profiling:
             for name, ms in eng.profile_read():
                 kernel_ms.setdefault(name, []).append(ms)
-        return n, valid, acc, info
+        return n, valid, acc, info, hit
 
     for _ in range(args.warmup):
         one_step()
@@ -289,14 +329,14 @@ def run_graft(args, ws, rank, local):
     launches = 0
     valid_rows = []
     accs = []
-    events_info = []
+    hits = []
     wall0 = time.perf_counter()
     for k in range(args.steps):
-        n, valid, acc, info = one_step(events[k])
+        n, valid, acc, info, hit = one_step(events[k])
         launches += n
         valid_rows.append(valid)
         accs.append(acc)
-        events_info.append(info[:, 0])
+        hits.append(hit)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if ws > 1:
@@ -340,6 +380,14 @@ def run_graft(args, ws, rank, local):
     # e2e through the C ABI from pinned host buffers
     e2e = run_e2e(args, w, eng, loop, stream, dev)
 
+    # the continuation matrix's populated rows (the pages quote its size as the
+    # bytes of the rows that hold successors) and the retrieval hit rate
+    try:
+        populated = int((eng.get_matrix(stream=stream)[:, 0] >= 0).sum())
+    except Exception:
+        populated = None
+    hit_rate = None if any(h is None for h in hits) or not hits else float(np.mean(np.concatenate(hits)))
+
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
@@ -364,6 +412,12 @@ def run_graft(args, ws, rank, local):
         "incremental": incremental,
         "next_rows": next_rows,
         "stats": {"mean_accepted_tokens_per_step": round(mat, 4), "valid_rows_per_step": statistics.mean(valid_rows),
+                  "retrieval_hit_rate": None if hit_rate is None else round(hit_rate, 4),
+                  "retrieval_hit_note": "share of request-steps whose deepest accepted node is a retrieved one "
+                                        "(null in static mode: in-place replacements are not identifiable from the "
+                                        "outputs)",
+                  "matrix_populated_rows": populated,
+                  "matrix_populated_bytes": None if populated is None else populated * 32,
                   "wall_s": round(wall, 2)},
     }
     return out

@@ -77,3 +77,57 @@ def test_reference_arm_under_torchrun_world_size_2():
     assert out["value"] > 0 and out["cpu_baseline"]["kind"] == "oracle"
     assert out["cpu_baseline"]["value"] == out["value"] == out["e2e"]["value"]
     assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("wid,sigma", [(0, 0.75), (4, None)])
+def test_winner_slot_and_retrieval_hits(wid, sigma):
+    """The bench recovers each request's deepest accepted node from the
+    step's outputs alone; on oracle-verified trees of a closed loop it equals
+    the winner found by brute force from the rows' argmaxes (deepest accepted
+    node, lower slot on ties), and retrieved winners occur."""
+    import numpy as np
+
+    import oracle
+    import workloads as W
+    b_ = _bench()
+    kw = {} if sigma is None else {"draft_sigma": sigma}
+    w = W.WORKLOADS[wid].scaled(V=400, B=2, **kw)
+    h = W.Harness(w)
+    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
+    C = oracle.new_matrix(w.V)
+    root, prev, ctx = h.init_state()
+    hits_seen = 0
+    for step in range(25):
+        tok, par, aux = h.draft(step, root, prev)
+        trees = [oracle.assemble(P, root[b], tok[b], aux[b], C, None if par is None else par[b]) for b in range(w.B)]
+        tt = np.stack([t.tok for t in trees])
+        pp = np.stack([t.par for t in trees]).astype(np.int8)
+        lg = h.tree_logits(tt, pp, ctx, prev)
+        accs, outs = [], []
+        for b in range(w.B):
+            acc, out, topk = oracle.verify(trees[b], lg[b], w.dtype)
+            y = topk[:, 0]
+            best_d, best_i = 0, 0
+            for i in range(1, w.S):
+                if tt[b][i] < 0:
+                    continue
+                ok, d, j = True, 0, i
+                while j != 0:
+                    p = int(pp[b][j])
+                    ok &= bool(tt[b][j] == y[p])
+                    d += 1
+                    j = p
+                if ok and d > best_d:
+                    best_d, best_i = d, i
+            assert best_d == acc
+            assert b_.winner_slot(tt[b], pp[b], acc, out) == best_i, (step, b)
+            oracle.update(C, trees[b], topk)
+            accs.append(acc)
+            outs.append(out)
+        acc_a, out_a = np.array(accs, np.int32), np.stack(outs)
+        hits = b_.retrieval_hits(w.mode, tt, pp, np.stack([t.info for t in trees]), acc_a, out_a)
+        assert all(hv in (0, 1) for hv in hits)
+        hits_seen += sum(hits)
+        h.advance(root, prev, ctx, out_a, acc_a)
+    assert hits_seen > 0
+    assert b_.retrieval_hits(W.MODE_STATIC, tt, pp, np.zeros((2, 4), np.int32), acc_a, out_a) is None
