@@ -40,7 +40,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.check_call(["nvcc", "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"])
+    subprocess.check_call(["nvcc", "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart", "-ldl"])
     os.replace(tmp, LIB)
     if verbose:
         for _, log in results:

@@ -13,6 +13,8 @@
 #include <queue>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "graft_internal.cuh"
 
 struct graft_handle {
@@ -105,6 +107,15 @@ void build_template(int max_depth, int width, int len, std::vector<int32_t>& par
     }
   }
 }
+
+// A named NVTX range around one ABI call, for profilers that record NVTX
+// (ncu --nvtx); header-only NVTX 3, a few nanoseconds when none is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Bracket one kernel launch with profiling events when tracing is on.
 struct ProfScope {
@@ -280,6 +291,7 @@ int graft_destroy(graft_handle* h) {
 
 int graft_warmup(graft_handle* h, const int32_t* d_tokens, const void* d_logits, int64_t n_rows, int64_t row_stride,
                  void* stream) {
+  NvtxRange nvtx("graft_warmup");
   if (!h) return GRAFT_EINVAL;
   h->last_launches = 0;
   if (n_rows < 0 || n_rows >= 0x7FFFFFFF) return fail(h, GRAFT_EINVAL, "n_rows must be in [0, 2^31-1)");
@@ -372,12 +384,14 @@ extern "C" {
 int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
                    const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes, int32_t* d_tree_tok,
                    int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info, void* stream) {
+  NvtxRange nvtx("graft_assemble");
   return assemble_impl(h, batch, d_root_tok, d_draft_tok, d_draft_parent, d_draft_aux, draft_nodes, nullptr, nullptr,
                        d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, stream);
 }
 
 int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, const float* d_draft_prob,
                 int32_t draft_nodes, int32_t layer, int32_t* d_event, void* stream) {
+  NvtxRange nvtx("graft_check");
   if (!h) return GRAFT_EINVAL;
   h->last_launches = 0;
   const graft_config& c = h->cfg;
@@ -403,6 +417,7 @@ int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, c
 
 int graft_retrieve(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_event,
                    int32_t* d_retrieved, void* stream) {
+  NvtxRange nvtx("graft_retrieve");
   if (!h) return GRAFT_EINVAL;
   h->last_launches = 0;
   const graft_config& c = h->cfg;
@@ -427,6 +442,7 @@ int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_
                           const int32_t* d_event, const int32_t* d_retrieved, int32_t* d_tree_tok,
                           int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info,
                           void* stream) {
+  NvtxRange nvtx("graft_assemble_staged");
   if (!h) return GRAFT_EINVAL;
   if (h->cfg.mode != GRAFT_MODE_CHECKPOINT) return fail(h, GRAFT_EINVAL, "graft_assemble_staged needs checkpoint mode");
   if (batch > 0 && (!d_event || !d_retrieved)) return fail(h, GRAFT_EINVAL, "null pointer");
@@ -436,6 +452,7 @@ int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_
 
 int graft_confidence(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, const float* d_draft_prob,
                      int32_t draft_nodes, float* d_best, void* stream) {
+  NvtxRange nvtx("graft_confidence");
   if (!h) return GRAFT_EINVAL;
   h->last_launches = 0;
   const graft_config& c = h->cfg;
@@ -505,6 +522,7 @@ int graft_set_thresholds(graft_handle* h, const float* thr) {
 
 int graft_coverage(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
                    const int32_t* d_info, const void* d_logits, int64_t row_stride, float* d_gain, void* stream) {
+  NvtxRange nvtx("graft_coverage");
   if (!h) return GRAFT_EINVAL;
   h->last_launches = 0;
   const graft_config& c = h->cfg;
@@ -616,6 +634,7 @@ extern "C" {
 int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
                         const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
                         int64_t row_stride, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream) {
+  NvtxRange nvtx("graft_verify_update");
   return verify_impl(h, batch, d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_logits, row_stride, d_accept_len,
                      d_out_tokens, false, 1.f, nullptr, nullptr, stream);
 }
@@ -624,6 +643,7 @@ int graft_verify_update_sample(graft_handle* h, int32_t batch, const int32_t* d_
                                const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
                                int64_t row_stride, float temperature, const float* d_u_accept,
                                const float* d_u_resid, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream) {
+  NvtxRange nvtx("graft_verify_update_sample");
   if (!h) return GRAFT_EINVAL;
   if (!(temperature > 0.f) || !std::isfinite(temperature)) return fail(h, GRAFT_EINVAL, "temperature must be > 0");
   if (batch > 0 && (!d_u_accept || !d_u_resid)) return fail(h, GRAFT_EINVAL, "null pointer");
