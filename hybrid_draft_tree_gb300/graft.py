@@ -346,7 +346,8 @@ class Graft:
 
     def set_matrix(self, m: np.ndarray, stream=None):
         m = np.ascontiguousarray(m, np.int32)
-        assert m.shape == (self.cfg.vocab, K)
+        if m.shape != (self.cfg.vocab, K):
+            raise GraftError(GRAFT_EINVAL, f"set_matrix: shape {m.shape}, expected ({self.cfg.vocab}, {K})")
         self._check(self.L.graft_set_matrix(self.h, m.ctypes.data_as(vp), _stream(stream)))
 
     def matrix_device_ptr(self) -> int:

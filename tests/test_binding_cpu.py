@@ -222,3 +222,13 @@ def test_empty_draft_is_passed_with_width_zero(as_device):
                  b["tpos"], b["tmask"], b["info"], stream=0)
     (name, args), = eng.L.calls
     assert _vals(args)[6] == 0
+
+
+def test_set_matrix_checks_its_shape():
+    import numpy as np
+    eng = _handle(V=100)
+    with pytest.raises(g.GraftError, match="shape"):
+        eng.set_matrix(np.zeros((99, 8), np.int32), stream=0)
+    eng.set_matrix(np.zeros((100, 8), np.int64), stream=0)        # converted to int32 on the host
+    (name, args), = eng.L.calls
+    assert name == "graft_set_matrix"

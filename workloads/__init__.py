@@ -149,6 +149,11 @@ def _p(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _ok(rc, what):
+    if rc != 0:
+        raise RuntimeError(f"{what} failed with status {rc}")
+
+
 u64 = ctypes.c_uint64
 i64 = ctypes.c_int64
 
@@ -220,7 +225,8 @@ class Harness:
             n = host().syn_draft_tree(w.V, w.kind, u64(w.seed), _p(self.table), ctypes.c_float(w.draft_sigma),
                                       i64(step), b, int(root[b]), int(prev[b]), _p(br), len(br), TREE_NODES,
                                       _p(tok[b]), _p(par[b]), _p(prob[b]))
-            assert n == TREE_NODES, n
+            if n != TREE_NODES:
+                raise RuntimeError(f"syn_draft_tree returned {n} nodes, expected {TREE_NODES}")
         return tok, par, prob
 
     def tree_rowparams(self, tok, par, root_ctx, root_prev):
@@ -254,7 +260,7 @@ class Harness:
         active = np.empty(w.hist_active, np.int32)
         rc = host().syn_history(u64(w.seed), w.V, w.hist_len, w.hist_active, ctypes.c_double(1.1),
                                 ctypes.c_double(0.3), 16, 64, _p(hist), _p(active))
-        assert rc == 0
+        _ok(rc, "syn_history")
         return hist, active
 
     def warm_rowparams(self):
@@ -306,17 +312,17 @@ class DeviceSynth:
         rc = self.lib.synd_tree_rowparams(w.V, w.kind, w.hit_all, ctypes.c_uint32(w.hit_num), ctypes.c_float(w.bias),
                                           u64(w.seed), _dp(self.table), B, S, _dp(tok), _dp(par), _dp(root_ctx),
                                           _dp(root_prev), _dp(rk), _dp(pl), _dp(bi), ctypes.c_void_p(stream))
-        assert rc == 0, rc
+        _ok(rc, "synd_tree_rowparams")
         return rk, pl, bi
 
     def fill_rows(self, rk, pl, bi, out, stream):
         n = rk.numel()
         rc = self.lib.synd_fill_rows(_dp(rk), _dp(pl), _dp(bi), i64(n), self.w.V, self.w.dtype, _dp(out),
                                      i64(out.stride(-2)), ctypes.c_void_p(stream))
-        assert rc == 0, rc
+        _ok(rc, "synd_fill_rows")
 
     def advance(self, out_tokens, accept_len, root, prev, ctx, stream):
         B, S = out_tokens.shape
         rc = self.lib.synd_advance(B, S, _dp(out_tokens), _dp(accept_len), _dp(root), _dp(prev), _dp(ctx),
                                    ctypes.c_void_p(stream))
-        assert rc == 0, rc
+        _ok(rc, "synd_advance")
