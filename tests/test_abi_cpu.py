@@ -75,3 +75,35 @@ def test_init_without_gpu_fails_cleanly():
     import hybrid_draft_tree_gb300 as g
     with pytest.raises(g.GraftError):
         g.Graft(g.graft_default_config(100, 1, 0, g.GRAFT_BF16))
+
+
+def test_config_validation_before_any_device_call():
+    """graft_init checks the configuration before it touches a device: on a
+    machine without a GPU a bad config is GRAFT_EINVAL and a good one reaches
+    the device query (GRAFT_ECUDA)."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("has a GPU")
+    import hybrid_draft_tree_gb300 as g
+    from hybrid_draft_tree_gb300 import graft as gb
+    L = g.load()
+
+    def init(**kw):
+        mode = kw.pop("mode", g.GRAFT_MODE_CHECKPOINT)
+        cfg = g.graft_default_config(kw.pop("vocab", 1000), kw.pop("max_batch", 4), mode, kw.pop("dtype", g.GRAFT_BF16),
+                                     **kw)
+        h = ctypes.c_void_p()
+        return L.graft_init(ctypes.byref(cfg), ctypes.byref(h))
+
+    for mode in (g.GRAFT_MODE_CHECKPOINT, g.GRAFT_MODE_STATIC, g.GRAFT_MODE_TAIL):
+        for dtype in (g.GRAFT_F32, g.GRAFT_BF16):
+            assert init(mode=mode, dtype=dtype) == gb.GRAFT_ECUDA
+    assert init(ablation=2, fixed_draft=0, tpl_depth=16, tpl_width=64, scan_kernel=3) == gb.GRAFT_ECUDA
+    assert init(budget=63, max_batch=1000) == gb.GRAFT_ECUDA          # the largest budget and batch * slots
+    bad = [dict(vocab=0), dict(topk=4), dict(budget=0), dict(budget=64), dict(max_batch=0), dict(max_batch=1100),
+           dict(mode=3), dict(dtype=2), dict(ckpt_draft=(8, 24, 61)), dict(ckpt_depth=(0, -1, 5)),
+           dict(tpl_depth=0), dict(tpl_depth=17), dict(tpl_width=0), dict(tpl_width=65), dict(ablation=3),
+           dict(ablation=1, mode=g.GRAFT_MODE_STATIC), dict(ablation=2, fixed_draft=61), dict(max_draft_nodes=-1),
+           dict(max_draft_nodes=17, mode=g.GRAFT_MODE_TAIL), dict(scan_kernel=4)]
+    for kw in bad:
+        assert init(**dict(kw)) == gb.GRAFT_EINVAL, kw
