@@ -107,3 +107,26 @@ def test_config_validation_before_any_device_call():
            dict(max_draft_nodes=17, mode=g.GRAFT_MODE_TAIL), dict(scan_kernel=4)]
     for kw in bad:
         assert init(**dict(kw)) == gb.GRAFT_EINVAL, kw
+
+
+def test_noalloc_argument_checks_before_any_device_call():
+    """graft_verify_update_noalloc refuses bad sizes and null buffers before
+    it touches a device; a batch of 0 is a no-op.  No pointer is
+    dereferenced on these paths (the last call stops at the device setup)."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("has a GPU")
+    import hybrid_draft_tree_gb300 as g
+    from hybrid_draft_tree_gb300 import graft as gb
+    L = g.load()
+    some = ctypes.c_void_p(4096)            # never dereferenced: every call below returns before any access
+
+    def call(V=1000, dt=g.GRAFT_BF16, B=2, S=61, stride=1000, ptr=some):
+        return L.graft_verify_update_noalloc(V, dt, B, S, ptr, ptr, ptr, ptr, ptr, ctypes.c_int64(stride), ptr, ptr,
+                                             ptr, ptr, ctypes.c_void_p(0))
+
+    assert call(B=0) == gb.GRAFT_OK
+    for kw in (dict(V=0), dict(dt=2), dict(S=0), dict(S=65), dict(B=-1), dict(B=2048 // 61 + 1), dict(stride=999),
+               dict(ptr=ctypes.c_void_p(None))):
+        assert call(**kw) == gb.GRAFT_EINVAL, kw
+    assert call() not in (gb.GRAFT_OK, gb.GRAFT_EINVAL)     # valid arguments: stops at the missing device
