@@ -130,3 +130,35 @@ def test_noalloc_argument_checks_before_any_device_call():
                dict(ptr=ctypes.c_void_p(None))):
         assert call(**kw) == gb.GRAFT_EINVAL, kw
     assert call() not in (gb.GRAFT_OK, gb.GRAFT_EINVAL)     # valid arguments: stops at the missing device
+
+
+def test_product_code_never_loads_the_oracle():
+    """The library, its binding and the input generators neither import the
+    oracle nor name its library; the benchmark imports it only inside the
+    CPU-baseline function (its reference leg), and libgraft.so links nothing
+    of it."""
+    import ast
+    import subprocess
+    for sub in ("hybrid_draft_tree_gb300", "workloads", "include"):
+        for dirpath, _, files in os.walk(os.path.join(ROOT, sub)):
+            for f in files:
+                path = os.path.join(dirpath, f)
+                if f.endswith(".py"):
+                    tree = ast.parse(open(path).read())
+                    for node in ast.walk(tree):
+                        if isinstance(node, ast.Import):
+                            assert all(a.name.split(".")[0] != "oracle" for a in node.names), path
+                        if isinstance(node, ast.ImportFrom):
+                            assert (node.module or "").split(".")[0] != "oracle", path
+                if f.endswith((".py", ".cu", ".cuh", ".c", ".h")):
+                    assert "graft_oracle" not in open(path).read(), path
+    bench = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    importers = [fn.name for fn in ast.walk(bench) if isinstance(fn, ast.FunctionDef)
+                 for node in ast.walk(fn) if isinstance(node, ast.Import) and any(a.name == "oracle" for a in node.names)]
+    assert importers == ["oracle_sample"]
+    assert not any(isinstance(node, ast.Import) and any(a.name == "oracle" for a in node.names) for node in bench.body)
+    import hybrid_draft_tree_gb300 as g
+    from hybrid_draft_tree_gb300 import _build
+    _build.build()
+    deps = subprocess.run(["ldd", g.library_path()], capture_output=True, text=True).stdout
+    assert "oracle" not in deps
