@@ -162,3 +162,14 @@ def test_product_code_never_loads_the_oracle():
     _build.build()
     deps = subprocess.run(["ldd", g.library_path()], capture_output=True, text=True).stdout
     assert "oracle" not in deps
+
+
+def test_oracle_shares_no_code_with_the_library():
+    """The oracle neither imports the package nor includes the library's
+    headers or sources (the two share only the seeded input generators)."""
+    odir = os.path.join(ROOT, "oracle")
+    for f in os.listdir(odir):
+        if f.endswith((".py", ".c", ".h")):
+            src = open(os.path.join(odir, f)).read()
+            for needle in ("hybrid_draft_tree_gb300", "graft.h", "graft_internal", "csrc", "libgraft.so"):
+                assert needle not in src, (f, needle)
