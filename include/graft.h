@@ -173,6 +173,12 @@ int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, c
 int graft_retrieve(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_event,
                    int32_t* d_retrieved, void* stream);
 
+int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                          const int16_t* d_draft_parent, const float* d_draft_prob, int32_t draft_nodes,
+                          const int32_t* d_event, const int32_t* d_retrieved, int32_t* d_tree_tok,
+                          int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info,
+                          void* stream);
+
 /* The retrieval template (article §二, second gear: rank paths below the
  * anchor; the rank-r successor of a node has max(1, width >> r) children of
  * its own, the anchor min(8, width); depth <= `depth`; entries in increasing
@@ -188,11 +194,6 @@ int graft_retrieve(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
  * [0, 65536] or a null array. */
 int graft_template(int32_t depth, int32_t width, int32_t len, int32_t* parent_out, int32_t* rank_out,
                    int32_t* depth_out);
-int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
-                          const int16_t* d_draft_parent, const float* d_draft_prob, int32_t draft_nodes,
-                          const int32_t* d_event, const int32_t* d_retrieved, int32_t* d_tree_tok,
-                          int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info,
-                          void* stream);
 
 /* Threshold calibration (article §二: the checkpoint thresholds are set from
  * the distribution of path confidences seen during warm-up).
@@ -312,7 +313,9 @@ int graft_sync(graft_handle* h, void* stream, uint32_t* out_flags);
 /* Message of the last failed call on this handle ("" if none). */
 const char* graft_last_error(const graft_handle* h);
 
-/* Kernel timing (tracing).  When enabled, every kernel this handle launches
+/* Kernel timing (tracing).  Every call that queues work is also wrapped in an
+ * NVTX range named after it (graft_verify_update, ...), visible to profilers
+ * that record NVTX.  When enabled, every kernel this handle launches
  * is bracketed by two CUDA events recorded on the call's stream (a few
  * hundred nanoseconds each).  graft_profile_read synchronises the device and
  * writes, for the kernels of the most recent calls since the last read (at
