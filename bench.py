@@ -247,6 +247,19 @@ def retrieval_hits(mode, tok, par, info, accept_len, out_tokens):
     return hits
 
 
+def hit_rate_of(hits):
+    """Mean of the per-step retrieval hits (lists of 0/1 per request); None
+    when any step has none (static mode, or a statistic that failed)."""
+    if not hits or any(h is None for h in hits):
+        return None
+    return float(np.mean(np.concatenate([np.asarray(h, np.float64) for h in hits])))
+
+
+def populated_rows(matrix) -> int:
+    """Rows of the continuation matrix that hold at least one successor."""
+    return int((np.asarray(matrix)[:, 0] >= 0).sum())
+
+
 def run_graft(args, ws, rank, local):
     import torch
     import hybrid_draft_tree_gb300 as g
@@ -383,10 +396,13 @@ def run_graft(args, ws, rank, local):
     # the continuation matrix's populated rows (the pages quote its size as the
     # bytes of the rows that hold successors) and the retrieval hit rate
     try:
-        populated = int((eng.get_matrix(stream=stream)[:, 0] >= 0).sum())
+        populated = populated_rows(eng.get_matrix(stream=stream))
     except Exception:
         populated = None
-    hit_rate = None if any(h is None for h in hits) or not hits else float(np.mean(np.concatenate(hits)))
+    try:
+        hit_rate = hit_rate_of(hits)
+    except Exception:
+        hit_rate = None
 
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,

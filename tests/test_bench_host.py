@@ -131,3 +131,13 @@ def test_winner_slot_and_retrieval_hits(wid, sigma):
         h.advance(root, prev, ctx, out_a, acc_a)
     assert hits_seen > 0
     assert b_.retrieval_hits(W.MODE_STATIC, tt, pp, np.zeros((2, 4), np.int32), acc_a, out_a) is None
+
+
+def test_hit_rate_and_populated_rows():
+    import numpy as np
+    b_ = _bench()
+    assert b_.hit_rate_of([[0, 1], [1, 1]]) == 0.75
+    assert b_.hit_rate_of([[0, 1], None]) is None and b_.hit_rate_of([]) is None
+    C = np.full((5, 8), -1, np.int32)
+    C[[1, 3], :] = 7
+    assert b_.populated_rows(C) == 2
