@@ -232,3 +232,21 @@ def test_set_matrix_checks_its_shape():
     eng.set_matrix(np.zeros((100, 8), np.int64), stream=0)        # converted to int32 on the host
     (name, args), = eng.L.calls
     assert name == "graft_set_matrix"
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libgraft.so (and without building it) the binding raises; it
+    has no other path to run the step on."""
+    from hybrid_draft_tree_gb300 import _build
+    monkeypatch.setattr(gb, "_lib", None)
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "libgraft.so"))
+    with pytest.raises(ImportError):
+        gb.load(build_if_missing=False)
+
+    def no_nvcc(*a, **k):
+        raise RuntimeError("nvcc failed")
+    monkeypatch.setattr(_build, "build", no_nvcc)
+    with pytest.raises(RuntimeError):
+        gb.load()
+    with pytest.raises(RuntimeError):
+        g.Graft(g.graft.graft_config())
