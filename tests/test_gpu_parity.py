@@ -254,55 +254,59 @@ def _incremental_case(w, cfg, steps):
     g.close()
 
 
-def _np_layer_best(par, prob):
-    conf = np.zeros(len(par), np.float32)
-    depth = np.zeros(len(par), np.int32)
-    for i in range(len(par)):                       # fp32 product, root first
-        conf[i] = prob[i] if par[i] < 0 else np.float32(conf[par[i]] * prob[i])
-        depth[i] = 0 if par[i] < 0 else depth[par[i]] + 1
+def _oracle_layer_best(par, prob):
+    """Best fp32 path confidence of checkpoint layers 0, 1, 5 from the
+    oracle's path confidences and depths (-1 for an empty layer)."""
+    conf, depth = oracle.path_conf(par, prob)
     return np.array([conf[depth == d].max() if (depth == d).any() else -1.0 for d in (0, 1, 5)], np.float32)
 
 
 def test_confidence_and_calibrated_thresholds():
     """graft_confidence returns each checkpoint layer's best fp32 path
-    confidence; thresholds calibrated from those over warm-up steps then
-    drive the checkpoints exactly as in the oracle with the same thresholds."""
+    confidence, equal to the maximum of the oracle's path confidences over
+    that layer; thresholds calibrated from those over warm-up steps then
+    drive the checkpoints exactly as in the oracle with the same thresholds.
+    The oracle runs the whole closed loop on its own matrix."""
     from workloads.device_loop import DeviceLoop
     w = W.WORKLOADS[0].scaled(V=3000, B=4, draft_sigma=0.75)
     g_ = G()
     eng = engine_for(w)
     loop = DeviceLoop(w, eng)
     best = torch.empty((w.B, 3), dtype=torch.float32, device="cuda")
-    samples = []
-    for step in range(6):
+    C = oracle.new_matrix(w.V)
+
+    def closed_step(P, step):
         tok, par, aux = loop.draft()
         eng.confidence(w.B, loop.d_par, loop.d_aux, best)
         got = best.cpu().numpy()
         for b in range(w.B):
-            assert np.array_equal(got[b], _np_layer_best(par[b], aux[b])), (step, b)
-        samples.append(got)
-        loop.assemble(); loop.make_logits(); loop.verify_update(); loop.advance()
-    thr = g_.calibrate_thresholds(np.concatenate(samples), 0.4)
-    eng.set_thresholds(thr)
-    P = oracle.make_params(w.V, ckpt_thr=tuple(float(x) for x in thr))
-    C = eng.get_matrix()
-    fired = 0
-    for step in range(8):
-        tok, par, aux = loop.draft()
+            assert np.array_equal(got[b], _oracle_layer_best(par[b], aux[b])), (step, b)
         loop.assemble()
         trees = [oracle.assemble(P, loop.root_h[b], tok[b], aux[b], C, par[b]) for b in range(w.B)]
         assert_trees_equal(loop, trees, step)
-        fired += sum(int(t.info[0] >= 0) for t in trees)
         loop.make_logits()
         tt = np.stack([t.tok for t in trees])
         pp = np.stack([t.par for t in trees]).astype(np.int8)
         lg = loop.h.tree_logits(tt, pp, loop.ctx_h, loop.prev_h)
         loop.verify_update()
+        acc_g = loop.accept_len.cpu().numpy()
+        out_g = loop.out_tokens.cpu().numpy()
         for b in range(w.B):
             acc, out, topk = oracle.verify(trees[b], lg[b], w.dtype)
             oracle.update(C, trees[b], topk)
+            assert acc_g[b] == acc and np.array_equal(out_g[b], out), (step, b)
+        assert np.array_equal(eng.get_matrix(), C), step
         loop.advance()
+        return got, sum(int(t.info[0] >= 0) for t in trees)
+
+    P0 = oracle.make_params(w.V)
+    samples = [closed_step(P0, step)[0] for step in range(6)]
+    thr = g_.calibrate_thresholds(np.concatenate(samples), 0.4)
+    eng.set_thresholds(thr)
+    P = oracle.make_params(w.V, ckpt_thr=tuple(float(x) for x in thr))
+    fired = sum(closed_step(P, 6 + step)[1] for step in range(8))
     assert fired > 0
+    assert eng.sync() == 0
     with pytest.raises(g_.GraftError):
         eng.set_thresholds([0.5, 1.5, 0.1])
     eng.close()
@@ -418,62 +422,6 @@ def test_lockstep_warmup_small(wid):
     if base.warm == "history":
         kw.update(hist_len=3000, hist_active=300)
     lockstep(base.scaled(**kw), 15, warm=True)
-
-
-@pytest.mark.slow
-@pytest.mark.parametrize("wid,steps", [(0, 100), (1, 6), (2, 3), (4, 2)])
-def test_lockstep_full_size(wid, steps):
-    """The five workloads at full size, in the launch configuration the benchmark times."""
-    w = W.WORKLOADS[wid]
-    lockstep(w, steps, warm=(w.warm == "rollouts"), check_rows=4)
-
-
-@pytest.mark.slow
-def test_warm_start_32k_full_size_sampled():
-    """32768-row warm start at V=151936 (9.96 GB of bf16 logits on the
-    device): sampled rows of the matrix against the oracle's top-8 of each
-    token's last occurrence, untouched rows stay empty, then decode steps in
-    lockstep."""
-    from workloads.device_loop import DeviceLoop
-    w = W.WORKLOADS[3]
-    g = engine_for(w)
-    loop = DeviceLoop(w, g)
-    toks_d, logits_d, (toks, rk, pl, bi) = loop.warm_inputs_device()
-    g.warmup(toks_d, logits_d)
-    del logits_d
-    torch.cuda.empty_cache()
-    Cg = g.get_matrix()
-    last = {}
-    for n, t in enumerate(toks.tolist()):
-        last[t] = n
-    present = np.zeros(w.V, bool)
-    present[list(last)] = True
-    assert (Cg[~present] == -1).all()
-    assert (Cg[present] >= 0).all()
-    rng = np.random.default_rng(0)
-    sample = rng.choice(sorted(last), 40, replace=False)
-    for t in sample:
-        n = last[t]
-        row = W.fill_rows(rk[n:n + 1], pl[n:n + 1], bi[n:n + 1], w.V, w.dtype)[0]
-        assert np.array_equal(Cg[t], oracle.topk8_row(row, w.dtype)), t
-    # continue decoding in lockstep from the warmed matrix
-    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
-    C = Cg.copy()
-    for step in range(3):
-        tok, par, aux = loop.draft()
-        loop.assemble()
-        trees = [oracle.assemble(P, loop.root_h[0], tok[0], aux[0], C, par[0])]
-        assert_trees_equal(loop, trees, step)
-        loop.make_logits()
-        lg = loop.h.tree_logits(trees[0].tok[None], trees[0].par[None].astype(np.int8), loop.ctx_h, loop.prev_h)
-        loop.verify_update()
-        acc, out, topk = oracle.verify(trees[0], lg[0], w.dtype)
-        oracle.update(C, trees[0], topk)
-        assert loop.accept_len.cpu().numpy()[0] == acc
-        assert np.array_equal(loop.out_tokens.cpu().numpy()[0], out)
-        assert np.array_equal(g.get_matrix(), C)
-        loop.advance()
-    assert g.sync() == 0
 
 
 # ------------------------------------------------------------------------------ assemble edge cases

@@ -158,15 +158,41 @@ u64 = ctypes.c_uint64
 i64 = ctypes.c_int64
 
 
-def fill_rows(rowkey, planted, bias, V, dtype, out=None):
-    """Host row filler: returns [n, V] float32 or uint16 (bf16 bits)."""
+def host_threads() -> int:
+    """Threads for the host row filler: the cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def fill_rows(rowkey, planted, bias, V, dtype, out=None, threads=1):
+    """Host row filler: returns [n, V] float32 or uint16 (bf16 bits).  With
+    threads > 1 the rows are split into contiguous blocks filled in parallel
+    (the C filler releases the GIL; every row is a pure function of its own
+    key, so the result is identical)."""
     rowkey = np.ascontiguousarray(rowkey, np.uint64)
     planted = np.ascontiguousarray(planted, np.int32)
     bias = np.ascontiguousarray(bias, np.float32)
     n = len(rowkey)
     if out is None:
         out = np.empty((n, V), np.float32 if dtype == F32 else np.uint16)
-    host().syn_fill_rows(_p(rowkey), _p(planted), _p(bias), i64(n), V, dtype, _p(out), i64(out.shape[-1]))
+    stride = out.shape[-1]
+    lib = host()
+
+    def fill(r0, r1):
+        if r1 > r0:
+            lib.syn_fill_rows(_p(rowkey[r0:]), _p(planted[r0:]), _p(bias[r0:]), i64(r1 - r0), V, dtype,
+                              _p(out.reshape(n, stride)[r0:]), i64(stride))
+
+    threads = max(1, min(int(threads), n))
+    if threads == 1:
+        fill(0, n)
+        return out
+    import concurrent.futures as cf
+    cuts = [n * k // threads for k in range(threads + 1)]
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda k: fill(cuts[k], cuts[k + 1]), range(threads)))
     return out
 
 
@@ -241,10 +267,11 @@ class Harness:
                                   _p(np.ascontiguousarray(root_prev, np.int32)), _p(rowkey), _p(planted), _p(bias))
         return rowkey, planted, bias
 
-    def tree_logits(self, tok, par, root_ctx, root_prev):
+    def tree_logits(self, tok, par, root_ctx, root_prev, threads=1):
         rk, pl, bi = self.tree_rowparams(tok, par, root_ctx, root_prev)
         B, S = rk.shape
-        return fill_rows(rk.reshape(-1), pl.reshape(-1), bi.reshape(-1), self.w.V, self.w.dtype).reshape(B, S, -1)
+        return fill_rows(rk.reshape(-1), pl.reshape(-1), bi.reshape(-1), self.w.V, self.w.dtype,
+                         threads=threads).reshape(B, S, -1)
 
     def prefix_rowparams(self, b, ctx, prev, t):
         rk = np.zeros(1, np.uint64)
