@@ -15,7 +15,11 @@
 // Host code may not use the array's name as a device address (in host code it
 // names a host-side stand-in), so the device address is obtained once per
 // device with cudaGetSymbolAddress, with that device current, on the first
-// call made on it.
+// call made on it.  The address belongs to the device's context: it is kept
+// with that context's id and looked up again when the current context is a
+// different one (after cudaDeviceReset, or once the primary context was
+// released and created anew).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -36,25 +40,70 @@ __device__ __align__(256) unsigned char g_scratch[kBytes];
 constexpr int kMaxDevices = 64;
 struct DeviceSetup {
   bool ready = false;
+  unsigned long long ctx_id = 0;     // id of the context the address below belongs to
   unsigned char* scratch = nullptr;  // device address of g_scratch on this device
   int num_sms = 0;
 };
 DeviceSetup g_setup[kMaxDevices];
 std::mutex g_setup_mutex;
 
-int setup_current_device(DeviceSetup** out) {
+// Driver entry points reached through the runtime (the library does not link
+// the driver library itself).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Id of the calling thread's current context (unique for the process's
+// lifetime: a context made after a reset gets a new id); 0 when the thread
+// has no current context yet.  Call with the mutex held.
+int current_context_id(unsigned long long* id) {
+  *id = 0;
+  if (!g_ctx_get_current || !g_ctx_get_id) {
+    cudaDriverEntryPointQueryResult q1, q2;
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || !f1)
+      return GRAFT_ECUDA;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess || !f2)
+      return GRAFT_ECUDA;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return GRAFT_ECUDA;
+  if (ctx == nullptr) return GRAFT_OK;
+  if (g_ctx_get_id(ctx, id) != CUDA_SUCCESS) return GRAFT_ECUDA;
+  return GRAFT_OK;
+}
+
+// The scratch address and SM count of the current device, looked up on the
+// first call made on it, and again whenever the current context is not the
+// one the address was taken in.  `stream` must belong to the current device.
+int setup_current_device(void* stream, DeviceSetup** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GRAFT_ECUDA;
+  int sdev = -1;
+  if (cudaStreamGetDevice((cudaStream_t)stream, &sdev) != cudaSuccess) return GRAFT_EINVAL;
+  if (sdev != dev) return GRAFT_EINVAL;  // the stream (and so the buffers) of another device
   std::lock_guard<std::mutex> lock(g_setup_mutex);
+  unsigned long long ctx_id = 0;
+  if (current_context_id(&ctx_id) != GRAFT_OK) return GRAFT_ECUDA;
   DeviceSetup& d = g_setup[dev];
-  if (!d.ready) {
+  if (!d.ready || ctx_id == 0 || d.ctx_id != ctx_id) {
+    d.ready = false;
     void* ptr = nullptr;
+    // (makes the device's primary context current on this thread if it was not)
     if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr) return GRAFT_ECUDA;
+    if (current_context_id(&ctx_id) != GRAFT_OK || ctx_id == 0) return GRAFT_ECUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
       return GRAFT_ECUDA;
     d.scratch = static_cast<unsigned char*>(ptr);
     d.num_sms = sms;
+    d.ctx_id = ctx_id;
     d.ready = true;
   }
   *out = &d;
@@ -79,7 +128,7 @@ extern "C" int graft_verify_update_noalloc(int32_t vocab, int32_t logits_dtype, 
       !d_out_tokens || !d_err_flags)
     return GRAFT_EINVAL;
   DeviceSetup* dev = nullptr;
-  const int rc = setup_current_device(&dev);
+  const int rc = setup_current_device(stream, &dev);
   if (rc != GRAFT_OK) return rc;
   const int grid = dev->num_sms * graft::verify_ctas_per_sm();
   if (rows > graft::verify_max_rows(grid)) return GRAFT_EINVAL;

@@ -286,9 +286,13 @@ int graft_verify_update_sample(graft_handle* h, int32_t batch, const int32_t* d_
  * so calls that overlap on the GPU (for example on two streams at once) race.
  * Nothing is carried from one call to the next.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress, no allocation);
- * make that first call before any stream capture.  Asynchronous; returns
- * GRAFT_EINVAL for bad arguments or sizes beyond the limit (nothing queued),
- * GRAFT_ECUDA if a CUDA call fails. */
+ * make that first call before any stream capture.  The address is tied to
+ * the device's context: the first call after cudaDeviceReset (or after the
+ * primary context was released and made again) looks it up anew, so make
+ * that call outside a capture too.  The current device must be the device of
+ * `stream` and of every d_* buffer.  Asynchronous; returns GRAFT_EINVAL for
+ * bad arguments, sizes beyond the limit or a stream of another device
+ * (nothing queued), GRAFT_ECUDA if a CUDA call fails. */
 #define GRAFT_NOALLOC_MAX_ROWS 2048
 #define GRAFT_NOALLOC_BYTES (GRAFT_NOALLOC_MAX_ROWS * (16 * 8 * 8 + 4 + 8 * 4))
 int graft_verify_update_noalloc(int32_t vocab, int32_t logits_dtype, int32_t batch, int32_t slots,
