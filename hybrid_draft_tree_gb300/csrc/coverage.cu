@@ -8,8 +8,8 @@
 // a boundary candidate; its token is new unless a kept draft child of the same
 // parent carries it.  The gain is the sum, over the new tokens, of their
 // softmax probability in the parent's logits row.  A diagnostic off the hot
-// path: one CTA per request streams each boundary parent's row once
-// (row_softmax.cuh).
+// path: one thread-block cluster of CL CTAs per request streams each boundary
+// parent's row once, split over the cluster's SMs (row_softmax.cuh).
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -21,17 +21,19 @@ namespace {
 using namespace scan;
 using namespace softmax;
 
-constexpr int CT = 1024;  // threads per CTA: one row per CTA, so memory parallelism comes from the threads
+constexpr int CT = 256;  // threads per CTA (CL CTAs per request)
 
 constexpr float LOG2E = 1.4426950408889634f;
 
 template <int DT>
-__global__ __launch_bounds__(CT) void k_coverage(VerifyArgs a, const int32_t* info, float* gain) {
+__global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t* info, float* gain) {
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
-  __shared__ RowStats<CT> st;
+  __shared__ ClusterRow<CT> st;
   __shared__ int32_t s_tok[MAX_S], s_par[MAX_S];
   __shared__ float s_x[MAX_S];  // a boundary candidate's logit in its parent's row, by slot
-  const int b = blockIdx.x, t = threadIdx.x, S = a.S;
+  const cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / CL, t = threadIdx.x, S = a.S;
   const int n_draft = info[(int64_t)b * 4 + 1], n_retr = info[(int64_t)b * 4 + 2];
   const int r0 = min(max(1 + n_draft, 1), S), r1 = min(r0 + max(n_retr, 0), S);
   if (t < S) {
@@ -39,18 +41,19 @@ __global__ __launch_bounds__(CT) void k_coverage(VerifyArgs a, const int32_t* in
     s_par[t] = a.tree_parent[(int64_t)b * S + t];
   }
   __syncthreads();
-  float total = 0.f;  // thread 0's running sum
+  float total = 0.f;  // thread 0's running sum (used in CTA 0)
+  int pass = 0;
   // boundary parents in slot order (a kept slot with a retrieved child)
   for (int p = 0; p < r0 && p < S; ++p) {
     bool has = false;
     for (int j = r0; j < r1; ++j) has |= s_par[j] == p;
-    if (!has || s_tok[p] < 0 || s_tok[p] >= a.g.V) continue;  // (uniform: shared values)
+    if (!has || s_tok[p] < 0 || s_tok[p] >= a.g.V) continue;  // (uniform: the same values in every CTA)
     const char* rowp = reinterpret_cast<const char*>(a.logits) + ((size_t)b * S + p) * (size_t)a.g.stride * ES;
     if (t >= r0 && t < r1 && s_par[t] == p && s_tok[t] >= 0 && s_tok[t] < a.g.V)
       s_x[t] = load_scalar<DT>(rowp, s_tok[t]);  // fetched beside the row pass
-    row_stats<DT, CT>(rowp, a.g.V, a.g.vec != 0, LOG2E, st);
+    cluster_row_stats<DT, CT>(cluster, rowp, a.g.V, a.g.vec != 0, LOG2E, st, pass++);
     const float M = st.M, Z = st.W;
-    if (t == 0 && Z > 0.f) {
+    if (t == 0 && rank == 0 && Z > 0.f) {
       for (int j = r0; j < r1; ++j) {
         const int32_t tk = s_tok[j];
         if (s_par[j] != p || tk < 0 || tk >= a.g.V) continue;
@@ -59,14 +62,27 @@ __global__ __launch_bounds__(CT) void k_coverage(VerifyArgs a, const int32_t* in
         if (!dup) total += exp2f((s_x[j] - M) * LOG2E) / Z;
       }
     }
+    __syncthreads();  // s_x is read before the next parent's loads
   }
-  if (t == 0) gain[b] = total;
+  if (t == 0 && rank == 0) gain[b] = total;
+  if (pass > 0) cluster.sync();  // the last pass's pairs are read before any CTA of the cluster exits
 }
 
 template <int DT>
 cudaError_t coverage_impl(const VerifyArgs& a, const int32_t* info, float* gain, cudaStream_t s) {
-  k_coverage<DT><<<a.batch, CT, 0, s>>>(a, info, gain);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.batch * CL);
+  cfg.blockDim = dim3(CT);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_coverage<DT>, a, info, gain);
 }
 
 }  // namespace

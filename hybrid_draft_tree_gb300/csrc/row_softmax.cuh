@@ -1,13 +1,22 @@
-// Block-wide softmax statistics of one logits row, for the kernels that need
-// target probabilities (stochastic verification, the coverage diagnostic).
+// Softmax statistics of one logits row, computed by a thread-block cluster,
+// for the kernels that need target probabilities (stochastic verification,
+// the coverage diagnostic).
 //
-// Thread t of the CTA owns the contiguous chunk [t*ch, min((t+1)*ch, V)) of
-// the row (ch a multiple of the vector width when the row is 16-byte aligned,
-// so the chunk is read with 16-byte loads) and keeps an online (max, sum of
-// exp2((x - max) * k2)) over it; k2 = log2(e) / temperature.  The chunks'
-// pairs stay in shared memory, so an inverse-CDF draw over the row can locate
-// its chunk without another pass.  All threads of the CTA must call.
+// One request's row is read by a cluster of CL CTAs (CL SMs): CTA r of the
+// cluster owns a contiguous range of the row, and thread t of the CTA owns a
+// contiguous chunk of that range (lengths multiples of the vector width when
+// the row is 16-byte aligned, so chunks are read with 16-byte loads).  Each
+// thread keeps an online (max, sum of exp2((x - max) * k2)) over its chunk,
+// k2 = log2(e) / temperature; warp 0 folds them into the CTA's pair, and the
+// CTAs exchange their pairs through distributed shared memory, each folding
+// the CL pairs in rank order, so every CTA of the cluster holds the same row
+// maximum and sum.  The chunks' pairs stay in shared memory, so an inverse-CDF
+// draw over the row can locate its CTA and its chunk without another pass;
+// given a staging buffer, the CTA also keeps its range of the row in shared
+// memory, so the draw reads no global memory at all.
+// All threads of every CTA of the cluster must call.
 #pragma once
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -16,13 +25,18 @@
 namespace graft {
 namespace softmax {
 using namespace scan;
+namespace cg = cooperative_groups;
+
+constexpr int CL = 8;  // CTAs per row: one portable thread-block cluster
 
 template <int NT>
-struct RowStats {
-  float m[NT];  // chunk maxima
-  float s[NT];  // chunk sums of exp2((x - m[t]) * k2)
-  float M, W;   // row maximum and sum of exp2((x - M) * k2)
-  int ch;       // elements per chunk
+struct ClusterRow {
+  float m[NT];        // chunk maxima
+  float s[NT];        // chunk sums of exp2((x - m[t]) * k2)
+  float cm[2], cs[2]; // this CTA's (max, sum) of the current pass, by pass parity (read by the other CTAs)
+  float ct;           // this CTA's weight in a final draw (read by the other CTAs)
+  float M, W;         // row maximum and sum of exp2((x - M) * k2), the same in every CTA of the cluster
+  int lo, hi, ch;     // this CTA's element range and its chunk length
 };
 
 // (m, s) <- online update with element x.
@@ -35,53 +49,121 @@ __device__ __forceinline__ void online_add(float& m, float& s, float x, float k2
   }
 }
 
-// Chunk size: V / NT rounded up to a multiple of `epl` (the elements of one
-// 16-byte load on the vector path, else 1).
-template <int NT>
-__device__ __forceinline__ int chunk_size(int V, int epl) {
-  int ch = (V + NT - 1) / NT;
-  return (ch + epl - 1) / epl * epl;
+// Element i of a staged range (the row's own type), and its store.
+template <int DT>
+__device__ __forceinline__ float stage_elem(const char* stage, int i) {
+  if (DT == GRAFT_BF16) return __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(stage)[i] << 16);
+  return reinterpret_cast<const float*>(stage)[i];
+}
+template <int DT>
+__device__ __forceinline__ void store_elem(char* stage, int i, float x) {
+  if (DT == GRAFT_BF16) reinterpret_cast<unsigned short*>(stage)[i] = (unsigned short)(__float_as_uint(x) >> 16);
+  else reinterpret_cast<float*>(stage)[i] = x;
 }
 
+// Element range [lo, hi) of cluster rank `rank` in a V-element row: ranges of
+// ceil(V / CL) rounded up to a multiple of `epl`.
+__device__ __forceinline__ void cta_range(int V, int epl, int rank, int& lo, int& hi) {
+  int per = (V + CL - 1) / CL;
+  per = (per + epl - 1) / epl * epl;
+  lo = min(rank * per, V);
+  hi = min(lo + per, V);
+}
+
+// Bytes of shared memory that hold one CTA's range of a V-element row.
+__device__ __host__ __forceinline__ int stage_bytes(int V, int esize) {
+  const int epl = 16 / esize;
+  int per = (V + CL - 1) / CL;
+  per = (per + epl - 1) / epl * epl;
+  return per * esize;
+}
+
+// One pass over row `rowp` (pass index `pass`: consecutive passes alternate
+// the exchange slots, so a CTA never overwrites a pair another CTA may still
+// be reading).  On return st.M, st.W hold the row's statistics in every CTA;
+// st.m / st.s / st.lo / st.hi / st.ch describe this CTA's chunks.  With
+// `stage` (stage_bytes(V, esize) bytes of shared memory, 16-byte aligned),
+// element v of this CTA's range is left at stage[v - lo].
 template <int DT, int NT>
-__device__ void row_stats(const char* rowp, int V, bool vec, float k2, RowStats<NT>& st) {
+__device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* rowp, int V, bool vec, float k2,
+                                  ClusterRow<NT>& st, int pass, char* stage = nullptr) {
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   const int t = threadIdx.x;
   constexpr int EPL = Vec16<DT>::EPL;
-  const int ch = chunk_size<NT>(V, vec ? EPL : 1);
-  const int v0 = min(t * ch, V), v1 = min(v0 + ch, V);
+  constexpr int UNR = 8;  // 16-byte loads in flight per thread
+  const int epl = vec ? EPL : 1;
+  int lo, hi;
+  cta_range(V, epl, (int)cluster.block_rank(), lo, hi);
+  int ch = (hi - lo + NT - 1) / NT;
+  ch = (ch + epl - 1) / epl * epl;
+  const int v0 = min(lo + t * ch, hi), v1 = min(v0 + ch, hi);
   float m = -INFINITY, s = 0.f;
   if (vec) {
-    const uint4* p = reinterpret_cast<const uint4*>(rowp);
-    const int full = v0 + (v1 - v0) / EPL * EPL;  // whole vectors of the chunk
-#pragma unroll 4
-    for (int v = v0; v < full; v += EPL) {
-      Vec16<DT> x;
-      x.r = p[v / EPL];
-      const float vm = x.vmax();
-      if (vm > m) { s *= exp2f((m - vm) * k2); m = vm; }  // one rescale per vector
-      if (m != -INFINITY) {
+    const uint4* p = reinterpret_cast<const uint4*>(rowp) + v0 / EPL;
+    const int nvec = (v1 - v0) / EPL;  // whole vectors of the chunk (only the row's last chunk has a rest)
+    uint4* sp = stage ? reinterpret_cast<uint4*>(stage + (size_t)(v0 - lo) * ES) : nullptr;
+    for (int base = 0; base < nvec; base += UNR) {
+      Vec16<DT> x[UNR];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) s += exp2f((x.elem(e) - m) * k2);
+      for (int u = 0; u < UNR; ++u)
+        if (base + u < nvec) x[u].r = __ldcs(p + base + u);
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        if (base + u >= nvec) break;
+        if (sp) sp[base + u] = x[u].r;
+        const float vm = x[u].vmax();
+        if (vm > m) { s *= exp2f((m - vm) * k2); m = vm; }  // one rescale per vector
+        if (m != -INFINITY) {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) s += exp2f((x[u].elem(e) - m) * k2);
+        }
       }
     }
-    for (int v = full; v < v1; ++v) online_add(m, s, load_scalar<DT>(rowp, v), k2);
+    for (int v = v0 + nvec * EPL; v < v1; ++v) {
+      const float x = load_scalar<DT>(rowp, v);
+      if (stage) store_elem<DT>(stage, v - lo, x);
+      online_add(m, s, x, k2);
+    }
   } else {
-    for (int v = v0; v < v1; ++v) online_add(m, s, load_scalar<DT>(rowp, v), k2);
+    for (int v = v0; v < v1; ++v) {
+      const float x = load_scalar<DT>(rowp, v);
+      if (stage) store_elem<DT>(stage, v - lo, x);
+      online_add(m, s, x, k2);
+    }
   }
   st.m[t] = m;
   st.s[t] = s;
+  if (t == 0) { st.lo = lo; st.hi = hi; st.ch = ch; }
   __syncthreads();
+  const int slot = pass & 1;
   if (t < 32) {
-    float M = -INFINITY;
-    for (int i = t; i < NT; i += 32) M = fmaxf(M, st.m[i]);
+    float cm = -INFINITY;
+    for (int i = t; i < NT; i += 32) cm = fmaxf(cm, st.m[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, o));
+    float cs = 0.f;
+    if (cm != -INFINITY)
+      for (int i = t; i < NT; i += 32) cs += st.m[i] == -INFINITY ? 0.f : st.s[i] * exp2f((st.m[i] - cm) * k2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(FULL, cs, o);
+    if (t == 0) { st.cm[slot] = cm; st.cs[slot] = cs; }
+  }
+  cluster.sync();  // every CTA's pair of this pass is written
+  if (t < 32) {
+    // lane r folds CTA r's pair; the same butterflies over the same values in
+    // every CTA give every CTA the same (M, W)
+    float mr = -INFINITY, sr = 0.f;
+    if (t < CL) {
+      mr = *cluster.map_shared_rank(&st.cm[slot], t);
+      sr = *cluster.map_shared_rank(&st.cs[slot], t);
+    }
+    float M = mr;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-    float W = 0.f;
-    if (M != -INFINITY)
-      for (int i = t; i < NT; i += 32) W += st.m[i] == -INFINITY ? 0.f : st.s[i] * exp2f((st.m[i] - M) * k2);
+    float W = (mr == -INFINITY) ? 0.f : sr * exp2f((mr - M) * k2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(FULL, W, o);
-    if (t == 0) { st.M = M; st.W = W; st.ch = ch; }
+    if (t == 0) { st.M = M; st.W = W; }
   }
   __syncthreads();
 }

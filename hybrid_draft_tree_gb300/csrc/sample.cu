@@ -12,12 +12,17 @@
 // with u_res.  Every emitted token is then distributed exactly as p.  The
 // uniforms are inputs.
 //
-// One CTA per request walks the accepted path.  Each node's row is read once
-// (row_softmax.cuh: per-thread contiguous chunks with their online max and sum
-// of exponentials); the final draw finds its chunk from the chunks' sums and
-// one warp scans that chunk, so no second pass over the row is needed.  The
-// top-8 and matrix update come from the scan kernels as in greedy
-// verification.
+// One thread-block cluster of CL CTAs per request walks the accepted path
+// (row_softmax.cuh: each node's row is read once, split over the cluster's
+// SMs, each CTA keeping its range in shared memory).  Every CTA takes the same
+// decisions from the same statistics, so the walk needs no further exchange;
+// the final draw exchanges the CTAs' weights once, and the CTA holding the
+// target finds its chunk and one warp scans it in shared memory, so no second
+// pass over the row is needed.  The top-8 and matrix update come
+// from the scan kernels as in greedy verification; this kernel reads only the
+// logits and the trees, so it is launched as a programmatic dependent of the
+// update kernel and runs beside it (it waits for that kernel only before it
+// exits, so its completion still implies theirs).
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -29,31 +34,38 @@ namespace {
 using namespace scan;
 using namespace softmax;
 
-constexpr int PT = 1024;  // threads per CTA: one row per CTA, so memory parallelism comes from the threads
+constexpr int PT = 256;  // threads per CTA (CL CTAs per request)
+constexpr int STAGE_MAX = 160 * 1024;  // shared memory for a CTA's range of the row; larger rows read it again
 constexpr float LOG2E = 1.4426950408889634f;
 
 template <int DT>
-__global__ __launch_bounds__(PT) void k_sample(VerifyArgs a) {
+__global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
-  __shared__ RowStats<PT> st;
+  extern __shared__ __align__(16) char s_stage[];  // this CTA's range of the current row (when staged)
+  __shared__ ClusterRow<PT> st;
   __shared__ int32_t s_tok[MAX_S], s_par[MAX_S], s_rej[MAX_S];
   __shared__ float s_x[MAX_S];         // logits of the node's children, by slot
   __shared__ float s_u[MAX_S];         // the request's acceptance uniforms, by slot
   __shared__ float s_cw[PT];           // chunk weights of the final draw
   __shared__ int s_acc, s_nrej, s_chunk, s_pick;
-  __shared__ float s_target, s_before;
-  const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5, S = a.S, V = a.g.V;
+  __shared__ float s_target, s_before, s_ures;
+  const cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / CL, t = threadIdx.x, lane = t & 31, warp = t >> 5, S = a.S, V = a.g.V;
   const float k2 = a.inv_temp * LOG2E;
   if (t < S) {
     s_tok[t] = a.tree_tok[(int64_t)b * S + t];
     s_par[t] = a.tree_parent[(int64_t)b * S + t];
     s_u[t] = a.u_accept[(int64_t)b * S + t];
   }
+  if (t == 0) s_ures = a.u_resid[b];
+  char* stage = staged ? s_stage : nullptr;
   __syncthreads();
   int32_t* out = a.out_tokens + (int64_t)b * S;
-  if (s_tok[0] < 0 || s_tok[0] >= V) {  // no valid root: nothing accepted, nothing emitted
-    if (t < S) out[t] = -1;
-    if (t == 0) a.accept_len[b] = 0;
+  if (s_tok[0] < 0 || s_tok[0] >= V) {  // no valid root: nothing accepted, nothing emitted (uniform in the cluster)
+    if (rank == 0 && t < S) out[t] = -1;
+    if (rank == 0 && t == 0) a.accept_len[b] = 0;
+    grid_dependency_wait();
     return;
   }
   int node = 0, len = 0;
@@ -64,9 +76,9 @@ __global__ __launch_bounds__(PT) void k_sample(VerifyArgs a) {
       const int32_t tk = s_tok[t];
       s_x[t] = (t > node && s_par[t] == node && tk >= 0 && tk < V) ? load_scalar<DT>(rowp, tk) : 0.f;
     }
-    row_stats<DT, PT>(rowp, V, a.g.vec != 0, k2, st);
+    cluster_row_stats<DT, PT>(cluster, rowp, V, a.g.vec != 0, k2, st, depth, stage);
     const float M = st.M, W = st.W;
-    if (t == 0) {
+    if (t == 0) {  // the same decisions in every CTA of the cluster
       float rem = 1.f;
       int acc = -1, nrej = 0;
       for (int j = node + 1; j < S && acc < 0; ++j) {
@@ -85,7 +97,7 @@ __global__ __launch_bounds__(PT) void k_sample(VerifyArgs a) {
     __syncthreads();
     const int acc = s_acc;
     if (acc >= 0) {
-      if (t == 0) out[len] = s_tok[acc];
+      if (rank == 0 && t == 0) out[len] = s_tok[acc];
       ++len;
       node = acc;
       continue;
@@ -93,33 +105,58 @@ __global__ __launch_bounds__(PT) void k_sample(VerifyArgs a) {
     // every child rejected (or a leaf): draw from the unrejected tokens.
     // 1. chunk weights relative to M, minus the rejected tokens in the chunk
     const int nrej = s_nrej;
-    const int ch = st.ch;
-    const int c0 = min(t * ch, V), c1 = min(c0 + ch, V);
+    const int ch = st.ch, lo = st.lo, hi = st.hi;
+    // element v of this CTA's range
+    auto elem = [&](int v) { return stage ? stage_elem<DT>(stage, v - lo) : load_scalar<DT>(rowp, v); };
+    const int c0 = min(lo + t * ch, hi), c1 = min(c0 + ch, hi);
     float cw = st.m[t] == -INFINITY ? 0.f : st.s[t] * exp2f((st.m[t] - M) * k2);
     for (int q = 0; q < nrej; ++q) {
       const int32_t r = s_rej[q];
-      if (r >= c0 && r < c1) cw -= exp2f((load_scalar<DT>(rowp, r) - M) * k2);
+      if (r >= c0 && r < c1) cw -= exp2f((elem(r) - M) * k2);
     }
     cw = fmaxf(cw, 0.f);
     s_cw[t] = cw;
-    // 2. the chunk holding the target (warp 0): lane l sums chunks 8l..8l+7 in
-    //    order, a warp scan orders the lanes; a fixed summation order
     __syncthreads();
+    // 2. warp 0: lane l sums chunks CPL*l .. CPL*l + CPL-1 in order, a warp
+    //    scan orders the lanes (a fixed summation order); the CTA's weight goes
+    //    to the other CTAs, which fold the CL weights in rank order
+    constexpr int CPL = PT / 32;
+    float w8[CPL];
+    float lsum = 0.f, incl = 0.f;
     if (warp == 0) {
-      constexpr int CPL = PT / 32;
-      float w8[CPL];
-      float lsum = 0.f;
 #pragma unroll
       for (int i = 0; i < CPL; ++i) { w8[i] = s_cw[lane * CPL + i]; lsum += w8[i]; }
-      float incl = lsum;
+      incl = lsum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float y = __shfl_up_sync(FULL, incl, o);
         if (lane >= o) incl += y;
       }
-      const float total = __shfl_sync(FULL, incl, 31);
-      const float target = a.u_resid[b] * total;
-      float run = incl - lsum;  // weight before this lane's chunks
+      if (lane == 31) st.ct = incl;
+    }
+    cluster.sync();  // every CTA's weight is written
+    int owner = -1;
+    float before_cta = 0.f, target = 0.f;
+    if (warp == 0) {
+      const float cwr = lane < CL ? *cluster.map_shared_rank(&st.ct, lane) : 0.f;
+      float ci = cwr;  // inclusive scan over the ranks
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(FULL, ci, o);
+        if (lane >= o) ci += y;
+      }
+      const float total = __shfl_sync(FULL, ci, CL - 1);
+      target = s_ures * total;
+      const unsigned hit = __ballot_sync(FULL, lane < CL && cwr > 0.f && ci > target);
+      const unsigned any = __ballot_sync(FULL, lane < CL && cwr > 0.f);
+      owner = hit ? __ffs(hit) - 1 : (any ? 31 - __clz(any) : -1);  // else rounding: the last CTA with weight
+      before_cta = __shfl_sync(FULL, ci - cwr, owner >= 0 ? owner : 0);
+    }
+    cluster.sync();  // the weights are read: no CTA's shared memory is accessed from here on
+    if (warp == 0 && owner < 0 && rank == 0 && lane == 0) s_pick = -1;  // no token has weight
+    if (warp == 0 && owner == rank) {
+      // 3. this CTA holds the target: its chunk, from the lanes' sums
+      float run = before_cta + incl - lsum;  // weight before this lane's chunks
       int c = -1, last = -1;
       float cb = 0.f, last_before = 0.f;
 #pragma unroll
@@ -141,26 +178,24 @@ __global__ __launch_bounds__(PT) void k_sample(VerifyArgs a) {
         s_before = bb;
         s_target = target;
       }
-    }
-    __syncthreads();
-    // 3. warp 0 scans the chunk: per-lane sub-ranges, a warp prefix, then the
-    //    lane holding the target walks its elements
-    if (warp == 0) {
-      const int c = s_chunk;
+      __syncwarp();
+      // 4. the chunk: per-lane sub-ranges, a warp prefix, then the lane
+      //    holding the target walks its elements
+      const int cidx = s_chunk;
       int pick = -1;
-      if (c >= 0) {
-        const int lo = min(c * ch, V), hi = min(lo + ch, V);
-        const float bef = s_before;  // weight of the chunks before c
-        const int sub = (hi - lo + 31) / 32;
-        const int l0 = min(lo + lane * sub, hi), l1 = min(l0 + sub, hi);
+      if (cidx >= 0) {
+        const int clo = min(lo + cidx * ch, hi), chi = min(clo + ch, hi);
+        const float bef = s_before;  // weight of everything before chunk cidx
+        const int sub = (chi - clo + 31) / 32;
+        const int l0 = min(clo + lane * sub, chi), l1 = min(l0 + sub, chi);
         float ls = 0.f;
-        int last = -1;
+        int lastv = -1;
         for (int v = l0; v < l1; ++v) {
           bool rej = false;
           for (int q = 0; q < nrej; ++q) rej |= s_rej[q] == v;
           if (rej) continue;
-          const float wv = exp2f((load_scalar<DT>(rowp, v) - M) * k2);
-          if (wv > 0.f) { ls += wv; last = v; }
+          const float wv = exp2f((elem(v) - M) * k2);
+          if (wv > 0.f) { ls += wv; lastv = v; }
         }
         float li = ls;
 #pragma unroll
@@ -174,40 +209,68 @@ __global__ __launch_bounds__(PT) void k_sample(VerifyArgs a) {
         const unsigned who = __ballot_sync(FULL, mine);
         int lpick = -1;
         if (who != 0 && lane == __ffs(who) - 1) {
-          float run = lb;
+          float rr = lb;
           for (int v = l0; v < l1 && lpick < 0; ++v) {
             bool rej = false;
             for (int q = 0; q < nrej; ++q) rej |= s_rej[q] == v;
             if (rej) continue;
-            const float wv = exp2f((load_scalar<DT>(rowp, v) - M) * k2);
+            const float wv = exp2f((elem(v) - M) * k2);
             if (wv <= 0.f) continue;
-            run += wv;
-            if (run > tgt) lpick = v;
+            rr += wv;
+            if (rr > tgt) lpick = v;
           }
-          if (lpick < 0) lpick = last;
+          if (lpick < 0) lpick = lastv;
         }
         pick = __shfl_sync(FULL, lpick, who != 0 ? __ffs(who) - 1 : 0);
         if (who == 0) {  // rounding: the chunk's last element with weight
-          const unsigned has = __ballot_sync(FULL, last >= 0);
-          pick = has ? __shfl_sync(FULL, last, 31 - __clz(has)) : -1;
+          const unsigned has = __ballot_sync(FULL, lastv >= 0);
+          pick = has ? __shfl_sync(FULL, lastv, 31 - __clz(has)) : -1;
         }
       }
       if (lane == 0) s_pick = pick;
     }
-    __syncthreads();
-    if (t == 0) {
+    // thread 0 (warp 0, which holds `owner`) of the owning CTA (of CTA 0 when
+    // no token has weight) writes the drawn token and the accepted length
+    if (t == 0 && (owner >= 0 ? owner == rank : rank == 0)) {
       out[len] = s_pick;
       a.accept_len[b] = len;
     }
-    for (int j = len + 1 + t; j < S; j += PT) out[j] = -1;
+    if (rank == 0)
+      for (int j = len + 1 + t; j < S; j += PT) out[j] = -1;
+    grid_dependency_wait();
     return;
   }
+  grid_dependency_wait();
 }
 
 template <int DT>
 cudaError_t sample_impl(const VerifyArgs& a, cudaStream_t s) {
-  k_sample<DT><<<a.batch, PT, 0, s>>>(a);
-  return cudaGetLastError();
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  const int bytes = stage_bytes(a.g.V, ES);
+  const int staged = bytes <= STAGE_MAX ? 1 : 0;
+  static int opted = 48 * 1024;  // dynamic shared memory allowed so far
+  if (staged && bytes > opted) {
+    const cudaError_t e = cudaFuncSetAttribute(k_sample<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    opted = bytes;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.batch * CL);
+  cfg.blockDim = dim3(PT);
+  cfg.dynamicSmemBytes = staged ? bytes : 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // the walk reads only the logits and the trees: it may start while the
+  // update kernel ahead of it runs (it waits for it only before exiting)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_sample<DT>, a, staged);
 }
 
 }  // namespace
