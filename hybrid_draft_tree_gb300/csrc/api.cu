@@ -35,11 +35,16 @@ struct graft_handle {
   int32_t* topk = nullptr;        // [rows][8]
   int32_t* row_nseg = nullptr;    // [rows]
   float* umax = nullptr;          // [rows][upr_max rounded up to 4] two-pass unit maxima
+  float* usec = nullptr;          // [rows][same] second largest element of every unit (scan_kernel 4)
+  uint8_t* upos = nullptr;        // [rows][same] position of every unit's maximum (scan_kernel 4)
+  float* warm_umax = nullptr;     // [min(V, WARM_TWO_PASS_ROWS)][upr_max rounded up to 4] the warm-up's
+  int warm_rows = 0;
   int upr_max = 0;
   int32_t* list = nullptr;        // [V] warm-up rows
   int32_t* count = nullptr;       // [1]
   uint32_t* err = nullptr;        // [1]
   int32_t last_launches = 0;
+  uint32_t wait_polls = 0;        // TMA scan wait limit (0 = the kernel's default)
   char msg[256] = {0};
   // tracing: event pairs around kernels, read back by graft_profile_read
   static constexpr int kProfSlots = 64;
@@ -143,7 +148,8 @@ void free_all(graft_handle* h) {
   for (auto& e : h->prof_ev)
     if (e) cudaEventDestroy(e);
   cudaFree(h->C); cudaFree(h->winner); cudaFree(h->tpl); cudaFree(h->part);
-  cudaFree(h->row_ticket); cudaFree(h->req_ticket); cudaFree(h->topk); cudaFree(h->row_nseg); cudaFree(h->umax);
+  cudaFree(h->row_ticket); cudaFree(h->req_ticket); cudaFree(h->topk); cudaFree(h->row_nseg); cudaFree(h->umax); cudaFree(h->usec); cudaFree(h->upos);
+  cudaFree(h->warm_umax);
   cudaFree(h->list); cudaFree(h->count); cudaFree(h->err);
 }
 
@@ -168,7 +174,7 @@ int check_cfg(const graft_config* c, graft_handle* h) {
   const int maxn = c->mode == GRAFT_MODE_TAIL ? c->budget : graft::MAX_DRAFT;
   if (c->max_draft_nodes < 0 || c->max_draft_nodes > maxn)
     return fail(h, GRAFT_EINVAL, "max_draft_nodes must be in [0, %d]", maxn);
-  if (c->scan_kernel < 0 || c->scan_kernel > 3) return fail(h, GRAFT_EINVAL, "scan_kernel must be 0, 1, 2 or 3");
+  if (c->scan_kernel < 0 || c->scan_kernel > 4) return fail(h, GRAFT_EINVAL, "scan_kernel must be in [0, 4]");
   return GRAFT_OK;
 }
 
@@ -252,7 +258,12 @@ int graft_init(const graft_config* cfg, graft_handle** out) {
     const int64_t epl_min = cfg->logits_dtype == GRAFT_BF16 ? 8 : 4;  // two-pass runs on 16-byte aligned rows only
     const int64_t upr = (V / epl_min + 31) / 32;
     h->upr_max = (int)(upr <= graft::TWO_PASS_MAX_UNITS ? upr : 0);
-    if (e == cudaSuccess && h->upr_max > 0) e = dalloc(&h->umax, rows * (size_t)((h->upr_max + 3) & ~3));
+    const size_t ups = (size_t)((h->upr_max + 3) & ~3);
+    if (e == cudaSuccess && h->upr_max > 0) e = dalloc(&h->umax, rows * ups);
+    if (e == cudaSuccess && h->upr_max > 0 && cfg->scan_kernel == 4) e = dalloc(&h->usec, rows * ups);
+    if (e == cudaSuccess && h->upr_max > 0 && cfg->scan_kernel == 4) e = dalloc(&h->upos, rows * ups);
+    h->warm_rows = (int)std::min<size_t>(V, graft::WARM_TWO_PASS_ROWS);
+    if (e == cudaSuccess && h->upr_max > 0) e = dalloc(&h->warm_umax, (size_t)h->warm_rows * ups);
   }
   if (e == cudaSuccess) e = dalloc(&h->list, V);
   if (e == cudaSuccess) e = dalloc(&h->count, 1);
@@ -310,13 +321,37 @@ int graft_warmup(graft_handle* h, const int32_t* d_tokens, const void* d_logits,
   a.count = h->count;
   a.C = h->C;
   a.err = h->err;
+  // the last occurrence of each token (listed on the device) takes the
+  // two-pass scan on aligned rows, up to warm_rows of them; any further rows
+  // (and unaligned rows) take the single-pass scan
+  const int32_t upr = (int32_t)((a.g.nslot + 31) / 32);
+  const bool two_pass = a.g.vec && h->warm_umax && a.g.nslot > 0 && upr <= h->upr_max;
+  a.start = two_pass ? h->warm_rows : 0;
+  graft::VerifyArgs v{};
+  v.g = a.g;
+  v.logits = d_logits;
+  v.umax = h->warm_umax;
+  v.top2 = 0;
+  v.upr = upr;
+  v.ups = (upr + 3) & ~3;
+  v.err = h->err;
+  const int grid1 = h->num_sms * graft::two_pass_ctas_per_sm();
+  const int dt = h->cfg.logits_dtype;
   cudaError_t e;
   {
     ProfScope ps(h, (cudaStream_t)stream, "warmup");
-    e = graft::launch_warmup(a, h->cfg.logits_dtype, h->warm_ctas, (cudaStream_t)stream);
+    e = graft::launch_warmup_begin(a, (cudaStream_t)stream);
+    if (e == cudaSuccess && two_pass)
+      e = graft::launch_warm_umax(v, h->list, h->count, h->warm_rows, dt, grid1, (cudaStream_t)stream);
+    if (e == cudaSuccess && two_pass)
+      e = graft::launch_warm_select(v, d_tokens, h->list, h->count, h->warm_rows, h->C, dt, h->num_sms * 2,
+                                    (cudaStream_t)stream);
+    if (e == cudaSuccess && n_rows > a.start)
+      e = graft::launch_warmup_scan(a, dt, h->warm_ctas, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = graft::launch_warmup_end(a, (cudaStream_t)stream);
   }
   if (e != cudaSuccess) return cuda_fail(h, e, "graft_warmup launch");
-  h->last_launches = 4;
+  h->last_launches = 3 + (two_pass ? 2 : 0) + (n_rows > a.start ? 1 : 0);
   return GRAFT_OK;
 }
 
@@ -349,7 +384,7 @@ graft::AssembleArgs assemble_args(const graft_handle* h, int32_t batch, int32_t 
 int assemble_impl(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
                   const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes,
                   const int32_t* d_event, const int32_t* d_retrieved, int32_t* d_tree_tok, int8_t* d_tree_parent,
-                  int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info, void* stream) {
+                  int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info, int8_t* d_slot_src, void* stream) {
   if (!h) return GRAFT_EINVAL;
   h->last_launches = 0;
   const graft_config& c = h->cfg;
@@ -367,6 +402,7 @@ int assemble_impl(graft_handle* h, int32_t batch, const int32_t* d_root_tok, con
   a.rtok_in = d_retrieved;
   a.tree_tok = d_tree_tok; a.tree_parent = d_tree_parent; a.tree_pos = d_tree_pos; a.tree_mask = d_tree_mask;
   a.info = d_info;
+  a.slot_src = d_slot_src;
   cudaError_t e;
   {
     ProfScope ps(h, (cudaStream_t)stream, "k_assemble");
@@ -386,7 +422,18 @@ int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
                    int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask, int32_t* d_info, void* stream) {
   NvtxRange nvtx("graft_assemble");
   return assemble_impl(h, batch, d_root_tok, d_draft_tok, d_draft_parent, d_draft_aux, draft_nodes, nullptr, nullptr,
-                       d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, stream);
+                       d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, nullptr, stream);
+}
+
+int graft_assemble_src(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                       const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes,
+                       int32_t* d_tree_tok, int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask,
+                       int32_t* d_info, int8_t* d_slot_src, void* stream) {
+  NvtxRange nvtx("graft_assemble_src");
+  if (!h) return GRAFT_EINVAL;
+  if (batch > 0 && !d_slot_src) return fail(h, GRAFT_EINVAL, "null pointer");
+  return assemble_impl(h, batch, d_root_tok, d_draft_tok, d_draft_parent, d_draft_aux, draft_nodes, nullptr, nullptr,
+                       d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, d_slot_src, stream);
 }
 
 int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, const float* d_draft_prob,
@@ -447,7 +494,7 @@ int graft_assemble_staged(graft_handle* h, int32_t batch, const int32_t* d_root_
   if (h->cfg.mode != GRAFT_MODE_CHECKPOINT) return fail(h, GRAFT_EINVAL, "graft_assemble_staged needs checkpoint mode");
   if (batch > 0 && (!d_event || !d_retrieved)) return fail(h, GRAFT_EINVAL, "null pointer");
   return assemble_impl(h, batch, d_root_tok, d_draft_tok, d_draft_parent, d_draft_prob, draft_nodes, d_event,
-                       d_retrieved, d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, stream);
+                       d_retrieved, d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_info, nullptr, stream);
 }
 
 int graft_confidence(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, const float* d_draft_prob,
@@ -592,12 +639,16 @@ int verify_impl(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const
   const bool two_pass_fits = a.g.vec && h->umax && a.g.nslot > 0 && a.upr <= h->upr_max &&
                              rows <= graft::two_pass_max_rows(grid2);
   const bool use_tma = tma_fits && c.scan_kernel == 2;
-  const bool use_two_pass = !use_tma && two_pass_fits && (c.scan_kernel == 0 || c.scan_kernel == 3);
+  const bool use_two_pass = !use_tma && two_pass_fits && (c.scan_kernel == 0 || c.scan_kernel >= 3);
   const int grid = h->num_sms * graft::verify_ctas_per_sm();
   if (!use_tma && !use_two_pass && rows > graft::verify_max_rows(grid))
     return fail(h, GRAFT_EINVAL, "batch * (budget + 1) = %lld rows exceeds %d on this GPU", (long long)rows,
                 graft::verify_max_rows(grid));
   a.umax = h->umax;
+  a.usec = h->usec;
+  a.upos = h->upos;
+  a.top2 = (c.scan_kernel == 4 && h->usec && h->upos) ? 1 : 0;
+  a.wait_polls = h->wait_polls;  // measured: the records slow pass 1 by more than they save
   cudaError_t e;
   if (use_two_pass) {
     {
@@ -688,6 +739,12 @@ int graft_sync(graft_handle* h, void* stream, uint32_t* out_flags) {
 const char* graft_last_error(const graft_handle* h) { return h ? h->msg : "null handle"; }
 
 int32_t graft_last_launch_count(const graft_handle* h) { return h ? h->last_launches : 0; }
+
+int graft_set_wait_limit(graft_handle* h, uint32_t polls) {
+  if (!h) return GRAFT_EINVAL;
+  h->wait_polls = polls;
+  return GRAFT_OK;
+}
 
 int graft_profile_enable(graft_handle* h, int32_t on) {
   if (!h) return GRAFT_EINVAL;

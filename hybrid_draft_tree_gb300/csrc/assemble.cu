@@ -355,6 +355,13 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   if (t < S) {
     const int64_t k = (int64_t)b * S + t;
     const int32_t tk = o_tok[t];
+    if (a.slot_src) {
+      // where the slot's token came from: the root, the drafter, or the matrix
+      // (retrieval slots follow the kept draft slots; in static mode the
+      // in-place replacements)
+      const bool retrieved = (a.mode == GRAFT_MODE_STATIC) ? o_rep[t] == 2 : t >= rbase;
+      a.slot_src[k] = (int8_t)(tk < 0 ? -1 : t == 0 ? 0 : retrieved ? 2 : 1);
+    }
     if (tk >= 0) {
       uint64_t m = 1ull << t;
       int p = o_par[t];

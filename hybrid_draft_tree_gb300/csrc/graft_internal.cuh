@@ -14,6 +14,7 @@ constexpr int MAX_SPLIT = 16;   // CTAs per logits row in the verify scan
 constexpr int TMA_CHUNK = 32768; // bytes per pipeline stage of the TMA verify scan
 constexpr int TWO_PASS_MAX_ROWS = 4096;   // verified rows per call on the two-pass scan
 constexpr int TWO_PASS_MAX_UNITS = 1024;  // 512-byte units per row on the two-pass scan (512 KB rows)
+constexpr int WARM_TWO_PASS_ROWS = 4096;  // warm-up rows per call on the two-pass scan (the rest: single pass)
 
 // Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth.
 struct TemplateDev {
@@ -44,6 +45,7 @@ struct AssembleArgs {
   int32_t* tree_pos;
   uint64_t* tree_mask;
   int32_t* info;
+  int8_t* slot_src;           // [batch][S] slot provenance (0 root, 1 draft, 2 retrieved, -1 pad), or nullptr
   uint32_t* err;
 };
 
@@ -81,6 +83,10 @@ struct VerifyArgs {
   int32_t* winner;            // [V] last-writer key (row + 1), 0 = none
   int32_t* row_nseg;          // [rows] number of partial top-8s the scan wrote for the row
   float* umax;                // two-pass scan: [rows][ups] maximum of every 512-byte unit
+  float* usec;                // two-pass scan with top2: [rows][ups] second largest element of every unit
+  uint8_t* upos;              // two-pass scan with top2: [rows][ups] position of the unit's maximum in the unit
+  int32_t top2;               // two-pass scan: 1 = units record (max, second, position), 0 = max only
+  uint32_t wait_polls;        // TMA scan: polls before an mbarrier wait gives up (0 = the kernel's default)
   int32_t upr;                // two-pass scan: units per row
   int32_t ups;                // two-pass scan: row stride of umax (upr rounded up to a multiple of 4)
   uint32_t* err;
@@ -90,6 +96,7 @@ struct VerifyArgs {
 struct WarmArgs {
   ScanGeom g;
   int64_t n_rows;
+  int32_t start;      // the single-pass scan takes list entries from here on
   const void* logits;
   const int32_t* tokens;
   int32_t* winner;
@@ -152,6 +159,12 @@ cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaS
 cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s);
 int two_pass_ctas_per_sm();
 int two_pass_max_rows(int grid);
-cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s);
+cudaError_t launch_warmup_begin(const WarmArgs& a, cudaStream_t s);
+cudaError_t launch_warmup_scan(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s);
+cudaError_t launch_warmup_end(const WarmArgs& a, cudaStream_t s);
+cudaError_t launch_warm_umax(const VerifyArgs& a, const int32_t* list, const int32_t* count, int cap, int dtype,
+                             int grid, cudaStream_t s);
+cudaError_t launch_warm_select(const VerifyArgs& a, const int32_t* tokens, const int32_t* list, const int32_t* count,
+                               int cap, int32_t* C, int dtype, int grid, cudaStream_t s);
 
 }  // namespace graft

@@ -560,7 +560,7 @@ __global__ __launch_bounds__(ST) void k_warm_scan(WarmArgs a) {
   __shared__ ScanSmem sm;
   const int esize = DT == GRAFT_BF16 ? 2 : 4;
   const int count = __ldcg(a.count);
-  for (int e = blockIdx.x; e < count; e += gridDim.x) {
+  for (int e = a.start + blockIdx.x; e < count; e += gridDim.x) {
     const int32_t n = __ldcg(a.list + e);
     const int32_t t = a.tokens[n];
     init_top(sm);
@@ -585,13 +585,8 @@ cudaError_t verify_impl(const VerifyArgs& a, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 template <int DT, bool VEC>
-cudaError_t warm_impl(const WarmArgs& a, int grid_ctas, cudaStream_t s) {
-  const int t = 256;
-  const unsigned g = (unsigned)((a.n_rows + t - 1) / t);
-  k_warm_mark<<<g, t, 0, s>>>(a);
-  k_warm_list<<<g, t, 0, s>>>(a);
+cudaError_t warm_scan_impl(const WarmArgs& a, int grid_ctas, cudaStream_t s) {
   k_warm_scan<DT, VEC><<<grid_ctas, ST, 0, s>>>(a);
-  k_warm_reset<<<g, t, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -608,10 +603,23 @@ cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
   k_finish<<<a.batch, FT, 0, s>>>(a, C);
   return cudaGetLastError();
 }
-cudaError_t launch_warmup(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s) {
+cudaError_t launch_warmup_begin(const WarmArgs& a, cudaStream_t s) {
+  const int t = 256;
+  const unsigned g = (unsigned)((a.n_rows + t - 1) / t);
+  k_warm_mark<<<g, t, 0, s>>>(a);
+  k_warm_list<<<g, t, 0, s>>>(a);
+  return cudaGetLastError();
+}
+cudaError_t launch_warmup_scan(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s) {
   if (dtype == GRAFT_BF16)
-    return a.g.vec ? warm_impl<GRAFT_BF16, true>(a, grid_ctas, s) : warm_impl<GRAFT_BF16, false>(a, grid_ctas, s);
-  return a.g.vec ? warm_impl<GRAFT_F32, true>(a, grid_ctas, s) : warm_impl<GRAFT_F32, false>(a, grid_ctas, s);
+    return a.g.vec ? warm_scan_impl<GRAFT_BF16, true>(a, grid_ctas, s) : warm_scan_impl<GRAFT_BF16, false>(a, grid_ctas, s);
+  return a.g.vec ? warm_scan_impl<GRAFT_F32, true>(a, grid_ctas, s) : warm_scan_impl<GRAFT_F32, false>(a, grid_ctas, s);
+}
+cudaError_t launch_warmup_end(const WarmArgs& a, cudaStream_t s) {
+  const int t = 256;
+  const unsigned g = (unsigned)((a.n_rows + t - 1) / t);
+  k_warm_reset<<<g, t, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace graft

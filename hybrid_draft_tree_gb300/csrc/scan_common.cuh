@@ -95,6 +95,24 @@ template <> struct Vec16<GRAFT_BF16> {
     const uint32_t u = *reinterpret_cast<const uint32_t*>(&m);
     return max_nan(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
   }
+  // the largest element (NaN-propagating) and the second largest of the eight
+  // (the largest of the others; equal to m1 when the maximum repeats):
+  // pairwise max/min of the even and of the odd halves, then their merge
+  __device__ __forceinline__ void top2(float& m1, float& m2) const {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
+    const __nv_bfloat162 hab = __hmax2_nan(a, b), lab = __hmin2(a, b);
+    const __nv_bfloat162 hcd = __hmax2_nan(c, d), lcd = __hmin2(c, d);
+    const __nv_bfloat162 h = __hmax2_nan(hab, hcd);                      // (max even, max odd)
+    const __nv_bfloat162 l = __hmax2(__hmin2(hab, hcd), __hmax2(lab, lcd));  // (2nd even, 2nd odd)
+    const uint32_t hu = *reinterpret_cast<const uint32_t*>(&h), lu = *reinterpret_cast<const uint32_t*>(&l);
+    const float he = __uint_as_float(hu << 16), ho = __uint_as_float(hu & 0xFFFF0000u);
+    const float le = __uint_as_float(lu << 16), lo = __uint_as_float(lu & 0xFFFF0000u);
+    m1 = max_nan(he, ho);
+    m2 = fmaxf(fminf(he, ho), fmaxf(le, lo));
+  }
   __device__ __forceinline__ float elem(int e) const {
     const uint32_t w = (e < 2) ? r.x : (e < 4) ? r.y : (e < 6) ? r.z : r.w;
     return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
@@ -120,6 +138,13 @@ template <> struct Vec16<GRAFT_F32> {
   }
   __device__ __forceinline__ float elem(int e) const {
     return __uint_as_float(e == 0 ? r.x : e == 1 ? r.y : e == 2 ? r.z : r.w);
+  }
+  // the largest element (NaN-propagating) and the second largest of the four
+  __device__ __forceinline__ void top2(float& m1, float& m2) const {
+    const float a = __uint_as_float(r.x), b = __uint_as_float(r.y);
+    const float c = __uint_as_float(r.z), d = __uint_as_float(r.w);
+    m1 = max_nan(max_nan(a, b), max_nan(c, d));
+    m2 = fmaxf(fminf(fmaxf(a, b), fmaxf(c, d)), fmaxf(fminf(a, b), fminf(c, d)));
   }
   // bit e set iff elem(e) >= t (NaN compares false)
   __device__ __forceinline__ unsigned ge_mask(float t) const {

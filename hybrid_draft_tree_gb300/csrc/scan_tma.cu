@@ -19,7 +19,10 @@
 // ticket), which stages the row's top-8, claims the token's matrix row
 // (atomicMax of row+1) and, if it completes its request, runs the acceptance
 // walk.  Every wait is bounded: on expiry the kernel flags GRAFT_ERR_TIMEOUT,
-// drains its copies in flight and finishes.
+// the producer stops issuing, waits for the copies it has in flight to land
+// (a separate, far longer bound with a back-off: a bulk copy of 32 KB lands
+// within microseconds) and the CTA finishes.  The consumers' and producer's
+// poll limit is a launch argument, so a test can make the waits run out.
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -36,7 +39,8 @@ constexpr int NSTAGE = 6;
 constexpr int VPL = TMA_CHUNK / 16 / NCT;  // 16-byte vectors per consumer lane per chunk
 constexpr int WCAP = 256;               // candidate keys per warp
 constexpr int MAXROWS = 128;            // rows one CTA may touch
-constexpr uint32_t SPIN = 1u << 22;     // try_wait polls before a wait gives up
+constexpr uint32_t SPIN = 1u << 22;     // try_wait polls before a wait gives up (unless the launch sets a limit)
+constexpr uint32_t DRAIN = 1u << 20;    // back-off rounds (1 us each) the drain waits for a copy in flight
 
 struct TmaSmem {
   u64 full[NSTAGE];
@@ -70,20 +74,29 @@ __device__ __forceinline__ bool mbar_try_wait(u64* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
-// one thread, bounded
-__device__ __forceinline__ bool mbar_wait(u64* bar, uint32_t parity) {
-  for (uint32_t it = 0; it < SPIN; ++it)
+// one thread, at most `polls` polls
+__device__ __forceinline__ bool mbar_wait(u64* bar, uint32_t parity, uint32_t polls) {
+  for (uint32_t it = 0; it < polls; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
-// whole warp, bounded, warp-uniform result
-__device__ __forceinline__ bool mbar_wait_warp(u64* bar, uint32_t parity) {
+// whole warp, at most `polls` polls, warp-uniform result
+__device__ __forceinline__ bool mbar_wait_warp(u64* bar, uint32_t parity, uint32_t polls) {
   bool ok = false;
-  for (uint32_t it = 0; it < SPIN; ++it) {
+  for (uint32_t it = 0; it < polls; ++it) {
     ok = mbar_try_wait(bar, parity);
     if (__all_sync(FULL, ok)) return true;
   }
   return __all_sync(FULL, ok);
+}
+// the drain: one thread waits for a copy it issued to land, backing off 1 us
+// between polls, for about a second at most
+__device__ __forceinline__ bool mbar_wait_drain(u64* bar, uint32_t parity) {
+  for (uint32_t it = 0; it < DRAIN; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(1000);
+  }
+  return false;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, u64* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -133,6 +146,7 @@ __global__ void __launch_bounds__(TPB, 1) k_verify_tma(VerifyArgs a) {
   constexpr int EPL = 16 / ES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const ScanGeom& g = a.g;
+  const uint32_t polls = a.wait_polls ? a.wait_polls : SPIN;
   const int S = a.S;
   const int rows = a.batch * S;
   const int G = gridDim.x, c = blockIdx.x;
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__(TPB, 1) k_verify_tma(VerifyArgs a) {
         const int64_t j = i - i0;
         const int s = (int)(j % NSTAGE);
         const uint32_t use = (uint32_t)(j / NSTAGE);
-        if (use > 0 && !mbar_wait(&sm.empty[s], (use - 1) & 1)) {
+        if (use > 0 && !mbar_wait(&sm.empty[s], (use - 1) & 1, polls)) {
           atomicOr(a.err, GRAFT_ERR_TIMEOUT);
           *(volatile int*)&sm.abort_flag = 1;
           break;
@@ -215,9 +229,11 @@ __global__ void __launch_bounds__(TPB, 1) k_verify_tma(VerifyArgs a) {
         bulk_g2s(ring + (size_t)s * TMA_CHUNK, src, bytes, &sm.full[s]);
         ++issued;
       }
-      // drain: every copy still in flight lands before this CTA may exit
+      // drain: every copy still in flight lands before this CTA may exit (the
+      // stages of the last NSTAGE copies; a stage is reissued only after its
+      // previous copy was consumed, or given up with the abort flag set first)
       for (int64_t j = issued > NSTAGE ? issued - NSTAGE : 0; j < issued; ++j)
-        mbar_wait(&sm.full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1);
+        if (!mbar_wait_drain(&sm.full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1)) atomicOr(a.err, GRAFT_ERR_TIMEOUT);
     }
     return;
   }
@@ -266,7 +282,7 @@ __global__ void __launch_bounds__(TPB, 1) k_verify_tma(VerifyArgs a) {
       cur_k = k;
     }
     if (!dead) dead = __any_sync(FULL, *(volatile int*)&sm.abort_flag != 0);
-    if (!dead && !mbar_wait_warp(&sm.full[s], use & 1)) {
+    if (!dead && !mbar_wait_warp(&sm.full[s], use & 1, polls)) {
       if (lane == 0) {
         atomicOr(a.err, GRAFT_ERR_TIMEOUT);
         *(volatile int*)&sm.abort_flag = 1;

@@ -26,12 +26,12 @@ GRAFT_F32, GRAFT_BF16 = 0, 1
 K = 8
 
 # Entry points declared in include/graft.h (checked by the CPU tests).
-EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup", "graft_assemble",
+EXPORTS = ("graft_default_config", "graft_init", "graft_destroy", "graft_warmup", "graft_assemble", "graft_assemble_src",
            "graft_verify_update", "graft_get_matrix", "graft_set_matrix", "graft_matrix_device_ptr",
            "graft_sync", "graft_last_error", "graft_last_launch_count", "graft_verify_update_noalloc",
            "graft_profile_enable", "graft_profile_read", "graft_check", "graft_retrieve", "graft_assemble_staged",
            "graft_confidence", "graft_calibrate_thresholds", "graft_set_thresholds", "graft_coverage",
-           "graft_verify_update_sample", "graft_template")
+           "graft_verify_update_sample", "graft_template", "graft_set_wait_limit")
 
 
 def calibrate_thresholds(best: np.ndarray, quantile: float) -> np.ndarray:
@@ -116,14 +116,16 @@ def load(build_if_missing: bool = True):
     L.graft_last_error.restype = ctypes.c_char_p
     L.graft_last_launch_count.argtypes = [vp]
     L.graft_last_launch_count.restype = i32
+    L.graft_set_wait_limit.argtypes = [vp, ctypes.c_uint32]
+    L.graft_set_wait_limit.restype = ctypes.c_int
     L.graft_profile_enable.argtypes = [vp, i32]
     L.graft_profile_enable.restype = ctypes.c_int
     L.graft_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), i32]
     L.graft_profile_read.restype = ctypes.c_int
     L.graft_verify_update_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp]
     L.graft_verify_update_noalloc.restype = ctypes.c_int
-    for name in ("graft_init", "graft_destroy", "graft_warmup", "graft_assemble", "graft_verify_update",
-                 "graft_get_matrix", "graft_set_matrix", "graft_sync"):
+    for name in ("graft_init", "graft_destroy", "graft_warmup", "graft_assemble", "graft_assemble_src",
+                 "graft_verify_update", "graft_get_matrix", "graft_set_matrix", "graft_sync"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -260,13 +262,19 @@ class Graft:
         self._check(self.L.graft_warmup(self.h, pt, pl, n, stride if n else self.cfg.vocab, _stream(stream)))
 
     def assemble(self, batch, root_tok, draft_tok, draft_parent, draft_aux, tree_tok, tree_parent, tree_pos, tree_mask,
-                 info, stream=None):
+                 info, stream=None, slot_src=None):
+        """With slot_src (int8 [batch, S]), also where each slot's token came
+        from: 0 root, 1 draft, 2 matrix (retrieval), -1 pad."""
         n = draft_tok.shape[-1]
         args = (_buf(root_tok, "root_tok", _dtypes("int32"), max(batch, 0)),
                 *self._draft(batch, draft_tok, draft_parent, draft_aux, n),
                 *self._tree(batch, tree_tok, tree_parent, tree_pos, tree_mask),
                 _buf(info, "info", _dtypes("int32"), max(batch, 0) * 4))
-        self._check(self.L.graft_assemble(self.h, batch, *args[:4], n, *args[4:], _stream(stream)))
+        if slot_src is None:
+            self._check(self.L.graft_assemble(self.h, batch, *args[:4], n, *args[4:], _stream(stream)))
+        else:
+            src = _buf(slot_src, "slot_src", _dtypes("int8"), max(batch, 0) * self.S)
+            self._check(self.L.graft_assemble_src(self.h, batch, *args[:4], n, *args[4:], src, _stream(stream)))
 
     # incremental drafting (checkpoint mode): see graft_check in include/graft.h
     def check(self, batch, draft_parent, draft_prob, layer, event, stream=None):
@@ -377,6 +385,10 @@ class Graft:
 
     def last_launch_count(self) -> int:
         return int(self.L.graft_last_launch_count(self.h))
+
+    def set_wait_limit(self, polls: int):
+        """Poll limit of the TMA scan's mbarrier waits (0 = the default)."""
+        self._check(self.L.graft_set_wait_limit(self.h, int(polls)))
 
 
 class TreeBuffers:

@@ -88,10 +88,14 @@ typedef struct {
   float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15) */
   float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4) */
   int32_t max_draft_nodes;/* largest draft tree (<= 256) or block (<= budget) per request */
-  int32_t scan_kernel;    /* verify scan: 0 = automatic (two-pass on 16-byte aligned rows, else
-                             single-pass), 1 = single-pass with a shared running top-8,
-                             2 = TMA-pipelined (aligned rows of >= 32 KB only), 3 = two-pass
-                             (unit maxima, then per-row selection; aligned rows only) */
+  int32_t scan_kernel;    /* verify scan: 0 = automatic (two-pass with unit maxima on 16-byte
+                             aligned rows, else single-pass), 1 = single-pass with a shared
+                             running top-8, 2 = TMA-pipelined (aligned rows of >= 32 KB only),
+                             3 = two-pass with unit maxima (pass 2 reads every candidate unit
+                             again), 4 = two-pass with unit records (maximum, second largest,
+                             position of the maximum: pass 2 reads again only units with two
+                             elements at or above its threshold, pass 1 does more work per
+                             unit); 3 and 4 take aligned rows only */
   int32_t ablation;       /* checkpoint mode only (article §五 ablations; 0 elsewhere):
                              0 = Graft, 1 = confidence pruning without retrieval (the freed
                              slots stay empty), 2 = fixed split (no checkpoints: the top
@@ -143,6 +147,19 @@ int graft_assemble(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
                    const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes,
                    int32_t* d_tree_tok, int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask,
                    int32_t* d_info, void* stream);
+
+/* graft_assemble plus where each slot's token came from:
+ *   d_slot_src[b][S]    0 = the root, 1 = a kept draft node, 2 = the matrix
+ *                       (a retrieval node; in static mode an in-place
+ *                       replacement), -1 = a pad slot
+ * so a caller can tell which accepted tokens retrieval contributed (the
+ * pages' retrieval hit rate), also in static mode where the replacements do
+ * not follow the draft slots.  Same work otherwise; GRAFT_EINVAL for a NULL
+ * d_slot_src with batch > 0. */
+int graft_assemble_src(graft_handle* h, int32_t batch, const int32_t* d_root_tok, const int32_t* d_draft_tok,
+                       const int16_t* d_draft_parent, const float* d_draft_aux, int32_t draft_nodes,
+                       int32_t* d_tree_tok, int8_t* d_tree_parent, int32_t* d_tree_pos, uint64_t* d_tree_mask,
+                       int32_t* d_info, int8_t* d_slot_src, void* stream);
 
 /* Incremental drafting (article §二 gears 1-2; checkpoint mode only).  The
  * checkpoints exist to stop the drafter early, and the retrieval gather runs
@@ -331,6 +348,16 @@ int graft_profile_read(graft_handle* h, const char** names, float* ms, int32_t m
 /* Number of kernel launches the last graft_assemble / graft_verify_update /
  * graft_warmup call queued. */
 int32_t graft_last_launch_count(const graft_handle* h);
+
+/* Failure detection: the TMA-pipelined verify scan (scan_kernel 2) bounds
+ * every mbarrier wait of its producer and consumers by a number of polls; on
+ * expiry it sets GRAFT_ERR_TIMEOUT in the handle's error word, stops issuing
+ * copies, waits (for about a second at most) for the copies it has in
+ * flight, and finishes, leaving the handle usable; the step's outputs are
+ * then invalid.  This call sets that limit for later calls on the handle
+ * (polls = 0 restores the default of 2^22 polls), so a test can make the
+ * waits run out on purpose.  It has no counterpart in the paper. */
+int graft_set_wait_limit(graft_handle* h, uint32_t polls);
 
 #ifdef __cplusplus
 }

@@ -156,20 +156,64 @@ def test_lockstep_small(wid, V, B, sigma, steps):
     assert any(a > 0 for _, a in stats)
 
 
-@pytest.mark.parametrize("scan_kernel", [1, 2, 3])
+@pytest.mark.parametrize("wid,V,B,sigma", [(0, 3000, 3, 0.75), (2, 777, 16, 0.75), (4, 6007, 64, 2.0)])
+def test_slot_provenance(wid, V, B, sigma):
+    """graft_assemble_src writes the same trees as graft_assemble (compared
+    with the oracle) plus each slot's provenance: the root, the kept draft
+    nodes (info[1] of them), the matrix (info[2]: retrieval nodes after the
+    kept draft slots, or in-place replacements in static mode), pads."""
+    from workloads.device_loop import DeviceLoop
+    w = W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=sigma)
+    g = engine_for(w)
+    loop = DeviceLoop(w, g, track_src=True)
+    P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
+    C = oracle.new_matrix(w.V)
+    retrieved = 0
+    for step in range(12):
+        tok, par, aux = loop.draft()
+        loop.assemble()
+        trees = [oracle.assemble(P, loop.root_h[b], tok[b], aux[b], C, None if par is None else par[b])
+                 for b in range(w.B)]
+        assert_trees_equal(loop, trees, step)
+        src = loop.src.cpu().numpy()
+        for b, tr in enumerate(trees):
+            valid = tr.tok >= 0
+            assert np.array_equal(src[b] == -1, ~valid), (step, b)
+            assert src[b][0] == (0 if valid[0] else -1)
+            assert int((src[b] == 1).sum()) == tr.info[1] and int((src[b] == 2).sum()) == tr.info[2], (step, b)
+            if w.mode != W.MODE_STATIC:
+                r0 = 1 + int(tr.info[1])
+                assert (src[b][1:r0][valid[1:r0]] == 1).all() and (src[b][r0:][valid[r0:]] == 2).all()
+            retrieved += int(tr.info[2])
+        loop.make_logits()
+        tt = np.stack([t.tok for t in trees])
+        pp = np.stack([t.par for t in trees]).astype(np.int8)
+        lg = loop.h.tree_logits(tt, pp, loop.ctx_h, loop.prev_h)
+        loop.verify_update()
+        for b in range(w.B):
+            acc, out, topk = oracle.verify(trees[b], lg[b], w.dtype)
+            oracle.update(C, trees[b], topk)
+        loop.advance()
+    assert retrieved > 0
+    assert g.sync() == 0
+    g.close()
+
+
+@pytest.mark.parametrize("scan_kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("wid,V,B,sigma,steps", [
     (2, 40000, 16, 2.0, 8),     # static, 80 KB rows: 3 chunks per row, rows split over CTAs
     (4, 24576, 64, 2.0, 6),     # tail, 64 requests x 17 slots
     (0, 16384, 1, 0.75, 20),    # fp32 checkpoint, 64 KB rows, few rows per step
 ])
 def test_lockstep_both_scan_kernels(scan_kernel, wid, V, B, sigma, steps):
-    """The single-pass, TMA-pipelined and two-pass verify scans on rows of
-    >= 32 KB, closed loop against the oracle."""
+    """The single-pass, TMA-pipelined and two-pass verify scans (unit maxima
+    only, and unit records) on rows of >= 32 KB, closed loop against the
+    oracle."""
     w = W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=sigma)
     lockstep(w, steps, check_rows=4, scan_kernel=scan_kernel)
 
 
-@pytest.mark.parametrize("scan_kernel", [1, 2, 3])
+@pytest.mark.parametrize("scan_kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
 @pytest.mark.parametrize("V,pad,fn", [(40000, 0, "normal"), (40003, 5, "normal"), (65536, 0, "ties"),
                                       (33000, 0, "constant")])
@@ -415,6 +459,37 @@ def _stochastic_case(w, temp, steps, seed, min_fraction=0.5):
     eng.close()
 
 
+@pytest.mark.parametrize("dtype,V,n,distinct,pad", [
+    (W.BF16, 12000, 5000, 4500, 0),   # more last occurrences than the two-pass warm-up takes: the rest single-pass
+    (W.F32, 9001, 3000, 800, 0),      # fp32, a vocabulary tail
+    (W.BF16, 7001, 2000, 1500, 1),    # rows off 16-byte boundaries: single-pass only
+])
+def test_warmup_paths_match_oracle(dtype, V, n, distinct, pad):
+    """graft_warmup against the oracle's row-by-row load: the two-pass scan
+    over the listed last occurrences, its single-pass remainder, unaligned
+    rows, tie-heavy rows (the exact rescan)."""
+    g_ = G()
+    rng = np.random.default_rng(V + n)
+    pool = rng.choice(V, distinct, replace=False).astype(np.int32)
+    toks = pool[rng.integers(0, distinct, n)]
+    vals = rng.normal(size=(n, V)).astype(np.float32)
+    ties = rng.random(n) < 0.1
+    vals[ties] = rng.integers(-2, 3, (int(ties.sum()), V)).astype(np.float32)
+    host_rows = (vals.view(np.uint32) >> 16).astype(np.uint16) if dtype == W.BF16 else vals
+    stride = V + pad
+    buf = np.zeros((n, stride), host_rows.dtype)
+    buf[:, :V] = host_rows
+    dev = u16_to_bf16_tensor(buf) if dtype == W.BF16 else torch.from_numpy(buf).cuda()
+    eng = g_.Graft(g_.graft_default_config(V, 1, 0, dtype))
+    for call in range(2):                         # the second call reuses the handle's warm-up scratch
+        eng.warmup(torch.from_numpy(toks).cuda(), dev[:, :V])
+        C = oracle.new_matrix(V)
+        oracle.warmup(C, toks, host_rows, dtype)
+        assert np.array_equal(eng.get_matrix(), C), call
+    assert eng.sync() == 0
+    eng.close()
+
+
 @pytest.mark.parametrize("wid", [1, 3])
 def test_lockstep_warmup_small(wid):
     base = W.WORKLOADS[wid]
@@ -651,6 +726,47 @@ def test_error_flags_and_recovery():
     assert acc.item() == 0 and out[0, 0].item() == 0     # argmax of a zero row is id 0
 
 
+def test_tma_scan_wait_limit_expires_and_the_handle_recovers():
+    """Failure detection on the GPU without a fault: the TMA scan's waits get
+    a limit of one poll, so they run out while its bulk copies are in flight;
+    the kernel flags GRAFT_ERR_TIMEOUT, lets its copies land and finishes.
+    With the default limit restored the next call on the same handle is
+    clean and matches the oracle."""
+    g_ = G()
+    rng = np.random.default_rng(21)
+    V, B, S = 40000, 8, 61
+    vals = rng.normal(size=(B * S, V)).astype(np.float32)
+    host_rows = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    logits = u16_to_bf16_tensor(host_rows)
+    trees = []
+    for b in range(B):
+        tok = rng.integers(0, V, S).astype(np.int32)
+        par = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, S)], np.int32)
+        trees.append(_tree_from_parents(tok, par))
+    eng = g_.Graft(g_.graft_default_config(V, B, 0, W.BF16, scan_kernel=2))
+    tt = torch.from_numpy(np.stack([t.tok for t in trees])).cuda()
+    tp = torch.from_numpy(np.stack([t.par for t in trees]).astype(np.int8)).cuda()
+    tpos = torch.from_numpy(np.stack([t.pos for t in trees])).cuda()
+    tm = torch.from_numpy(np.stack([t.mask for t in trees]).view(np.int64)).cuda()
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty((B, S), dtype=torch.int32, device="cuda")
+    eng.set_wait_limit(1)
+    eng.verify_update(B, tt, tp, tpos, tm, logits, acc, out)
+    assert eng.sync(raise_on_error=False) & g_.graft.GRAFT_ERR_TIMEOUT
+    eng.set_wait_limit(0)
+    C0 = rng.integers(-1, V, (V, 8)).astype(np.int32)
+    eng.set_matrix(C0)
+    eng.verify_update(B, tt, tp, tpos, tm, logits, acc, out)
+    assert eng.sync() == 0
+    C = C0.copy()
+    for b in range(B):
+        a, o, topk = oracle.verify(trees[b], host_rows.reshape(B, S, V)[b], W.BF16)
+        oracle.update(C, trees[b], topk)
+        assert acc.cpu().numpy()[b] == a and np.array_equal(out.cpu().numpy()[b], o)
+    assert np.array_equal(eng.get_matrix(), C)
+    eng.close()
+
+
 def test_invalid_arguments_are_rejected():
     g_ = G()
     eng = g_.Graft(g_.graft_default_config(100, 2, 0, W.BF16))
@@ -665,7 +781,7 @@ def test_invalid_arguments_are_rejected():
         eng.check(2, torch.zeros((2, 4), dtype=torch.int16, device="cuda"), torch.ones((2, 4), device="cuda"), -1, ev)
     for mode, kw in ((0, dict(topk=4)), (1, dict(ablation=1)), (2, dict(ablation=2)), (0, dict(ablation=3)),
                      (0, dict(ablation=2, fixed_draft=61)), (0, dict(tpl_width=65)), (0, dict(tpl_depth=17)),
-                     (0, dict(scan_kernel=5))):
+                     (0, dict(scan_kernel=5)), (0, dict(scan_kernel=-1))):
         with pytest.raises(g_.GraftError):
             g_.Graft(g_.graft_default_config(100, 2, mode, W.BF16, **kw))
 

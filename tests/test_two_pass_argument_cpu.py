@@ -13,6 +13,13 @@ below T0.  The top-8 of the kept elements (value descending, id ascending) is
 therefore the row's.  The kernel falls back to an exact rescan when T0 is
 -inf (fewer than 8 finite lane maxima), when more than 128 units or more than
 192 elements are kept; the model reports those cases instead.
+
+With unit records, pass 1 also keeps each unit's second largest element
+(with multiplicity: equal to the maximum when it repeats) and the lowest
+position of its maximum.  A kept unit whose second largest element is below
+T0 holds exactly one element >= T0, its maximum, at the recorded position;
+pass 2 reads only the other kept units again.  The model checks that this
+gives the same kept elements, hence the same top-8.
 """
 import numpy as np
 import pytest
@@ -25,9 +32,10 @@ def reference_top8(x):
     return order[:8]
 
 
-def two_pass_top8(x, epl):
+def two_pass_top8(x, epl, records=False):
     """(top-8 ids, None) from the selection rule, or (None, reason) where the
-    kernel takes its exact rescan."""
+    kernel takes its exact rescan.  records: pass 2 takes single-element
+    units from the unit records instead of reading them again."""
     V = len(x)
     nslot = V // epl
     upr = -(-nslot // 32)
@@ -47,10 +55,17 @@ def two_pass_top8(x, epl):
     units = np.flatnonzero(umax >= T0)
     if len(units) > UCAP:
         return None, "units"
+    ue = 32 * epl
+    usort = -np.sort(-body.reshape(upr, ue), axis=1) if upr else np.zeros((0, 2))
+    usec = usort[:, 1] if upr else np.zeros(0)                     # second largest, with multiplicity
+    upos = body.reshape(upr, ue).argmax(axis=1) if upr else np.zeros(0, np.int64)   # lowest on ties
     ids = []
     for u in units:
-        lo, hi = u * 32 * epl, min((u + 1) * 32 * epl, nslot * epl)
-        ids.extend(lo + np.flatnonzero(x[lo:hi] >= T0))
+        lo, hi = u * ue, min((u + 1) * ue, nslot * epl)
+        if records and not usec[u] >= T0:
+            ids.append(lo + int(upos[u]))                        # the only element >= T0
+        else:
+            ids.extend(lo + np.flatnonzero(x[lo:hi] >= T0))
     ids.extend(nslot * epl + np.flatnonzero(x[nslot * epl:] >= T0))
     if len(ids) > ECAP:
         return None, "elements"
@@ -63,12 +78,15 @@ def two_pass_top8(x, epl):
 
 def _check(x, epl):
     got, why = two_pass_top8(x, epl)
+    rec, why_r = two_pass_top8(x, epl, records=True)
+    assert why_r == why
     if got is None:
         return why
     want = np.full(8, -1, np.int64)
     ref = reference_top8(x)
     want[:len(ref)] = ref
     assert np.array_equal(got, want)
+    assert np.array_equal(rec, want)
     return None
 
 
@@ -117,3 +135,28 @@ def test_fallbacks_are_taken_where_the_caps_bind():
     assert two_pass_top8(np.arange(7, dtype=np.float32), 8)[1] == "T0 = -inf"          # fewer than 8 lanes
     small = np.random.default_rng(1).normal(0, 1, 300).astype(np.float32)             # 2 units only
     assert two_pass_top8(small, 8)[1] == "T0 = -inf"
+
+
+@pytest.mark.parametrize("epl", [8, 4])
+def test_unit_records_decide_most_rows_without_a_reload(epl):
+    """On the synthetic rows (normal noise plus a planted successor) most
+    kept units hold a single element >= T0, so the records replace the
+    reload; a unit holding two of the top elements is read again."""
+    rng = np.random.default_rng(11 + epl)
+    V = 151936
+    single = multi = 0
+    for _ in range(6):
+        x = rng.normal(0, 1, V).astype(np.float32)
+        x[rng.integers(0, V)] += 5
+        x[3 * 32 * epl + 1] = x[3 * 32 * epl + 2] = 9.0           # two top elements in one unit
+        assert _check(x, epl) is None
+        nslot = V // epl
+        upr = -(-nslot // 32)
+        body = np.full(upr * 32 * epl, -np.inf)
+        body[:nslot * epl] = x[:nslot * epl]
+        srt = -np.sort(-body.reshape(upr, 32 * epl), axis=1)
+        T0 = np.sort(x)[::-1][7]                                   # the 8th largest element (>= the rule's T0)
+        kept = srt[:, 0] >= T0
+        single += int((kept & (srt[:, 1] < T0)).sum())
+        multi += int((kept & (srt[:, 1] >= T0)).sum())
+    assert multi >= 6 and single > 5 * multi
