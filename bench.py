@@ -266,17 +266,14 @@ def winner_slot(tok, par, accept_len, out_tokens) -> int:
     return int(hits[0]) if len(hits) else -1
 
 
-def retrieval_hits(mode, tok, par, info, accept_len, out_tokens):
-    """Per request: 1 when the deepest accepted node is a retrieved one, else
-    0 (None in static mode, whose in-place replacements the outputs do not
-    identify).  Checkpoint and tail trees hold their retrieved nodes after the
-    kept draft nodes: slots 1 + info[b][1] .. info[b][3] - 1."""
-    if mode == W.MODE_STATIC:
-        return None
+def retrieval_hits(src, tok, par, accept_len, out_tokens):
+    """Per request: 1 when the deepest accepted node came from the matrix
+    (slot provenance 2, as graft_assemble_src reports it: a retrieval node,
+    or an in-place replacement in static mode), else 0."""
     hits = []
     for b in range(len(accept_len)):
         ws_ = winner_slot(tok[b], par[b], int(accept_len[b]), out_tokens[b])
-        hits.append(int(accept_len[b] > 0 and ws_ >= 1 + int(info[b][1])))
+        hits.append(int(accept_len[b] > 0 and ws_ >= 0 and src[b][ws_] == 2))
     return hits
 
 
@@ -350,7 +347,7 @@ class DecodeTimer:
         acc = loop.accept_len.cpu().numpy()
         info = loop.info.cpu().numpy()
         try:
-            hit = retrieval_hits(self.w.mode, loop.tok.cpu().numpy(), loop.par.cpu().numpy(), info, acc,
+            hit = retrieval_hits(loop.src.cpu().numpy(), loop.tok.cpu().numpy(), loop.par.cpu().numpy(), acc,
                                  loop.out_tokens.cpu().numpy())
         except Exception:                                # a statistic only: never costs the measurement
             hit = None
@@ -391,7 +388,7 @@ def run_graft(args, ws, rank, local):
         w = w.scaled(seed=w.seed + 1000 * rank)
     eng = make_engine(w, args.scan_kernel)
     stream = torch.cuda.Stream(dev)
-    loop = DeviceLoop(w, eng, device=dev, stream=stream)
+    loop = DeviceLoop(w, eng, device=dev, stream=stream, track_src=True)
     flush_l2 = make_flush(dev)
     if w.warm != "none":
         toks_d, logits_d, _ = loop.warm_inputs_device()
@@ -485,9 +482,9 @@ def run_graft(args, ws, rank, local):
         "next_rows": next_rows,
         "stats": {"mean_accepted_tokens_per_step": round(mat, 4), "valid_rows_per_step": statistics.mean(valid_rows),
                   "retrieval_hit_rate": None if hit_rate is None else round(hit_rate, 4),
-                  "retrieval_hit_note": "share of request-steps whose deepest accepted node is a retrieved one "
-                                        "(null in static mode: in-place replacements are not identifiable from the "
-                                        "outputs)",
+                  "retrieval_hit_note": "share of request-steps whose deepest accepted node came from the matrix "
+                                        "(slot provenance from graft_assemble_src; in static mode an in-place "
+                                        "replacement)",
                   "prune_depth_histogram": prune_histogram(w.mode, [r[3] for r in recs]),
                   "matrix_populated_rows": populated,
                   "matrix_populated_bytes": None if populated is None else populated * 32,
@@ -528,7 +525,7 @@ def run_other_workload(wid, dev, steps, flush_l2, peak, warm_reps=3):
     w = W.WORKLOADS[wid]
     eng = make_engine(w)
     stream = torch.cuda.Stream(dev)
-    loop = DeviceLoop(w, eng, device=dev, stream=stream)
+    loop = DeviceLoop(w, eng, device=dev, stream=stream, track_src=True)
     res = {"workload": w.name, "vocab": w.V, "batch": w.B, "slots_per_request": w.S,
            "mode": ["checkpoint", "static", "tail"][w.mode], "dtype": "bf16" if w.dtype == W.BF16 else "f32"}
     if w.warm != "none":
@@ -687,6 +684,14 @@ def run_incremental(w, eng, loop, stream, flush_l2, steps=30):
     return out
 
 
+def pinned_copy(t):
+    """A copy of device tensor t in page-locked host memory."""
+    import torch
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t)
+    return h
+
+
 def run_e2e(args, w, eng, loop, stream, dev):
     """Same step through the C ABI with host buffers: the inputs of recorded
     steps are replayed from pinned memory (H2D inside the timed region, one
@@ -704,9 +709,8 @@ def run_e2e(args, w, eng, loop, stream, dev):
         loop.assemble()
         loop.make_logits()
         stream.synchronize()
-        rec.append(dict(root=loop.root.cpu().pin_memory(), tok=loop.d_tok.cpu().pin_memory(),
-                        par=loop.d_par.cpu().pin_memory(), aux=loop.d_aux.cpu().pin_memory(),
-                        logits=loop.logits.cpu().pin_memory()))
+        rec.append({k: pinned_copy(t) for k, t in (("root", loop.root), ("tok", loop.d_tok), ("par", loop.d_par),
+                                                    ("aux", loop.d_aux), ("logits", loop.logits))})
         loop.verify_update()
         loop.advance()
     tail = w.mode == W.MODE_TAIL
@@ -761,19 +765,24 @@ def run_e2e(args, w, eng, loop, stream, dev):
     e1.record(stream)
     e1.synchronize()
     ms = e0.elapsed_time(e1)
-    # the link alone: the logits' pinned-to-device copy on the copy stream
-    lms = []
-    for _ in range(5):
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(cs)
-        with torch.cuda.stream(cs):
-            sets[0]["logits"].copy_(rec[0]["logits"], non_blocking=True)
-        c1.record(cs)
-        c1.synchronize()
-        lms.append(c0.elapsed_time(c1))
-    link = rec[0]["logits"].numel() * rec[0]["logits"].element_size() / (min(lms) / 1e3) / 1e9
+    # the link alone: each recorded step's logits copied from pinned memory on the copy stream
+    lbytes = rec[0]["logits"].numel() * rec[0]["logits"].element_size()
+    links = []
+    for r in rec:
+        lms = []
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(cs)
+            with torch.cuda.stream(cs):
+                sets[0]["logits"].copy_(r["logits"], non_blocking=True)
+            c1.record(cs)
+            c1.synchronize()
+            lms.append(c0.elapsed_time(c1))
+        links.append(lbytes / (min(lms) / 1e3) / 1e9)
+    link = statistics.mean(links)
     return {"value": round(steps / (ms / 1e3), 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "h2d_link_GBps": round(link, 1),
+            "h2d_link_GBps_per_buffer": [round(x, 1) for x in links],
             "h2d_GBps_achieved": round(h2d * steps / (ms / 1e3) / 1e9, 1),
             "note": "inputs copied from pinned host memory each step (copy stream, double-buffered: step k + 1's "
                     "copy overlaps step k's kernels); h2d_link_GBps = a lone pinned-to-device copy of the logits"}

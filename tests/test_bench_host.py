@@ -125,12 +125,21 @@ def test_winner_slot_and_retrieval_hits(wid, sigma):
             accs.append(acc)
             outs.append(out)
         acc_a, out_a = np.array(accs, np.int32), np.stack(outs)
-        hits = b_.retrieval_hits(w.mode, tt, pp, np.stack([t.info for t in trees]), acc_a, out_a)
+        # slot provenance of checkpoint / tail trees: the kept draft slots follow
+        # the root, the retrieved ones follow them (info[1] kept draft slots)
+        src = np.where(tt >= 0, 1, -1).astype(np.int8)
+        src[:, 0] = np.where(tt[:, 0] >= 0, 0, -1)
+        for b in range(w.B):
+            r0 = 1 + int(trees[b].info[1])
+            src[b, r0:][tt[b, r0:] >= 0] = 2
+        hits = b_.retrieval_hits(src, tt, pp, acc_a, out_a)
         assert all(hv in (0, 1) for hv in hits)
+        for b in range(w.B):
+            wsl = b_.winner_slot(tt[b], pp[b], acc_a[b], out_a[b])
+            assert hits[b] == int(acc_a[b] > 0 and wsl >= 1 + int(trees[b].info[1]))
         hits_seen += sum(hits)
         h.advance(root, prev, ctx, out_a, acc_a)
     assert hits_seen > 0
-    assert b_.retrieval_hits(W.MODE_STATIC, tt, pp, np.zeros((2, 4), np.int32), acc_a, out_a) is None
 
 
 def test_hit_rate_and_populated_rows():

@@ -15,7 +15,7 @@ from . import F32, MODE_TAIL, DeviceSynth, Harness, Workload
 
 
 class DeviceLoop:
-    def __init__(self, w: Workload, engine, device="cuda:0", stream=None):
+    def __init__(self, w: Workload, engine, device="cuda:0", stream=None, track_src=False):
         import torch
         self.torch = torch
         self.w = w
@@ -39,6 +39,8 @@ class DeviceLoop:
         self.pos = torch.empty((B, S), dtype=torch.int32, device=dev)
         self.mask = torch.empty((B, S), dtype=torch.int64, device=dev)
         self.info = torch.empty((B, 4), dtype=torch.int32, device=dev)
+        # with track_src, assemble also writes each slot's provenance (0 root, 1 draft, 2 retrieved, -1 pad)
+        self.src = torch.empty((B, S), dtype=torch.int8, device=dev) if track_src else None
         self.accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
         self.out_tokens = torch.empty((B, S), dtype=torch.int32, device=dev)
         ldt = torch.float32 if w.dtype == F32 else torch.bfloat16
@@ -62,8 +64,12 @@ class DeviceLoop:
 
     def assemble(self):
         par = None if self.w.mode == MODE_TAIL else self.d_par
-        self.g.assemble(self.w.B, self.root, self.d_tok, par, self.d_aux, self.tok, self.par, self.pos, self.mask,
-                        self.info, stream=self.stream)
+        if self.src is None:
+            self.g.assemble(self.w.B, self.root, self.d_tok, par, self.d_aux, self.tok, self.par, self.pos, self.mask,
+                            self.info, stream=self.stream)
+        else:
+            self.g.assemble(self.w.B, self.root, self.d_tok, par, self.d_aux, self.tok, self.par, self.pos, self.mask,
+                            self.info, stream=self.stream, slot_src=self.src)
 
     def assemble_incremental(self, side_stream=None):
         """The same step through the incremental-drafting calls: checkpoint
