@@ -33,7 +33,7 @@ __global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t*
   __shared__ float s_x[MAX_S];  // a boundary candidate's logit in its parent's row, by slot
   const cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  const int b = blockIdx.x / CL, t = threadIdx.x, S = a.S;
+  const int b = blockIdx.x / CL, t = threadIdx.x, S = a.S, warp = t >> 5, lane = t & 31;
   const int n_draft = info[(int64_t)b * 4 + 1], n_retr = info[(int64_t)b * 4 + 2];
   const int r0 = min(max(1 + n_draft, 1), S), r1 = min(r0 + max(n_retr, 0), S);
   if (t < S) {
@@ -41,26 +41,48 @@ __global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t*
     s_par[t] = a.tree_parent[(int64_t)b * S + t];
   }
   __syncthreads();
-  float total = 0.f;  // thread 0's running sum (used in CTA 0)
+  // boundary parents (a kept slot with a retrieved child), in slot order
+  __shared__ unsigned long long s_bmask;
+  if (t == 0) s_bmask = 0ull;
+  __syncthreads();
+  if (t >= r0 && t < r1) {
+    const int p = s_par[t];
+    if (p >= 0 && p < r0) atomicOr(&s_bmask, 1ull << p);
+  }
+  __syncthreads();
+  uint64_t bmask = s_bmask;
+  float total = 0.f;  // lane 0 of warp 0's running sum (used in CTA 0)
   int pass = 0;
-  // boundary parents in slot order (a kept slot with a retrieved child)
-  for (int p = 0; p < r0 && p < S; ++p) {
-    bool has = false;
-    for (int j = r0; j < r1; ++j) has |= s_par[j] == p;
-    if (!has || s_tok[p] < 0 || s_tok[p] >= a.g.V) continue;  // (uniform: the same values in every CTA)
+  while (bmask != 0ull) {  // (uniform: the same values in every CTA)
+    const int p = __ffsll((long long)bmask) - 1;
+    bmask &= bmask - 1ull;
+    if (s_tok[p] < 0 || s_tok[p] >= a.g.V) continue;
     const char* rowp = reinterpret_cast<const char*>(a.logits) + ((size_t)b * S + p) * (size_t)a.g.stride * ES;
-    if (t >= r0 && t < r1 && s_par[t] == p && s_tok[t] >= 0 && s_tok[t] < a.g.V)
-      s_x[t] = load_scalar<DT>(rowp, s_tok[t]);  // fetched beside the row pass
+    {  // the candidates' logits, fetched beside the row pass by the CTA's last two warps
+      const int j = t - (CT - 64);
+      if (j >= r0 && j < r1 && s_par[j] == p && s_tok[j] >= 0 && s_tok[j] < a.g.V)
+        s_x[j] = load_scalar<DT>(rowp, s_tok[j]);
+    }
     cluster_row_stats<DT, CT>(cluster, rowp, a.g.V, a.g.vec != 0, LOG2E, st, pass++);
     const float M = st.M, Z = st.W;
-    if (t == 0 && rank == 0 && Z > 0.f) {
-      for (int j = r0; j < r1; ++j) {
+    if (warp == 0 && rank == 0 && Z > 0.f) {
+      // the kept draft children of p; a candidate with one of their tokens is not new
+      uint64_t kept = 0ull;
+      for (int base = 0; base < r0; base += 32) {
+        const int q = base + lane;
+        kept |= (uint64_t)__ballot_sync(FULL, q >= 1 && q < r0 && s_par[q] == p) << base;
+      }
+      float g = 0.f;
+      for (int j = r0 + lane; j < r1; j += 32) {
         const int32_t tk = s_tok[j];
         if (s_par[j] != p || tk < 0 || tk >= a.g.V) continue;
-        bool dup = false;  // a kept draft child of p with the same token is not new
-        for (int q = 1; q < r0; ++q) dup |= s_par[q] == p && s_tok[q] == tk;
-        if (!dup) total += exp2f((s_x[j] - M) * LOG2E) / Z;
+        bool dup = false;
+        for (uint64_t km = kept; km != 0ull; km &= km - 1ull) dup |= s_tok[__ffsll((long long)km) - 1] == tk;
+        if (!dup) g += exp2f((s_x[j] - M) * LOG2E) / Z;
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(FULL, g, o);
+      total += g;
     }
     __syncthreads();  // s_x is read before the next parent's loads
   }

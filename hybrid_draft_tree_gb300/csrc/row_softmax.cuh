@@ -107,16 +107,25 @@ __device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* 
 #pragma unroll
       for (int u = 0; u < UNR; ++u)
         if (base + u < nvec) x[u].r = __ldcs(p + base + u);
+      // the batch's maximum first (one rescale per batch), then its
+      // exponentials into four independent partial sums
+      float bm = -INFINITY;
 #pragma unroll
       for (int u = 0; u < UNR; ++u) {
         if (base + u >= nvec) break;
         if (sp) sp[base + u] = x[u].r;
-        const float vm = x[u].vmax();
-        if (vm > m) { s *= exp2f((m - vm) * k2); m = vm; }  // one rescale per vector
-        if (m != -INFINITY) {
+        bm = fmaxf(bm, x[u].vmax());
+      }
+      if (bm > m) { s *= exp2f((m - bm) * k2); m = bm; }
+      if (m != -INFINITY) {
+        float q[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) s += exp2f((x[u].elem(e) - m) * k2);
+        for (int u = 0; u < UNR; ++u) {
+          if (base + u >= nvec) break;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) q[e & 3] += exp2f((x[u].elem(e) - m) * k2);
         }
+        s += (q[0] + q[1]) + (q[2] + q[3]);
       }
     }
     for (int v = v0 + nvec * EPL; v < v1; ++v) {

@@ -71,28 +71,43 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
   int node = 0, len = 0;
   for (int depth = 0; depth < S; ++depth) {  // the path has fewer than S nodes
     const char* rowp = reinterpret_cast<const char*>(a.logits) + ((size_t)b * S + node) * (size_t)a.g.stride * ES;
-    // the children's logits, fetched beside the row pass
-    if (t < S) {
-      const int32_t tk = s_tok[t];
-      s_x[t] = (t > node && s_par[t] == node && tk >= 0 && tk < V) ? load_scalar<DT>(rowp, tk) : 0.f;
+    // the children's logits, fetched beside the row pass by the CTA's last
+    // two warps (the first ones start the row's loads without waiting)
+    {
+      const int j = t - (PT - 64);
+      if (j >= 0 && j < S) {
+        const int32_t tk = s_tok[j];
+        s_x[j] = (j > node && s_par[j] == node && tk >= 0 && tk < V) ? load_scalar<DT>(rowp, tk) : 0.f;
+      }
     }
     cluster_row_stats<DT, PT>(cluster, rowp, V, a.g.vec != 0, k2, st, depth, stage);
     const float M = st.M, W = st.W;
-    if (t == 0) {  // the same decisions in every CTA of the cluster
-      float rem = 1.f;
-      int acc = -1, nrej = 0;
-      for (int j = node + 1; j < S && acc < 0; ++j) {
-        const int32_t tk = s_tok[j];
-        if (s_par[j] != node || tk < 0 || tk >= V) continue;
-        bool seen = false;
-        for (int q = 0; q < nrej; ++q) seen |= s_rej[q] == tk;
-        if (seen) continue;  // a repeated token: its mass is gone
-        const float pc = exp2f((s_x[j] - M) * k2) / W;
-        if (s_u[j] * rem < pc) acc = j;
-        else { rem -= pc; s_rej[nrej++] = tk; }
+    if (warp == 0) {  // the same decisions in every CTA of the cluster
+      // the node's children in slot order, found by the whole warp; then one
+      // lane tests them in that order (each test depends on the ones before)
+      uint64_t kids = 0ull;
+      for (int base = 0; base < S; base += 32) {
+        const int j = base + lane;
+        const bool c = j > node && j < S && s_par[j] == node && s_tok[j] >= 0 && s_tok[j] < V;
+        kids |= (uint64_t)__ballot_sync(FULL, c) << base;
       }
-      s_acc = acc;
-      s_nrej = nrej;
+      if (lane == 0) {
+        float rem = 1.f;
+        int acc = -1, nrej = 0;
+        while (kids != 0ull && acc < 0) {
+          const int j = __ffsll((long long)kids) - 1;
+          kids &= kids - 1ull;
+          const int32_t tk = s_tok[j];
+          bool seen = false;
+          for (int q = 0; q < nrej; ++q) seen |= s_rej[q] == tk;
+          if (seen) continue;  // a repeated token: its mass is gone
+          const float pc = exp2f((s_x[j] - M) * k2) / W;
+          if (s_u[j] * rem < pc) acc = j;
+          else { rem -= pc; s_rej[nrej++] = tk; }
+        }
+        s_acc = acc;
+        s_nrej = nrej;
+      }
     }
     __syncthreads();
     const int acc = s_acc;
