@@ -207,7 +207,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
       s_key[t] = key;
     }
     __syncthreads();
-    bool keep = false;
+    bool kept = false;
     if (t < nn && my_depth <= cut) {
       const unsigned long long mine = s_key[t];
       const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(s_key);
@@ -227,12 +227,12 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
         r0 += x.x > mine;
         r1 += x.y > mine;
       }
-      keep = r0 + r1 + r2 + r3 < D;
+      kept = r0 + r1 + r2 + r3 < D;
     }
-    const int pre = block_excl_count(keep, s_warp, n_draft);
-    if (t < MAX_DRAFT) s_slot[t] = keep ? 1 + pre : -1;
+    const int pre = block_excl_count(kept, s_warp, n_draft);
+    if (t < MAX_DRAFT) s_slot[t] = kept ? 1 + pre : -1;
     __syncthreads();
-    if (keep) {
+    if (kept) {
       const int s = 1 + pre;
       const int p = s_par[t];
       int ps = 0;
