@@ -18,6 +18,21 @@ constexpr int WALK = 8;  // ancestors a node walks for its path confidence (deep
 
 __device__ __forceinline__ void raise_err(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
 
+// Bitonic sort of a warp's 64-bit keys, descending (lane 0 holds the largest).
+__device__ __forceinline__ unsigned long long bitonic32_desc_u64(unsigned long long key, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, j);
+      const bool desc = (lane & k) == 0;
+      const bool low = (lane & j) == 0;
+      key = (low == desc) ? (key > o ? key : o) : (key < o ? key : o);
+    }
+  }
+  return key;
+}
+
 // Block-wide exclusive prefix count of a predicate.  All threads must call.
 __device__ __forceinline__ int block_excl_count(bool v, int* s_warp, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -115,10 +130,10 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   __shared__ int32_t o_pos[MAX_S];
   __shared__ int32_t o_rep[MAX_S];
   __shared__ int s_warp[AT / 32];
-  __shared__ int s_bad, s_best[3], s_tcut, s_maxdepth;
+  __shared__ int s_bad, s_best[3], s_tcut, s_chain;
 
   const uint64_t keep = l2_keep_policy();
-  if (t == 0) { s_bad = 0; s_tcut = n; s_maxdepth = 0; }
+  if (t == 0) { s_bad = 0; s_tcut = n; s_chain = 0; }
   if (t < 3) s_best[t] = -1;
   if (t < MAX_S) {
     o_tok[t] = -1; o_par[t] = -1; o_pos[t] = -1; o_rep[t] = 0; s_rtok[t] = -1; s_rslot[t] = -1; s_cnt0[t] = 0;
@@ -161,7 +176,6 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
   if (a.mode != GRAFT_MODE_TAIL) {
     // ---- path confidence, root to leaf (gear 1) ---------------------------
     const int my_depth = block_path_conf(nn, t, prob, s_par, s_prob, s_conf, s_depth);
-    if (t < nn) atomicMax(&s_maxdepth, my_depth);
 
     // ---- checkpoints: best path confidence of layers 0, 1, 5 ---------------
     int D = a.budget, cut = INT_MAX;
@@ -199,35 +213,32 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
 
     // ---- keep the top-D candidates by (confidence desc, index asc) --------
     // key = (conf bits << 32) | (~index) for candidates (conf >= 0, so its bits
-    // order like the value), 0 otherwise; rank = number of larger keys.
-    if (t < MAX_DRAFT) {
-      unsigned long long key = 0ull;
-      if (t < nn && my_depth <= cut)
-        key = ((unsigned long long)__float_as_uint(s_conf[t]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
-      s_key[t] = key;
-    }
+    // order like the value), 0 otherwise; rank = number of larger keys.  Each
+    // warp sorts its 32 keys (bitonic, in registers); a candidate's rank is
+    // then the sum over the warps' sorted lists of the keys above its own,
+    // found by binary search in each list.
+    const unsigned long long mine =
+        (t < nn && my_depth <= cut)
+            ? (((unsigned long long)__float_as_uint(s_conf[t]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t))
+            : 0ull;
+    s_key[t] = bitonic32_desc_u64(mine, t & 31);
     __syncthreads();
     bool kept = false;
-    if (t < nn && my_depth <= cut) {
-      const unsigned long long mine = s_key[t];
-      const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(s_key);
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // independent accumulators: the loads overlap
-      const int pairs = (nn + 1) / 2;      // s_key[nn] is 0 when nn is odd
-      int j = 0;
-#pragma unroll 4
-      for (; j + 2 <= pairs; j += 2) {
-        const ulonglong2 x = k2[j], y = k2[j + 1];
-        r0 += x.x > mine;
-        r1 += x.y > mine;
-        r2 += y.x > mine;
-        r3 += y.y > mine;
+    if (mine != 0ull) {
+      const int nw = (nn + 31) >> 5;  // warps holding candidates
+      int rank = 0;
+#pragma unroll
+      for (int w = 0; w < AT / 32; ++w) {
+        if (w < nw) {
+          const unsigned long long* L = s_key + 32 * w;  // descending; zeros last
+          int lo = 0;
+#pragma unroll
+          for (int step = 16; step > 0; step >>= 1)   // lo = number of keys above `mine`
+            if (L[lo + step - 1] > mine) lo += step;
+          rank += lo + (L[lo] > mine ? 1 : 0);
+        }
       }
-      for (; j < pairs; ++j) {
-        const ulonglong2 x = k2[j];
-        r0 += x.x > mine;
-        r1 += x.y > mine;
-      }
-      kept = r0 + r1 + r2 + r3 < D;
+      kept = rank < D;
     }
     const int pre = block_excl_count(kept, s_warp, n_draft);
     if (t < MAX_DRAFT) s_slot[t] = kept ? 1 + pre : -1;
@@ -255,7 +266,6 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
       // replaced children]; with no candidate there it keeps its draft token,
       // so every request verifies the same number of slots.
       const int used = 1 + n_draft;
-      const int maxpos = s_maxdepth + 1;
       const int nrep_local = (t >= 1 && t < used) ? o_rep[t] : 0;
       // rank of a replaced slot among its parent's replaced children (slot
       // order): lanes of one warp with the same parent match, and warp 1 adds
@@ -268,10 +278,21 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
         srank = __popc(same & ((1u << (t & 31)) - 1u));
         if (t < 32 && rep_me && (same >> t) == 1u) s_cnt0[pkey] = __popc(same);  // the group's last lane
       }
+      // rounds of gathers by chain depth (the replaced slots on the path from
+      // the slot up to its first kept ancestor): a chain's first slot reads
+      // its kept parent's token, so every chain starts in round 1 whatever
+      // its level, and round r needs only round r - 1's results
+      int cdepth = 0;
+      if (rep_me) {
+        cdepth = 1;
+        for (int p = o_par[t]; p >= 1 && o_rep[p]; p = o_par[p]) ++cdepth;
+        atomicMax(&s_chain, cdepth);
+      }
       __syncthreads();
       if (t >= 32 && rep_me) srank += s_cnt0[pkey];
-      for (int level = 1; level <= maxpos; ++level) {
-        if (t >= 1 && t < used && o_pos[t] == level && o_rep[t]) {
+      const int rounds = s_chain;
+      for (int level = 1; level <= rounds; ++level) {
+        if (t >= 1 && t < used && cdepth == level) {
           const int p = o_par[t];
           const int32_t ptok = o_tok[p];
           int32_t tk = -1;
