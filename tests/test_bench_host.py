@@ -150,3 +150,27 @@ def test_hit_rate_and_populated_rows():
     C = np.full((5, 8), -1, np.int32)
     C[[1, 3], :] = 7
     assert b_.populated_rows(C) == 2
+
+
+def test_prune_histogram_and_cpu_baseline_entry():
+    """The prune-depth histogram counts each request-step's info[0] (fired
+    checkpoint layer, or the kept block prefix in tail mode; none in static
+    mode), and the CPU-baseline object reports the all-cores figure with the
+    one-core figure beside it."""
+    import numpy as np
+
+    import workloads as W
+    b_ = _bench()
+    infos = [np.array([[-1, 60, 0, 61], [1, 24, 30, 55]], np.int32), np.array([[-1, 60, 0, 61], [5, 40, 12, 53]])]
+    h = b_.prune_histogram(W.MODE_CHECKPOINT, infos)
+    assert h == {"key": "fired_layer", "counts": {"-1": 2, "1": 1, "5": 1}}
+    assert b_.prune_histogram(W.MODE_TAIL, infos)["key"] == "kept_prefix"
+    assert b_.prune_histogram(W.MODE_STATIC, infos) is None
+    det = {"steps": 4, "requests": 16, "threads": 8, "one_core": 2.0, "all_cores": 12.5, "one_core_s": 2.0,
+           "all_cores_s": 0.32, "warm_s": None, "warm_rows": 0}
+    e = b_.cpu_baseline_entry(det, W.WORKLOADS[2])
+    assert e["value"] == 12.5 and e["cores"] == 8 and e["kind"] == "oracle"
+    assert e["one_core"] == {"value": 2.0, "unit": "steps/s", "cores": 1, "timed_s": 2.0}
+    assert "warm_start" not in e
+    det.update(warm_s=1.25, warm_rows=1280)
+    assert b_.cpu_baseline_entry(det, W.WORKLOADS[1])["warm_start"]["rows"] == 1280
