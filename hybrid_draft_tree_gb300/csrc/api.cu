@@ -27,7 +27,7 @@ struct graft_handle {
   bool tma_ready = false;   // the TMA scan's shared-memory opt-in succeeded
   int32_t* C = nullptr;           // [V][8]
   int32_t* winner = nullptr;      // [V]
-  int32_t* tpl = nullptr;         // [3][tpl_len]: parent, rank, depth
+  int32_t* tpl = nullptr;         // [3][tpl_len]: parent, rank, depth; then [tpl_len + 1]: depth maxima of prefixes
   int tpl_len = 0;
   unsigned long long* part = nullptr;  // [rows][MAX_SPLIT][8]
   int32_t* row_ticket = nullptr;  // [rows]
@@ -248,7 +248,7 @@ int graft_init(const graft_config* cfg, graft_handle** out) {
   const size_t rows = (size_t)cfg->max_batch * h->S;
   e = dalloc(&h->C, V * graft::K);
   if (e == cudaSuccess) e = dalloc(&h->winner, V);
-  if (e == cudaSuccess) e = dalloc(&h->tpl, 3 * (size_t)(h->tpl_len > 0 ? h->tpl_len : 1));
+  if (e == cudaSuccess) e = dalloc(&h->tpl, 4 * (size_t)h->tpl_len + 1);
   if (e == cudaSuccess) e = dalloc(&h->part, rows * graft::MAX_SPLIT * graft::K);
   if (e == cudaSuccess) e = dalloc(&h->row_ticket, rows);
   if (e == cudaSuccess) e = dalloc(&h->req_ticket, (size_t)cfg->max_batch);
@@ -276,10 +276,13 @@ int graft_init(const graft_config* cfg, graft_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(h->req_ticket, 0, cfg->max_batch * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->count, 0, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(uint32_t));
-  if (e == cudaSuccess && h->tpl_len > 0) {
+  if (e == cudaSuccess) {
     std::vector<int32_t> all(tp);
     all.insert(all.end(), tr.begin(), tr.end());
     all.insert(all.end(), td.begin(), td.end());
+    int32_t m = 0;  // depth maxima of the template's prefixes: the gather rounds a retrieval of R entries takes
+    all.push_back(0);
+    for (int32_t d : td) all.push_back(m = std::max(m, d));
     e = cudaMemcpy(h->tpl, all.data(), all.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -376,6 +379,7 @@ graft::AssembleArgs assemble_args(const graft_handle* h, int32_t batch, int32_t 
   a.tpl.parent = h->tpl;
   a.tpl.rank = h->tpl + h->tpl_len;
   a.tpl.depth = h->tpl + 2 * h->tpl_len;
+  a.tpl.maxdepth = h->tpl + 3 * h->tpl_len;
   a.tpl.len = h->tpl_len;
   a.err = h->err;
   return a;

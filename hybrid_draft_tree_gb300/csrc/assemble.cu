@@ -335,8 +335,7 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
     const int jd = mine ? a.tpl.depth[j] : 0;
     const int jq = mine ? a.tpl.parent[j] : -1;
     const int jr = mine ? a.tpl.rank[j] : 0;
-    int maxd = 0;
-    for (int q = 0; q < R; ++q) maxd = max(maxd, a.tpl.depth[q]);
+    int maxd = a.tpl.maxdepth[R];  // the gather rounds
     if (a.rtok_in) {
       // incremental drafting: graft_retrieve gathered the entries already
       if (mine) {
@@ -483,8 +482,7 @@ __global__ __launch_bounds__(MAX_S) void k_retrieve(AssembleArgs a, const int32_
   const int jq = mine ? a.tpl.parent[j] : -1;
   const int jr = mine ? a.tpl.rank[j] : 0;
   s_rtok[j] = -1;
-  int maxd = 0;
-  for (int q = 0; q < R; ++q) maxd = max(maxd, a.tpl.depth[q]);
+  const int maxd = a.tpl.maxdepth[R];  // the gather rounds
   __syncthreads();
   for (int level = 1; level <= maxd; ++level) {
     if (mine && jd == level) {

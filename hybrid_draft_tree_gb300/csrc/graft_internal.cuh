@@ -16,11 +16,13 @@ constexpr int TWO_PASS_MAX_ROWS = 4096;   // verified rows per call on the two-p
 constexpr int TWO_PASS_MAX_UNITS = 1024;  // 512-byte units per row on the two-pass scan (512 KB rows)
 constexpr int WARM_TWO_PASS_ROWS = 4096;  // warm-up rows per call on the two-pass scan (the rest: single pass)
 
-// Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth.
+// Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth;
+// maxdepth[R] = the largest depth among entries 0 .. R-1 (maxdepth[0] = 0).
 struct TemplateDev {
   const int32_t* parent;
   const int32_t* rank;
   const int32_t* depth;
+  const int32_t* maxdepth;
   int32_t len;
 };
 

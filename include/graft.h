@@ -119,8 +119,10 @@ int graft_destroy(graft_handle* h);
 /* Warm-up bulk load (article §六): for n = 0..n_rows-1 in order,
  *   C[d_tokens[n]] <- top-8 ids of logits row n  (value descending, id ascending),
  * so the last occurrence of a token wins.  d_logits row n starts at element
- * n * row_stride (row_stride >= V).  Rows whose token recurs later are not read.
- * Queues four kernels; no host synchronisation. */
+ * n * row_stride (row_stride >= V).  Rows whose token recurs later are not read:
+ * the last occurrences are listed on the device, the first 4096 of them (on
+ * 16-byte aligned rows) take the two-pass scan, any others the single-pass
+ * scan.  Queues five or six kernels; no host synchronisation. */
 int graft_warmup(graft_handle* h, const int32_t* d_tokens, const void* d_logits, int64_t n_rows,
                  int64_t row_stride, void* stream);
 
