@@ -278,10 +278,10 @@ __global__ __launch_bounds__(AT) void k_assemble(AssembleArgs a) {
         srank = __popc(same & ((1u << (t & 31)) - 1u));
         if (t < 32 && rep_me && (same >> t) == 1u) s_cnt0[pkey] = __popc(same);  // the group's last lane
       }
-      // rounds of gathers by chain depth (the replaced slots on the path from
+      // gathers in passes by chain depth (the replaced slots on the path from
       // the slot up to its first kept ancestor): a chain's first slot reads
-      // its kept parent's token, so every chain starts in round 1 whatever
-      // its level, and round r needs only round r - 1's results
+      // its kept parent's token, so every chain starts in the first pass
+      // whatever its level, and pass r needs only pass r - 1's results
       int cdepth = 0;
       if (rep_me) {
         cdepth = 1;

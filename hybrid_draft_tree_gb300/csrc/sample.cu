@@ -263,11 +263,9 @@ cudaError_t sample_impl(const VerifyArgs& a, cudaStream_t s) {
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   const int bytes = stage_bytes(a.g.V, ES);
   const int staged = bytes <= STAGE_MAX ? 1 : 0;
-  static int opted = 48 * 1024;  // dynamic shared memory allowed so far
-  if (staged && bytes > opted) {
+  if (staged && bytes > 48 * 1024) {  // above the default limit the kernel must opt in (per device: set it each time)
     const cudaError_t e = cudaFuncSetAttribute(k_sample<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    opted = bytes;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.batch * CL);

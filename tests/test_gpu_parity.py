@@ -408,6 +408,15 @@ def test_stochastic_verification_matches_oracle(wid, B, temp):
     _stochastic_case(w, temp, 10, wid * 10 + int(temp * 10))
 
 
+@pytest.mark.parametrize("V,B", [(100003, 2), (330007, 1)])
+def test_stochastic_verification_long_fp32_rows(V, B):
+    """fp32 rows whose eighth per cluster CTA needs more than the default 48 KB
+    of shared memory (the kernel opts in) and more than the 160 KB it stages
+    (the draw then re-reads its chunk from global memory)."""
+    w = W.WORKLOADS[0].scaled(V=V, B=B, draft_sigma=0.75, bias=16.0)   # the planted token dominates each draw
+    _stochastic_case(w, 1.0, 4, V % 97)
+
+
 @pytest.mark.slow
 def test_stochastic_verification_full_size_static():
     """The same on the static workload at full size (16 x 61 rows of 151936).
