@@ -1,16 +1,16 @@
-// Pass 1 of the two-pass verify scan (the default path for 16-byte aligned
-// rows): unit maxima.
+// Pass 1 of the two-pass verify scan (for 16-byte aligned rows): unit
+// maxima.
 //
 // The verify + update pass of a Graft step (popular-science article on arXiv
 // 2605.20104, section 二 third gear) needs the top-8 of every verified slot's
 // logits row.  Selection work on the streaming path costs memory parallelism,
-// so this kernel only streams: a persistent grid reads the valid rows once, in
-// equal contiguous slices, with 16-byte evict-first loads, and writes the
-// maximum of every 512-byte unit (32 lanes x 16 bytes), 1/128 of the bytes
-// read.  No shared state and no barriers on the stream.  Pass 2 (select.cu)
-// then finds each row's top-8 from its unit maxima.  The warm-up (article
-// section 六) runs the same pass over the rows its listing kernel names: the
-// last occurrence of each token.
+// so this kernel only streams: a persistent grid reads the valid rows once,
+// in equal contiguous slices of units, with 16-byte evict-first loads, and
+// writes the maximum of every 512-byte unit (32 lanes x 16 bytes), 1/128 of
+// the bytes read.  No shared state and no barriers on the stream.
+// Pass 2 (select.cu) then finds each row's top-8 from its unit maxima.  The
+// warm-up (article section 六) runs the same pass over the rows its listing
+// kernel names: the last occurrence of each token.
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -30,33 +30,30 @@ __device__ __forceinline__ uint4 neg_inf_vec(int dt) {
   return make_uint4(w, w, w, w);
 }
 
-// LIST = false: the valid rows of the verified trees (token in [0, V)), unit
-// records stored by row.  LIST = true (the warm-up): the first min(*count,
-// cap) rows named by `list`, unit records stored by list position.
-// TOP2 = true: besides its maximum, each unit records its second largest
-// element (the largest of the others) and the position of its maximum in the
-// unit (the lowest on ties), so pass 2 can take a unit with one element at or
-// above its threshold without reading the unit again.
-template <int DT, bool LIST, bool TOP2>
-__global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a, const int32_t* list, const int32_t* count, int cap) {
-  __shared__ int warpsum[UW];
-  __shared__ int rowlist[UMAXROWS];
-  grid_dependents_launch();  // pass 2 may be scheduled as SMs free up; it waits for this grid's results
-  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const ScanGeom& g = a.g;
-  const int rows = LIST ? 0 : a.batch * a.S;
-  const int64_t nslot = g.nslot;
-  const int64_t upr = a.upr;
+// This CTA's share: units [u0, u1) of the rows' NU = rows * upr units, which
+// fall in compacted rows k0 .. klast (rowlist[k - k0] = the row behind k).
+struct Slice {
+  int64_t u0, u1, k0, klast;
+  bool live;  // false: nothing to stream here (the whole CTA agrees)
+};
 
-  // compact the valid rows (same result in every CTA)
+// Compacts the rows and fills `rowlist` for this CTA's slice (ends with a
+// CTA barrier).  LIST = false: the valid tree rows.  LIST = true: the first
+// min(*count, cap) entries of `list`.  warpsum: UW ints of shared memory.
+template <bool LIST>
+__device__ __forceinline__ Slice compact_rows(const VerifyArgs& a, const int32_t* list, const int32_t* count, int cap,
+                                              int* rowlist, int* warpsum) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rows = LIST ? 0 : a.batch * a.S;
+  const int V = a.g.V;
+  const int64_t upr = a.upr;
   const int per = (rows + UT - 1) / UT;
   const int r0 = min(tid * per, rows), r1 = min(r0 + per, rows);
   int cnt = 0;
   for (int r = r0; r < r1; ++r) {
     const int32_t t = a.tree_tok[r];
-    cnt += (t >= 0 && t < g.V);
-    if (t >= g.V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
+    cnt += (t >= 0 && t < V);
+    if (t >= V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
   }
   int incl = cnt;
 #pragma unroll
@@ -74,98 +71,169 @@ __global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a, const int32_t* lis
     total += x;
   }
   if (LIST) total = min(__ldcg(count), cap);
+  Slice s{0, 0, 0, -1, false};
   const int64_t NU = (int64_t)total * upr;
-  if (NU == 0) return;
   const int Ge = (int)min((int64_t)gridDim.x, NU);
   const int c = blockIdx.x;
-  if (c >= Ge) return;
-  const int64_t u0 = (int64_t)c * NU / Ge, u1 = (int64_t)(c + 1) * NU / Ge;
-  const int64_t k0 = u0 / upr, klast = (u1 - 1) / upr;
-  if (klast - k0 + 1 > UMAXROWS) {  // the host keeps rows <= (UMAXROWS - 2) * grid
-    if (tid == 0) atomicOr(a.err, GRAFT_ERR_TREE);
-    return;
+  if (NU > 0 && c < Ge) {
+    s.u0 = (int64_t)c * NU / Ge;
+    s.u1 = (int64_t)(c + 1) * NU / Ge;
+    s.k0 = s.u0 / upr;
+    s.klast = (s.u1 - 1) / upr;
+    s.live = true;
+    if (s.klast - s.k0 + 1 > UMAXROWS) {  // the host keeps rows <= (UMAXROWS - 2) * grid
+      if (tid == 0) atomicOr(a.err, GRAFT_ERR_TREE);
+      s.live = false;
+    }
   }
-  if (LIST) {
-    for (int64_t k = k0 + tid; k <= klast; k += UT) rowlist[k - k0] = __ldcg(list + k);
-  } else {
-    int64_t vidx = wbase + incl - cnt;
-    for (int r = r0; r < r1; ++r) {
-      const int32_t t = a.tree_tok[r];
-      if (t >= 0 && t < g.V) {
-        if (vidx >= k0 && vidx <= klast) rowlist[vidx - k0] = r;
-        ++vidx;
+  if (s.live) {
+    if (LIST) {
+      for (int64_t k = s.k0 + tid; k <= s.klast; k += UT) rowlist[k - s.k0] = __ldcg(list + k);
+    } else {
+      int64_t vidx = wbase + incl - cnt;
+      for (int r = r0; r < r1; ++r) {
+        const int32_t t = a.tree_tok[r];
+        if (t >= 0 && t < V) {
+          if (vidx >= s.k0 && vidx <= s.klast) rowlist[vidx - s.k0] = r;
+          ++vidx;
+        }
       }
     }
   }
   __syncthreads();
+  return s;
+}
 
-  for (int64_t k = k0; k <= klast; ++k) {
-    const int row = rowlist[k - k0];
-    const int64_t ulo = max(u0, k * upr) - k * upr, uhi = min(u1, (k + 1) * upr) - k * upr;
-    const uint4* rowv = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(a.logits) +
-                                                       (size_t)row * (size_t)g.stride * ES);
-    float* um = a.umax + (size_t)(LIST ? k : row) * a.ups;
-    float* us = TOP2 ? a.usec + (size_t)(LIST ? k : row) * a.ups : nullptr;
-    uint8_t* up = TOP2 ? a.upos + (size_t)(LIST ? k : row) * a.ups : nullptr;
-    for (int64_t ub = ulo + (int64_t)warp * UNV; ub < uhi; ub += (int64_t)UW * UNV) {
-      Vec16<DT> v[UNV];
-      if (ub + UNV <= uhi && (ub + UNV) * 32 <= nslot) {
-#pragma unroll
-        for (int kk = 0; kk < UNV; ++kk) v[kk].r = __ldcs(rowv + (ub + kk) * 32 + lane);
+// Streams this CTA's slice.  The slice's units are dealt to the warps in
+// groups of UNV as one flat sequence, across row boundaries: warp w takes
+// groups w, w + UW, ..., so the warps' shares differ by one group at most
+// (a loop per row would give each warp its own remainder at every row end).
+// A group inside one row is read with straight loads; a group that crosses a
+// row end (or the slice end) locates each unit on its own.  Unit records go
+// to row `row` (LIST = false) or list position k (LIST = true) of a.umax
+// (and, with TOP2, a.usec / a.upos: besides its maximum, each unit records
+// its second largest element, the largest of the others, and the position of
+// its maximum in the unit, the lowest on ties, so pass 2 can take a unit with
+// one element at or above its threshold without reading the unit again).
+template <int DT, bool LIST, bool TOP2>
+__device__ __forceinline__ void stream_units(const VerifyArgs& a, const Slice& sl, const int* rowlist, int warp,
+                                             int lane) {
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  const ScanGeom& g = a.g;
+  const int64_t nslot = g.nslot;
+  const int64_t upr = a.upr;
+  const char* base = reinterpret_cast<const char*>(a.logits);
+  const size_t rstride = (size_t)g.stride * ES;
+  const int64_t nu = sl.u1 - sl.u0;
+  const int upr32 = a.upr;  // <= TWO_PASS_MAX_UNITS
+  // the group's first unit as (compacted row k, unit j of that row), walked
+  // forward from one division
+  int64_t k = (sl.u0 + (int64_t)warp * UNV) / upr;
+  int j = (int)(sl.u0 + (int64_t)warp * UNV - k * upr);
+  for (int64_t g0 = (int64_t)warp * UNV; g0 < nu; g0 += (int64_t)UW * UNV) {
+    const bool one_row = j + UNV <= upr32 && g0 + UNV <= nu;
+    const int row0 = rowlist[k - sl.k0];
+    // unit kk of the group: its compacted row kr, its row, its index jj in the row
+    auto locate = [&](int kk, int64_t& kr, int& row, int64_t& jj) {
+      if (one_row) {
+        kr = k; row = row0; jj = j + kk;
       } else {
-#pragma unroll
-        for (int kk = 0; kk < UNV; ++kk) {
-          const int64_t s = (ub + kk) * 32 + lane;
-          v[kk].r = (ub + kk < uhi && s < nslot) ? __ldcs(rowv + s) : neg_inf_vec(DT);
-        }
+        kr = min(k + (j + kk) / upr32, sl.klast);  // units past the slice end are masked out
+        jj = (j + kk) % upr32;
+        row = rowlist[kr - sl.k0];
       }
-      if (!TOP2) {
+    };
+    Vec16<DT> v[UNV];
+    if (one_row && (j + UNV) * 32 <= nslot) {
+      const uint4* rowv = reinterpret_cast<const uint4*>(base + (size_t)row0 * rstride);
 #pragma unroll
-        for (int kk = 0; kk < UNV; ++kk) {
-          const float m = v[kk].vmax();
-          if (m != m) atomicOr(a.err, GRAFT_ERR_NAN);
-          const int32_t mi = __reduce_max_sync(FULL, ord_int(m));
-          if (lane == kk && ub + kk < uhi) um[ub + kk] = from_ord_int(mi);
-        }
-      } else {
-        // per unit: the maximum (warp reduction), the lowest lane holding it,
-        // the largest of everything else (that lane's second, the other
-        // lanes' maxima), and that lane's 16 bytes, handed to lane kk
-        float mk = 0.f, sk = 0.f;
-        int wk = 0;
-        Vec16<DT> ck;
-        ck.r = make_uint4(0u, 0u, 0u, 0u);
+      for (int kk = 0; kk < UNV; ++kk) v[kk].r = __ldcs(rowv + (j + kk) * 32 + lane);
+    } else {
 #pragma unroll
-        for (int kk = 0; kk < UNV; ++kk) {
-          float m1, m2;
-          v[kk].top2(m1, m2);
-          if (m1 != m1) atomicOr(a.err, GRAFT_ERR_NAN);
-          const int32_t k1 = ord_int(m1);
-          const int32_t mi = __reduce_max_sync(FULL, k1);
-          const unsigned wm = __ballot_sync(FULL, k1 == mi);
-          const int w = __ffs(wm) - 1;
-          const int32_t xi = __reduce_max_sync(FULL, lane == w ? ord_int(m2) : k1);
-          uint4 r;
-          r.x = __shfl_sync(FULL, v[kk].r.x, w);
-          r.y = __shfl_sync(FULL, v[kk].r.y, w);
-          r.z = __shfl_sync(FULL, v[kk].r.z, w);
-          r.w = __shfl_sync(FULL, v[kk].r.w, w);
-          if (lane == kk) {
-            mk = from_ord_int(mi);
-            sk = (wm & (wm - 1u)) ? mk : from_ord_int(xi);  // the maximum held by two lanes: it repeats
-            wk = w;
-            ck.r = r;
-          }
-        }
-        if (lane < UNV && ub + lane < uhi) {
-          const unsigned em = ck.ge_mask(mk);  // the maximum's elements in lane wk's 16 bytes
-          um[ub + lane] = mk;
-          us[ub + lane] = sk;
-          up[ub + lane] = (uint8_t)(wk * Vec16<DT>::EPL + (em ? __ffs(em) - 1 : 0));
-        }
+      for (int kk = 0; kk < UNV; ++kk) {
+        int64_t kr, jj;
+        int row;
+        locate(kk, kr, row, jj);
+        const int64_t s = jj * 32 + lane;
+        v[kk].r = (g0 + kk < nu && s < nslot)
+                      ? __ldcs(reinterpret_cast<const uint4*>(base + (size_t)row * rstride) + s)
+                      : neg_inf_vec(DT);
       }
     }
+    // lane kk stores unit kk's records
+    int64_t kr_l = 0, jj_l = 0;
+    int row_l = 0;
+    const bool st = lane < UNV && g0 + lane < nu;
+    if (st) locate(lane, kr_l, row_l, jj_l);
+    const size_t rec = (size_t)(LIST ? kr_l : row_l) * a.ups + jj_l;
+    if (!TOP2) {
+      float mk = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < UNV; ++kk) {
+        const float m = v[kk].vmax();
+        if (m != m) atomicOr(a.err, GRAFT_ERR_NAN);
+        const int32_t mi = __reduce_max_sync(FULL, ord_int(m));
+        if (lane == kk) mk = from_ord_int(mi);
+      }
+      if (st) a.umax[rec] = mk;
+    } else {
+      // per unit: the maximum (warp reduction), the lowest lane holding it,
+      // the largest of everything else (that lane's second, the other
+      // lanes' maxima), and that lane's 16 bytes, handed to lane kk
+      float mk = 0.f, sk = 0.f;
+      int wk = 0;
+      Vec16<DT> ck;
+      ck.r = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int kk = 0; kk < UNV; ++kk) {
+        float m1, m2;
+        v[kk].top2(m1, m2);
+        if (m1 != m1) atomicOr(a.err, GRAFT_ERR_NAN);
+        const int32_t k1 = ord_int(m1);
+        const int32_t mi = __reduce_max_sync(FULL, k1);
+        const unsigned wm = __ballot_sync(FULL, k1 == mi);
+        const int w = __ffs(wm) - 1;
+        const int32_t xi = __reduce_max_sync(FULL, lane == w ? ord_int(m2) : k1);
+        uint4 r;
+        r.x = __shfl_sync(FULL, v[kk].r.x, w);
+        r.y = __shfl_sync(FULL, v[kk].r.y, w);
+        r.z = __shfl_sync(FULL, v[kk].r.z, w);
+        r.w = __shfl_sync(FULL, v[kk].r.w, w);
+        if (lane == kk) {
+          mk = from_ord_int(mi);
+          sk = (wm & (wm - 1u)) ? mk : from_ord_int(xi);  // the maximum held by two lanes: it repeats
+          wk = w;
+          ck.r = r;
+        }
+      }
+      if (st) {
+        const unsigned em = ck.ge_mask(mk);  // the maximum's elements in lane wk's 16 bytes
+        a.umax[rec] = mk;
+        a.usec[rec] = sk;
+        a.upos[rec] = (uint8_t)(wk * Vec16<DT>::EPL + (em ? __ffs(em) - 1 : 0));
+      }
+    }
+    j += UW * UNV;
+    while (j >= upr32) {
+      j -= upr32;
+      ++k;
+    }
   }
+}
+
+
+// LIST = false: the valid rows of the verified trees, unit records stored by
+// row.  LIST = true (the warm-up): the first min(*count, cap) rows named by
+// `list`, unit records stored by list position.  TOP2: units also record
+// their second largest element and the position of their maximum.
+template <int DT, bool LIST, bool TOP2>
+__global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a, const int32_t* list, const int32_t* count, int cap) {
+  __shared__ int warpsum[UW];
+  __shared__ int rowlist[UMAXROWS];
+  grid_dependents_launch();  // pass 2 may be scheduled as SMs free up; it waits for this grid's results
+  const Slice sl = compact_rows<LIST>(a, list, count, cap, rowlist, warpsum);
+  if (!sl.live) return;
+  stream_units<DT, LIST, TOP2>(a, sl, rowlist, threadIdx.x >> 5, threadIdx.x & 31);
 }
 
 template <int DT, bool LIST>
