@@ -12,7 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgraft.so")
 OBJDIR = os.path.join(PKG, "_build")
-SOURCES = ("api.cu", "assemble.cu", "scan.cu", "umax.cu", "select.cu", "coverage.cu", "sample.cu", "scan_tma.cu", "noalloc.cu")
+SOURCES = ("api.cu", "assemble.cu", "scan.cu", "umax.cu", "select.cu", "coverage.cu", "sample.cu", "scan_tma.cu", "noalloc.cu",
+           "cluster_select.cu")
 NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
               "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

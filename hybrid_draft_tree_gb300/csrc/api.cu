@@ -174,7 +174,7 @@ int check_cfg(const graft_config* c, graft_handle* h) {
   const int maxn = c->mode == GRAFT_MODE_TAIL ? c->budget : graft::MAX_DRAFT;
   if (c->max_draft_nodes < 0 || c->max_draft_nodes > maxn)
     return fail(h, GRAFT_EINVAL, "max_draft_nodes must be in [0, %d]", maxn);
-  if (c->scan_kernel < 0 || c->scan_kernel > 4) return fail(h, GRAFT_EINVAL, "scan_kernel must be in [0, 4]");
+  if (c->scan_kernel < 0 || c->scan_kernel > 5) return fail(h, GRAFT_EINVAL, "scan_kernel must be in [0, 5]");
   return GRAFT_OK;
 }
 
@@ -643,6 +643,10 @@ int verify_impl(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const
   const bool two_pass_fits = a.g.vec && h->umax && a.g.nslot > 0 && a.upr <= h->upr_max &&
                              rows <= graft::two_pass_max_rows(grid2);
   const bool use_tma = tma_fits && c.scan_kernel == 2;
+  // few rows, each staged in a cluster's shared memory: one launch, no reload
+  const int esize = c.logits_dtype == GRAFT_BF16 ? 2 : 4;
+  const bool use_cluster = graft::cluster_select_fits((int)rows, c.vocab, esize) &&
+                           (c.scan_kernel == 5 || (c.scan_kernel == 0 && graft::cluster_select_auto((int)rows, c.vocab, esize)));
   const bool use_two_pass = !use_tma && two_pass_fits && (c.scan_kernel == 0 || c.scan_kernel >= 3);
   const int grid = h->num_sms * graft::verify_ctas_per_sm();
   if (!use_tma && !use_two_pass && rows > graft::verify_max_rows(grid))
@@ -654,6 +658,15 @@ int verify_impl(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const
   a.top2 = (c.scan_kernel == 4 && h->usec && h->upos) ? 1 : 0;
   a.wait_polls = h->wait_polls;  // measured: the records slow pass 1 by more than they save
   cudaError_t e;
+  if (use_cluster) {
+    {
+      ProfScope ps(h, (cudaStream_t)stream, "k_cluster_select");
+      e = graft::launch_cluster_select(a, c.logits_dtype, h->C, (cudaStream_t)stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "graft_verify_update cluster launch");
+    h->last_launches = 1;
+    return sample ? launch_sample_step(h, a, stream) : GRAFT_OK;
+  }
   if (use_two_pass) {
     {
       ProfScope ps(h, (cudaStream_t)stream, "k_umax");

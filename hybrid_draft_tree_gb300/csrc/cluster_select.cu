@@ -1,0 +1,292 @@
+// The verify + update pass of a Graft step (popular-science article on arXiv
+// 2605.20104, section 二 third gear) for small steps: few verified rows, each
+// small enough to sit in the shared memory of one thread-block cluster.
+//
+// With few rows (a single request's tree: 61 rows) the two-pass scan is all
+// latency: two launches, a stream of a few MB, then pass 2's chain of unit
+// maxima, a candidate reload and the request ticket.  Here one cluster of CL
+// CTAs takes one row: each CTA stages its range of the row in shared memory
+// (the row's only read), keeping every thread's maximum, and takes T, the 8th
+// largest of its threads' maxima.  Eight distinct elements of the range reach
+// T (each is its thread's maximum), so every element of the range's top-8 is
+// >= T; the CTA lists its elements >= T from shared memory and sorts them
+// into its exact top-8 (value desc, id asc).  The row's top-8 is among the 8
+// CTAs' top-8s: CTA 0 of the cluster merges the 64 keys through distributed
+// shared memory, writes the row's share of the update and, for the row
+// completing a request, runs its acceptance from the request's tree arrays,
+// which it staged in shared memory at the start.  A range with fewer than 8
+// finite thread maxima, or with more than RCAP elements >= T (heavy ties),
+// takes its exact top-8 by repeated maxima over the staged range instead.
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+
+#include <climits>
+
+#include "graft_internal.cuh"
+#include "row_softmax.cuh"
+#include "scan_common.cuh"
+
+namespace graft {
+namespace {
+using namespace scan;
+namespace cg = cooperative_groups;
+using softmax::CL;
+
+constexpr int RT = 256;     // threads per CTA
+constexpr int RW = RT / 32;
+constexpr int RCAP = 128;   // elements >= T one CTA may list before its exact pass
+constexpr int UNR = 8;      // 16-byte loads in flight per thread while staging
+
+// The 8 largest of the 32 lanes' x (ordered ints, with multiplicity; INT_MIN
+// past the end): lane r < 8 returns the r-th.
+__device__ __forceinline__ int32_t top8_of_lanes(int32_t x, int lane) {
+  int32_t out = INT_MIN;
+#pragma unroll
+  for (int r = 0; r < K; ++r) {
+    const int32_t m = __reduce_max_sync(FULL, x);
+    const int owner = __ffs(__ballot_sync(FULL, x == m)) - 1;
+    if (lane == owner) x = INT_MIN;
+    if (lane == r) out = m;
+  }
+  return out;
+}
+
+// The same over 64 values, two per lane (x0, x1).
+__device__ __forceinline__ int32_t top8_of_pairs(int32_t x0, int32_t x1, int lane) {
+  int32_t out = INT_MIN;
+#pragma unroll
+  for (int r = 0; r < K; ++r) {
+    const int32_t m = __reduce_max_sync(FULL, max(x0, x1));
+    const int owner = __ffs(__ballot_sync(FULL, x0 == m || x1 == m)) - 1;
+    if (lane == owner) {
+      if (x0 == m) x0 = INT_MIN;
+      else x1 = INT_MIN;
+    }
+    if (lane == r) out = m;
+  }
+  return out;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C) {
+  extern __shared__ __align__(16) char stage[];
+  __shared__ int32_t stok[CLUSTER_MAX_ROWS];
+  __shared__ uint64_t smask[MAX_S];  // CTA 0: the tree arrays of this row's request
+  __shared__ int32_t spos[MAX_S];
+  __shared__ int8_t spar[MAX_S];
+  __shared__ int32_t wtop[RW][K];    // each warp's 8 largest thread maxima
+  __shared__ u64 s_list[RCAP];       // this CTA's elements >= T
+  __shared__ u64 s_top[K];           // this CTA's top-8 keys (read by CTA 0)
+  __shared__ u64 s_wbest[RW];
+  __shared__ int s_nc, s_T;
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  constexpr int EPL = Vec16<DT>::EPL;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int row = blockIdx.x / CL;
+  const int rows = a.batch * a.S;  // the host keeps rows <= CLUSTER_MAX_ROWS
+  const int V = a.g.V;
+  grid_dependents_launch();  // the stochastic walk may be scheduled as SMs free up; it waits for this grid
+
+  for (int r = t; r < rows; r += RT) stok[r] = __ldcg(a.tree_tok + r);
+  const int b = row / a.S;
+  if (rank == 0)
+    for (int i = t; i < a.S; i += RT) {
+      const size_t q = (size_t)b * a.S + i;
+      spar[i] = __ldcg(a.tree_parent + q);
+      spos[i] = __ldcg(a.tree_pos + q);
+      smask[i] = __ldcg(reinterpret_cast<const unsigned long long*>(a.tree_mask) + q);
+    }
+  if (t == 0) s_nc = 0;
+  __syncthreads();
+  const int32_t tok = stok[row];
+  // a request with no valid slot has no row to finish it: its first row's cluster does
+  if (rank == 0 && warp == 0 && !a.sample && row == b * a.S && request_valid(a, stok, b, lane) == 0)
+    accept_request(a, b, lane, stok);
+  if (rank == 0 && t == 0 && tok >= V) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
+  if (tok < 0 || tok >= V) return;  // the whole cluster (one row) leaves before any exchange
+
+  // 1. stage this CTA's range of the row; every thread keeps its chunk's maximum
+  const bool vec = a.g.vec;
+  const int epl = vec ? EPL : 1;
+  int lo, hi;
+  softmax::cta_range(V, epl, rank, lo, hi);
+  int ch = (hi - lo + RT - 1) / RT;
+  ch = (ch + epl - 1) / epl * epl;
+  const int v0 = min(lo + t * ch, hi), v1 = min(v0 + ch, hi);
+  const char* rowp = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.g.stride * ES;
+  float tm = -INFINITY;  // NaN elements are flagged and left out
+  bool nan = false;
+  const int nvec = vec ? (v1 - v0) / EPL : 0;  // whole vectors (only the row's last chunk has a rest)
+  const uint4* sv = reinterpret_cast<const uint4*>(stage + (size_t)(v0 - lo) * ES);
+  if (nvec > 0) {
+    const uint4* p = reinterpret_cast<const uint4*>(rowp) + v0 / EPL;
+    uint4* sp = reinterpret_cast<uint4*>(stage + (size_t)(v0 - lo) * ES);
+    for (int base = 0; base < nvec; base += UNR) {
+      Vec16<DT> x[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u)
+        if (base + u < nvec) x[u].r = __ldcs(p + base + u);
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        if (base + u >= nvec) break;
+        sp[base + u] = x[u].r;
+        const float m = x[u].vmax();
+        if (m != m) {
+          nan = true;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) tm = fmaxf(tm, x[u].elem(e));  // fmaxf drops NaN
+        } else {
+          tm = fmaxf(tm, m);
+        }
+      }
+    }
+  }
+  for (int v = v0 + nvec * EPL; v < v1; ++v) {
+    const float x = load_scalar<DT>(rowp, v);
+    softmax::store_elem<DT>(stage, v - lo, x);
+    if (x != x) nan = true;
+    tm = fmaxf(tm, x);
+  }
+  if (nan) atomicOr(a.err, GRAFT_ERR_NAN);
+
+  // 2. T = the 8th largest of this CTA's thread maxima
+  {
+    const int32_t w8 = top8_of_lanes(ord_int(tm), lane);
+    if (lane < K) wtop[warp][lane] = w8;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int32_t c8 = top8_of_pairs(wtop[lane >> 3][lane & 7], wtop[4 + (lane >> 3)][lane & 7], lane);
+    if (lane == K - 1) s_T = c8;
+  }
+  __syncthreads();
+  const float T = from_ord_int(s_T);
+  bool exact = !(s_T != INT_MIN && T > -INFINITY);  // fewer than 8 finite thread maxima
+
+  // 3. this CTA's elements >= T, from shared memory, then its top-8
+  if (!exact) {
+    for (int q = 0; q < nvec; ++q) {
+      Vec16<DT> x;
+      x.r = sv[q];
+      unsigned m = x.ge_mask(T);
+      while (m) {
+        const int e = __ffs(m) - 1;
+        m &= m - 1;
+        const int pos = atomicAdd(&s_nc, 1);
+        if (pos < RCAP) s_list[pos] = make_key(x.elem(e), v0 + q * EPL + e);
+      }
+    }
+    for (int v = v0 + nvec * EPL; v < v1; ++v) {
+      const float x = softmax::stage_elem<DT>(stage, v - lo);
+      if (x >= T) {
+        const int pos = atomicAdd(&s_nc, 1);
+        if (pos < RCAP) s_list[pos] = make_key(x, v);
+      }
+    }
+    __syncthreads();
+    exact = s_nc > RCAP;  // heavy ties: the list overflowed
+    if (!exact && warp == 0) {
+      const u64 top = warp_merge(0ull, s_list, s_nc, lane);
+      if (lane < K) s_top[lane] = top;
+    }
+  }
+  if (exact) {
+    // exact pass: 8 rounds of block-wide maxima below the last
+    u64 prev = ~0ull;
+    for (int r = 0; r < K; ++r) {
+      u64 best = 0ull;
+      for (int v = v0; v < v1; ++v) {
+        const u64 key = make_key(softmax::stage_elem<DT>(stage, v - lo), v);
+        if (key < prev && key > best) best = key;
+      }
+      best = warp_max_u64(best);
+      if (lane == 0) s_wbest[warp] = best;
+      __syncthreads();
+      u64 cb = lane < RW ? s_wbest[lane] : 0ull;
+      cb = warp_max_u64(cb);
+      if (t == 0) s_top[r] = cb;  // 0 (no key) once the range runs out
+      prev = cb;
+      __syncthreads();
+    }
+  }
+  cluster.sync();  // every CTA's top-8 is written
+
+  // 4. CTA 0 merges the 8 CTAs' top-8s (lane l reads keys l and l + 32 of the 64)
+  u64 top = 0ull;
+  if (rank == 0 && warp == 0) {
+    const u64 k0 = *cluster.map_shared_rank(&s_top[lane & 7], lane >> 3);
+    const u64 k1 = *cluster.map_shared_rank(&s_top[lane & 7], 4 + (lane >> 3));
+    const u64 hi0 = bitonic32_desc(k0, lane), hi1 = bitonic32_desc(k1, lane);
+    // the top-8 of two descending lists of 32: lanes 0..7 of the first, 8..15 take the second's 0..7
+    const u64 y = __shfl_sync(FULL, hi1, lane & 7);
+    top = bitonic32_desc(lane < K ? hi0 : (lane < 2 * K ? y : 0ull), lane);
+  }
+  cluster.sync();  // CTA 0 has read the keys: the other CTAs may leave
+  if (rank != 0 || warp != 0) return;
+  const int32_t id = key_id(top);
+  if (lane < K) a.topk[(size_t)row * K + lane] = id;
+  // the matrix row of the token: written unless a later row in (request,
+  // slot) order carries the same token
+  bool later = false;
+  for (int r = row + 1 + lane; r < rows; r += 32) later |= stok[r] == tok;
+  later = __any_sync(FULL, later);
+  if (!later && lane < K) st_keep(C + (size_t)tok * K + lane, id, l2_keep_policy());
+  if (a.sample) return;  // stochastic verification accepts in its own kernel
+  // the warp that completes the request's last valid row runs acceptance
+  const int nv = request_valid(a, stok, b, lane);
+  __syncwarp();
+  int tk = 0;
+  if (lane == 0) tk = ticket_acq_rel(&a.req_ticket[b]);
+  tk = __shfl_sync(FULL, tk, 0);
+  if (tk == nv - 1) {
+    if (lane == 0) a.req_ticket[b] = 0;
+    __syncwarp();
+    accept_staged(a, b, lane, stok, spar, spos, smask);
+  }
+}
+
+template <int DT>
+cudaError_t cluster_select_impl(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  const int bytes = softmax::stage_bytes(a.g.V, ES);
+  if (bytes > 48 * 1024) {  // above the default limit the kernel must opt in (per device: set it each time)
+    const cudaError_t e = cudaFuncSetAttribute(k_cluster_select<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.batch * a.S * CL);
+  cfg.blockDim = dim3(RT);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_cluster_select<DT>, a, C);
+}
+
+}  // namespace
+
+bool cluster_select_fits(int rows, int V, int esize) {
+  return rows <= CLUSTER_MAX_ROWS && softmax::stage_bytes(V, esize) <= CLUSTER_STAGE_MAX;
+}
+
+// Measured on GB300 (verify_update, L2 flushed): one request of 61 rows of
+// 32000 fp32 (16 KB per CTA), 15.0-17.0 us against 18.1-19.0 us on the
+// two-pass scan; of 128256 bf16 (32 KB per CTA), 25.1 against 19.6; of
+// 151936 bf16 (38 KB), 20.5 against 20.4; two requests or more, slower (each
+// further ~61 rows adds a wave of clusters).
+bool cluster_select_auto(int rows, int V, int esize) {
+  return rows <= CLUSTER_AUTO_ROWS && softmax::stage_bytes(V, esize) <= CLUSTER_AUTO_STAGE;
+}
+
+cudaError_t launch_cluster_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s) {
+  return dtype == GRAFT_BF16 ? cluster_select_impl<GRAFT_BF16>(a, C, s) : cluster_select_impl<GRAFT_F32>(a, C, s);
+}
+
+}  // namespace graft

@@ -270,6 +270,82 @@ static __device__ void accept_request(const VerifyArgs& a, int b, int lane, cons
   }
 }
 
+// Greedy acceptance of request b (one warp) from tree arrays staged in shared
+// memory (sp/spos/smask indexed by slot): match(i) = slot i is valid and is the
+// root or carries its parent's argmax; accepted(i) <=> mask_i & ~match == 0;
+// the winner is the accepted slot of greatest position (ties: lower slot); its
+// path tokens after the root, then the bonus token argmax(winner), are emitted.
+// The argmax of every slot's row is fetched in one round trip to L2.
+static __device__ __forceinline__ void accept_staged(const VerifyArgs& a, int b, int lane, const int32_t* stok,
+                                           const int8_t* sp, const int32_t* spos, const uint64_t* smask) {
+  const int S = a.S;
+  const size_t base = (size_t)b * S;
+  int32_t tk[2], ps[2], am[2], pp[2];
+  uint64_t mk[2];
+  bool ok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    tk[h] = s < S ? stok[base + s] : -1;  // raw: a token >= V (flagged by pass 1) still counts as a node
+    const bool v = tk[h] >= 0 && tk[h] < a.g.V;
+    am[h] = v ? __ldcg(a.topk + (base + s) * K) : -1;
+    ps[h] = v ? spos[s] : -1;
+    mk[h] = v ? smask[s] : 0ull;
+    pp[h] = v && s > 0 ? (int)sp[s] : -1;
+  }
+  bool mt[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    const int p = pp[h];
+    const int q = p >= 0 ? p : 0;
+    const int32_t pa0 = __shfl_sync(FULL, am[0], q & 31), pa1 = __shfl_sync(FULL, am[1], q & 31);
+    const int32_t ptk0 = __shfl_sync(FULL, tk[0], q & 31), ptk1 = __shfl_sync(FULL, tk[1], q & 31);
+    const int32_t pam = q < 32 ? pa0 : pa1, ptk = q < 32 ? ptk0 : ptk1;
+    ok[h] = false;
+    mt[h] = false;
+    if (tk[h] >= 0 && tk[h] < a.g.V) {
+      if (s == 0) {
+        ok[h] = ps[h] == 0;
+        mt[h] = ok[h];
+      } else {
+        ok[h] = p >= 0 && p < s && ptk >= 0 && ps[h] >= 1 && ps[h] < S;
+        mt[h] = ok[h] && tk[h] == pam;
+      }
+      if (!ok[h]) atomicOr(a.err, GRAFT_ERR_TREE);
+    }
+  }
+  const uint64_t match = (uint64_t)__ballot_sync(FULL, mt[0]) | ((uint64_t)__ballot_sync(FULL, mt[1]) << 32);
+  int wkey = -1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    if (ok[h] && ((mk[h] >> s) & 1ull) && (mk[h] & ~match) == 0ull) wkey = max(wkey, (ps[h] << 8) | (255 - s));
+  }
+  wkey = __reduce_max_sync(FULL, wkey);
+  int32_t* out = a.out_tokens + base;
+  if (wkey < 0) {  // no valid root: nothing accepted, nothing emitted
+    for (int j = lane; j < S; j += 32) out[j] = -1;
+    if (lane == 0) a.accept_len[b] = 0;
+    return;
+  }
+  const int w = 255 - (wkey & 255);
+  const int L = wkey >> 8;
+  const uint64_t mw = smask[w];
+  const int32_t bonus0 = __shfl_sync(FULL, am[0], w & 31), bonus1 = __shfl_sync(FULL, am[1], w & 31);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    if (s > 0 && ok[h] && ((mw >> s) & 1ull) && ps[h] <= L) out[ps[h] - 1] = tk[h];
+  }
+  for (int j = lane; j < S; j += 32)
+    if (j > L) out[j] = -1;
+  if (lane == 0) {
+    out[L] = w < 32 ? bonus0 : bonus1;
+    a.accept_len[b] = L;
+  }
+}
+
 // ---- pieces shared by the row-selection kernels ------------------------------------
 template <int DT>
 static __device__ __noinline__ u64 exact_row(const uint4* rowv, int64_t nslot, const char* rowp, int tail, int lane) {

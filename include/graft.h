@@ -88,14 +88,18 @@ typedef struct {
   float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15) */
   float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4) */
   int32_t max_draft_nodes;/* largest draft tree (<= 256) or block (<= budget) per request */
-  int32_t scan_kernel;    /* verify scan: 0 = automatic (two-pass with unit maxima on 16-byte
-                             aligned rows, else single-pass), 1 = single-pass with a shared
+  int32_t scan_kernel;    /* verify scan: 0 = automatic (cluster per row for up to 64 rows
+                             whose eighth is at most 16 KB, else two-pass with unit maxima on
+                             16-byte aligned rows, else single-pass), 1 = single-pass with a shared
                              running top-8, 2 = TMA-pipelined (aligned rows of >= 32 KB only),
                              3 = two-pass with unit maxima (pass 2 reads every candidate unit
                              again), 4 = two-pass with unit records (maximum, second largest,
                              position of the maximum: pass 2 reads again only units with two
                              elements at or above its threshold, pass 1 does more work per
-                             unit); 3 and 4 take aligned rows only */
+                             unit); 3 and 4 take aligned rows only; 5 = cluster per row (one
+                             thread-block cluster of 8 CTAs stages each row in shared memory and
+                             selects its top-8 on chip, one launch; up to 256 rows whose eighth
+                             fits 200 KB, else as 3) */
   int32_t ablation;       /* checkpoint mode only (article §五 ablations; 0 elsewhere):
                              0 = Graft, 1 = confidence pruning without retrieval (the freed
                              slots stay empty), 2 = fixed split (no checkpoints: the top

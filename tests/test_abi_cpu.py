@@ -99,12 +99,13 @@ def test_config_validation_before_any_device_call():
         for dtype in (g.GRAFT_F32, g.GRAFT_BF16):
             assert init(mode=mode, dtype=dtype) == gb.GRAFT_ECUDA
     assert init(ablation=2, fixed_draft=0, tpl_depth=16, tpl_width=64, scan_kernel=4) == gb.GRAFT_ECUDA
+    assert init(scan_kernel=5) == gb.GRAFT_ECUDA
     assert init(budget=63, max_batch=1000) == gb.GRAFT_ECUDA          # the largest budget and batch * slots
     bad = [dict(vocab=0), dict(topk=4), dict(budget=0), dict(budget=64), dict(max_batch=0), dict(max_batch=1100),
            dict(mode=3), dict(dtype=2), dict(ckpt_draft=(8, 24, 61)), dict(ckpt_depth=(0, -1, 5)),
            dict(tpl_depth=0), dict(tpl_depth=17), dict(tpl_width=0), dict(tpl_width=65), dict(ablation=3),
            dict(ablation=1, mode=g.GRAFT_MODE_STATIC), dict(ablation=2, fixed_draft=61), dict(max_draft_nodes=-1),
-           dict(max_draft_nodes=17, mode=g.GRAFT_MODE_TAIL), dict(scan_kernel=5)]
+           dict(max_draft_nodes=17, mode=g.GRAFT_MODE_TAIL), dict(scan_kernel=6)]
     for kw in bad:
         assert init(**dict(kw)) == gb.GRAFT_EINVAL, kw
 

@@ -199,21 +199,22 @@ def test_slot_provenance(wid, V, B, sigma):
     g.close()
 
 
-@pytest.mark.parametrize("scan_kernel", [1, 2, 3, 4])
+@pytest.mark.parametrize("scan_kernel", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("wid,V,B,sigma,steps", [
     (2, 40000, 16, 2.0, 8),     # static, 80 KB rows: 3 chunks per row, rows split over CTAs
     (4, 24576, 64, 2.0, 6),     # tail, 64 requests x 17 slots
     (0, 16384, 1, 0.75, 20),    # fp32 checkpoint, 64 KB rows, few rows per step
 ])
 def test_lockstep_both_scan_kernels(scan_kernel, wid, V, B, sigma, steps):
-    """The single-pass, TMA-pipelined and two-pass verify scans (unit maxima
-    only, and unit records) on rows of >= 32 KB, closed loop against the
-    oracle."""
+    """The single-pass, TMA-pipelined, two-pass (unit maxima only, and unit
+    records) and cluster-per-row verify scans on rows of >= 32 KB, closed loop
+    against the oracle (the cluster path takes the 61-row case; the others
+    fall back to the two-pass scan)."""
     w = W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=sigma)
     lockstep(w, steps, check_rows=4, scan_kernel=scan_kernel)
 
 
-@pytest.mark.parametrize("scan_kernel", [1, 2, 3, 4])
+@pytest.mark.parametrize("scan_kernel", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
 @pytest.mark.parametrize("V,pad,fn", [(40000, 0, "normal"), (40003, 5, "normal"), (65536, 0, "ties"),
                                       (33000, 0, "constant")])
@@ -417,6 +418,14 @@ def test_stochastic_verification_long_fp32_rows(V, B):
     _stochastic_case(w, 1.0, 4, V % 97)
 
 
+@pytest.mark.parametrize("wid,B", [(0, 2), (2, 1)])
+def test_stochastic_verification_after_the_cluster_verify(wid, B):
+    """Sampling acceptance when the greedy pass is the cluster-per-row verify
+    (it writes the staged top-8s and the matrix, the walk follows it)."""
+    w = W.WORKLOADS[wid].scaled(V=5000, B=B, draft_sigma=0.75, bias=12.0)
+    _stochastic_case(w, 1.0, 8, 40 + wid, scan_kernel=5)
+
+
 @pytest.mark.slow
 def test_stochastic_verification_full_size_static():
     """The same on the static workload at full size (16 x 61 rows of 151936).
@@ -426,9 +435,9 @@ def test_stochastic_verification_full_size_static():
     _stochastic_case(W.WORKLOADS[2].scaled(bias=20.0, hit_rate=1.0), 1.0, 2, 99)
 
 
-def _stochastic_case(w, temp, steps, seed, min_fraction=0.5):
+def _stochastic_case(w, temp, steps, seed, min_fraction=0.5, **cfg):
     from workloads.device_loop import DeviceLoop
-    eng = engine_for(w)
+    eng = engine_for(w, **cfg)
     loop = DeviceLoop(w, eng)
     P = oracle.make_params(w.V, budget=w.budget, mode=w.mode)
     C = oracle.new_matrix(w.V)
@@ -696,6 +705,39 @@ def test_verify_ties_and_candidate_overflow(dtype, fn):
     _verify_case(20000, dtype, 33, 2, fn, seed=11)
 
 
+def _sparse(rng, n, V):
+    """Rows of -inf but for a few finite values: most threads and CTAs see
+    no finite element (fewer than 8 finite maxima: the exact pass)."""
+    v = np.full((n, V), -np.inf, np.float32)
+    k = min(5, V)
+    for r in range(n):
+        v[r, rng.choice(V, k, replace=False)] = rng.normal(size=k)
+    return v
+
+
+@pytest.mark.parametrize("V", [1, 7, 8, 37, 1000, 4099, 40000])
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_cluster_verify_ragged_vocab(V, dtype):
+    """The cluster-per-row verify on tiny and ragged rows: CTAs with empty or
+    partial ranges, a scalar rest after the last whole vector."""
+    _verify_case(V, dtype, 61, 2, _normal, seed=V + 1, scan_kernel=5)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("fn", [_ties, _constant, _sparse])
+def test_cluster_verify_ties_overflow_and_sparse_rows(dtype, fn):
+    """Heavy ties and all-equal rows (a CTA's list overflows: its exact pass)
+    and rows of -inf with a few finite values (no threshold: the exact pass)."""
+    _verify_case(20000, dtype, 33, 2, fn, seed=12, scan_kernel=5)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("pad,off", [(1, 0), (3, 1)])
+def test_cluster_verify_unaligned_rows(dtype, pad, off):
+    """Row starts off 16-byte boundaries: scalar staging."""
+    _verify_case(3001, dtype, 17, 3, _normal, stride_pad=pad, offset_elems=off, seed=pad + 7, scan_kernel=5)
+
+
 def test_batch_zero_is_a_noop():
     g_ = G()
     eng = g_.Graft(g_.graft_default_config(100, 4, 0, W.BF16))
@@ -790,7 +832,7 @@ def test_invalid_arguments_are_rejected():
         eng.check(2, torch.zeros((2, 4), dtype=torch.int16, device="cuda"), torch.ones((2, 4), device="cuda"), -1, ev)
     for mode, kw in ((0, dict(topk=4)), (1, dict(ablation=1)), (2, dict(ablation=2)), (0, dict(ablation=3)),
                      (0, dict(ablation=2, fixed_draft=61)), (0, dict(tpl_width=65)), (0, dict(tpl_depth=17)),
-                     (0, dict(scan_kernel=5)), (0, dict(scan_kernel=-1))):
+                     (0, dict(scan_kernel=6)), (0, dict(scan_kernel=-1))):
         with pytest.raises(g_.GraftError):
             g_.Graft(g_.graft_default_config(100, 2, mode, W.BF16, **kw))
 
