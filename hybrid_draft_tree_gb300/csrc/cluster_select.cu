@@ -6,7 +6,8 @@
 // latency: two launches, a stream of a few MB, then pass 2's chain of unit
 // maxima, a candidate reload and the request ticket.  Here one cluster of CL
 // CTAs takes one row: each CTA stages its range of the row in shared memory
-// (the row's only read), keeping every thread's maximum, and takes T, the 8th
+// (the row's only read: bulk copies into shared memory), then every thread
+// takes the maximum of its chunk, and the CTA takes T, the 8th
 // largest of its threads' maxima.  Eight distinct elements of the range reach
 // T (each is its thread's maximum), so every element of the range's top-8 is
 // >= T; the CTA lists its elements >= T from shared memory and sorts them
@@ -22,6 +23,7 @@
 
 #include <climits>
 
+#include "bulk_copy.cuh"
 #include "graft_internal.cuh"
 #include "row_softmax.cuh"
 #include "scan_common.cuh"
@@ -29,13 +31,15 @@
 namespace graft {
 namespace {
 using namespace scan;
+using namespace bulk;
 namespace cg = cooperative_groups;
 using softmax::CL;
 
 constexpr int RT = 256;     // threads per CTA
 constexpr int RW = RT / 32;
 constexpr int RCAP = 128;   // elements >= T one CTA may list before its exact pass
-constexpr int UNR = 8;      // 16-byte loads in flight per thread while staging
+constexpr int UNR = 8;      // 16-byte loads in flight per thread while staging (unaligned rows)
+constexpr uint32_t BULK = 32768;  // bytes per bulk copy
 
 // The 8 largest of the 32 lanes' x (ordered ints, with multiplicity; INT_MIN
 // past the end): lane r < 8 returns the r-th.
@@ -79,6 +83,7 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
   __shared__ u64 s_top[K];           // this CTA's top-8 keys (read by CTA 0)
   __shared__ u64 s_wbest[RW];
   __shared__ int s_nc, s_T;
+  __shared__ unsigned long long s_bar;  // the staging copies' barrier
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   constexpr int EPL = Vec16<DT>::EPL;
   cg::cluster_group cluster = cg::this_cluster();
@@ -98,7 +103,11 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
       spos[i] = __ldcg(a.tree_pos + q);
       smask[i] = __ldcg(reinterpret_cast<const unsigned long long*>(a.tree_mask) + q);
     }
-  if (t == 0) s_nc = 0;
+  if (t == 0) {
+    s_nc = 0;
+    mbar_init(&s_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   __syncthreads();
   const int32_t tok = stok[row];
   // a request with no valid slot has no row to finish it: its first row's cluster does
@@ -120,34 +129,57 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
   bool nan = false;
   const int nvec = vec ? (v1 - v0) / EPL : 0;  // whole vectors (only the row's last chunk has a rest)
   const uint4* sv = reinterpret_cast<const uint4*>(stage + (size_t)(v0 - lo) * ES);
-  if (nvec > 0) {
-    const uint4* p = reinterpret_cast<const uint4*>(rowp) + v0 / EPL;
-    uint4* sp = reinterpret_cast<uint4*>(stage + (size_t)(v0 - lo) * ES);
-    for (int base = 0; base < nvec; base += UNR) {
-      Vec16<DT> x[UNR];
-#pragma unroll
-      for (int u = 0; u < UNR; ++u)
-        if (base + u < nvec) x[u].r = __ldcs(p + base + u);
-#pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        if (base + u >= nvec) break;
-        sp[base + u] = x[u].r;
-        const float m = x[u].vmax();
-        if (m != m) {
-          nan = true;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) tm = fmaxf(tm, x[u].elem(e));  // fmaxf drops NaN
-        } else {
-          tm = fmaxf(tm, m);
-        }
+  if (vec) {
+    // the range's whole vectors in bulk copies issued by one thread (the
+    // row and the stage are 16-byte aligned), the rest after the last whole
+    // vector with plain loads; then every thread reads its chunk back
+    const uint32_t bytes = (uint32_t)((hi - lo) / EPL) * 16u;
+    if (t == 0 && bytes > 0) {
+      mbar_expect_tx(&s_bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += BULK)
+        bulk_g2s(stage + off, rowp + (size_t)lo * ES + off, min(BULK, bytes - off), &s_bar);
+    }
+    for (int v = lo + (int)(bytes / ES) + t; v < hi; v += RT)
+      softmax::store_elem<DT>(stage, v - lo, load_scalar<DT>(rowp, v));
+    if (warp == 0 && bytes > 0) {
+      const bool ok = mbar_poll_warp(&s_bar, 0, a.wait_polls ? a.wait_polls : SPIN);
+      if (!ok && lane == 0) {
+        atomicOr(a.err, GRAFT_ERR_TIMEOUT);  // the step's results are not valid
+        mbar_wait_drain(&s_bar, 0);          // the copies land before this CTA reads on or exits
       }
     }
-  }
-  for (int v = v0 + nvec * EPL; v < v1; ++v) {
-    const float x = load_scalar<DT>(rowp, v);
-    softmax::store_elem<DT>(stage, v - lo, x);
-    if (x != x) nan = true;
-    tm = fmaxf(tm, x);
+    __syncthreads();
+    if (bytes > 0) (void)mbar_test_wait(&s_bar, 0);  // each thread observes the completed phase itself
+    for (int q = 0; q < nvec; ++q) {
+      Vec16<DT> x;
+      x.r = sv[q];
+      const float m = x.vmax();
+      if (m != m) {
+        nan = true;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) tm = fmaxf(tm, x.elem(e));  // fmaxf drops NaN
+      } else {
+        tm = fmaxf(tm, m);
+      }
+    }
+    for (int v = v0 + nvec * EPL; v < v1; ++v) {
+      const float x = softmax::stage_elem<DT>(stage, v - lo);
+      if (x != x) nan = true;
+      tm = fmaxf(tm, x);
+    }
+  } else {
+    for (int base = v0; base < v1; base += UNR) {
+      float x[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) x[u] = base + u < v1 ? load_scalar<DT>(rowp, base + u) : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        if (base + u >= v1) break;
+        softmax::store_elem<DT>(stage, base + u - lo, x[u]);
+        if (x[u] != x[u]) nan = true;
+        tm = fmaxf(tm, x[u]);
+      }
+    }
   }
   if (nan) atomicOr(a.err, GRAFT_ERR_NAN);
 

@@ -27,10 +27,12 @@
 
 #include "graft_internal.cuh"
 #include "scan_common.cuh"
+#include "bulk_copy.cuh"
 
 namespace graft {
 namespace {
 using namespace scan;
+using namespace bulk;
 
 constexpr int NCW = 8;                  // consumer warps
 constexpr int NCT = NCW * 32;           // consumer threads
@@ -39,8 +41,6 @@ constexpr int NSTAGE = 6;
 constexpr int VPL = TMA_CHUNK / 16 / NCT;  // 16-byte vectors per consumer lane per chunk
 constexpr int WCAP = 256;               // candidate keys per warp
 constexpr int MAXROWS = 128;            // rows one CTA may touch
-constexpr uint32_t SPIN = 1u << 22;     // try_wait polls before a wait gives up (unless the launch sets a limit)
-constexpr uint32_t DRAIN = 1u << 20;    // back-off rounds (1 us each) the drain waits for a copy in flight
 
 struct TmaSmem {
   u64 full[NSTAGE];
@@ -54,54 +54,6 @@ struct TmaSmem {
 };
 constexpr size_t SMEM_BYTES = (size_t)NSTAGE * TMA_CHUNK + sizeof(TmaSmem);
 
-// ---- mbarrier / bulk-copy primitives (inline PTX) ---------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(u64* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(u64* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(u64* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(u64* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-  return ok != 0;
-}
-// one thread, at most `polls` polls
-__device__ __forceinline__ bool mbar_wait(u64* bar, uint32_t parity, uint32_t polls) {
-  for (uint32_t it = 0; it < polls; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-// whole warp, at most `polls` polls, warp-uniform result
-__device__ __forceinline__ bool mbar_wait_warp(u64* bar, uint32_t parity, uint32_t polls) {
-  bool ok = false;
-  for (uint32_t it = 0; it < polls; ++it) {
-    ok = mbar_try_wait(bar, parity);
-    if (__all_sync(FULL, ok)) return true;
-  }
-  return __all_sync(FULL, ok);
-}
-// the drain: one thread waits for a copy it issued to land, backing off 1 us
-// between polls, for about a second at most
-__device__ __forceinline__ bool mbar_wait_drain(u64* bar, uint32_t parity) {
-  for (uint32_t it = 0; it < DRAIN; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    __nanosleep(1000);
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, u64* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
 
 // CTA owning global chunk i when T chunks are split over G CTAs.

@@ -387,7 +387,7 @@ class Graft:
         return int(self.L.graft_last_launch_count(self.h))
 
     def set_wait_limit(self, polls: int):
-        """Poll limit of the TMA scan's mbarrier waits (0 = the default)."""
+        """Poll limit of the bulk-copy kernels' mbarrier waits (0 = the default)."""
         self._check(self.L.graft_set_wait_limit(self.h, int(polls)))
 
 

@@ -355,12 +355,13 @@ int graft_profile_read(graft_handle* h, const char** names, float* ms, int32_t m
  * graft_warmup call queued. */
 int32_t graft_last_launch_count(const graft_handle* h);
 
-/* Failure detection: the TMA-pipelined verify scan (scan_kernel 2) bounds
- * every mbarrier wait of its producer and consumers by a number of polls; on
- * expiry it sets GRAFT_ERR_TIMEOUT in the handle's error word, stops issuing
- * copies, waits (for about a second at most) for the copies it has in
- * flight, and finishes, leaving the handle usable; the step's outputs are
- * then invalid.  This call sets that limit for later calls on the handle
+/* Failure detection: the kernels that stage logits with bulk copies (the
+ * TMA-pipelined verify scan, scan_kernel 2, and the cluster-per-row verify,
+ * scan_kernel 5 or the automatic choice for small steps) bound every
+ * mbarrier wait by a number of polls; on expiry they set GRAFT_ERR_TIMEOUT in
+ * the handle's error word, stop issuing copies, wait (for about a second at
+ * most) for the copies they have in flight, and finish, leaving the handle
+ * usable; the step's outputs are then invalid.  This call sets that limit for later calls on the handle
  * (polls = 0 restores the default of 2^22 polls), so a test can make the
  * waits run out on purpose.  It has no counterpart in the paper. */
 int graft_set_wait_limit(graft_handle* h, uint32_t polls);

@@ -777,15 +777,17 @@ def test_error_flags_and_recovery():
     assert acc.item() == 0 and out[0, 0].item() == 0     # argmax of a zero row is id 0
 
 
-def test_tma_scan_wait_limit_expires_and_the_handle_recovers():
-    """Failure detection on the GPU without a fault: the TMA scan's waits get
-    a limit of one poll, so they run out while its bulk copies are in flight;
-    the kernel flags GRAFT_ERR_TIMEOUT, lets its copies land and finishes.
-    With the default limit restored the next call on the same handle is
-    clean and matches the oracle."""
+@pytest.mark.parametrize("scan_kernel,B", [(2, 8), (5, 4)])
+def test_bulk_copy_wait_limit_expires_and_the_handle_recovers(scan_kernel, B):
+    """Failure detection on the GPU without a fault: the waits for the bulk
+    copies (the TMA scan's ring, the cluster verify's staging) get a limit of
+    one poll, so they run out while the copies are in flight; the kernel
+    flags GRAFT_ERR_TIMEOUT, lets its copies land and finishes.  With the
+    default limit restored the next call on the same handle is clean and
+    matches the oracle."""
     g_ = G()
     rng = np.random.default_rng(21)
-    V, B, S = 40000, 8, 61
+    V, S = 40000, 61
     vals = rng.normal(size=(B * S, V)).astype(np.float32)
     host_rows = (vals.view(np.uint32) >> 16).astype(np.uint16)
     logits = u16_to_bf16_tensor(host_rows)
@@ -794,7 +796,7 @@ def test_tma_scan_wait_limit_expires_and_the_handle_recovers():
         tok = rng.integers(0, V, S).astype(np.int32)
         par = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, S)], np.int32)
         trees.append(_tree_from_parents(tok, par))
-    eng = g_.Graft(g_.graft_default_config(V, B, 0, W.BF16, scan_kernel=2))
+    eng = g_.Graft(g_.graft_default_config(V, B, 0, W.BF16, scan_kernel=scan_kernel))
     tt = torch.from_numpy(np.stack([t.tok for t in trees])).cuda()
     tp = torch.from_numpy(np.stack([t.par for t in trees]).astype(np.int8)).cuda()
     tpos = torch.from_numpy(np.stack([t.pos for t in trees])).cuda()
