@@ -7,7 +7,7 @@
 // maxima, a candidate reload and the request ticket.  Here one cluster of CL
 // CTAs takes one row: each CTA stages its range of the row in shared memory
 // (the row's only read: bulk copies into shared memory), then every thread
-// takes the maximum of its chunk, and the CTA takes T, the 8th
+// takes the maximum of its elements, and the CTA takes T, the 8th
 // largest of its threads' maxima.  Eight distinct elements of the range reach
 // T (each is its thread's maximum), so every element of the range's top-8 is
 // >= T; the CTA lists its elements >= T from shared memory and sorts them
@@ -116,31 +116,31 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
   if (rank == 0 && t == 0 && tok >= V) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
   if (tok < 0 || tok >= V) return;  // the whole cluster (one row) leaves before any exchange
 
-  // 1. stage this CTA's range of the row; every thread keeps its chunk's maximum
+  // 1. stage this CTA's range of the row; every thread keeps the maximum of
+  //    its elements.  Thread t owns the range's whole 16-byte vectors t,
+  //    t + RT, ... and its other elements t, t + RT, ... after them: a warp's
+  //    shared-memory reads are then consecutive (no bank conflicts), and any
+  //    split of the elements among the threads serves the threshold argument
   const bool vec = a.g.vec;
   const int epl = vec ? EPL : 1;
   int lo, hi;
   softmax::cta_range(V, epl, rank, lo, hi);
-  int ch = (hi - lo + RT - 1) / RT;
-  ch = (ch + epl - 1) / epl * epl;
-  const int v0 = min(lo + t * ch, hi), v1 = min(v0 + ch, hi);
+  const int nv = vec ? (hi - lo) / EPL : 0;  // whole vectors of the range
+  const int rest0 = lo + nv * EPL;            // its first element after them
   const char* rowp = reinterpret_cast<const char*>(a.logits) + (size_t)row * (size_t)a.g.stride * ES;
+  const uint4* sv = reinterpret_cast<const uint4*>(stage);
   float tm = -INFINITY;  // NaN elements are flagged and left out
   bool nan = false;
-  const int nvec = vec ? (v1 - v0) / EPL : 0;  // whole vectors (only the row's last chunk has a rest)
-  const uint4* sv = reinterpret_cast<const uint4*>(stage + (size_t)(v0 - lo) * ES);
   if (vec) {
-    // the range's whole vectors in bulk copies issued by one thread (the
-    // row and the stage are 16-byte aligned), the rest after the last whole
-    // vector with plain loads; then every thread reads its chunk back
-    const uint32_t bytes = (uint32_t)((hi - lo) / EPL) * 16u;
+    // the whole vectors in bulk copies issued by one thread (the row and the
+    // stage are 16-byte aligned), the rest with plain loads
+    const uint32_t bytes = (uint32_t)nv * 16u;
     if (t == 0 && bytes > 0) {
       mbar_expect_tx(&s_bar, bytes);
       for (uint32_t off = 0; off < bytes; off += BULK)
         bulk_g2s(stage + off, rowp + (size_t)lo * ES + off, min(BULK, bytes - off), &s_bar);
     }
-    for (int v = lo + (int)(bytes / ES) + t; v < hi; v += RT)
-      softmax::store_elem<DT>(stage, v - lo, load_scalar<DT>(rowp, v));
+    for (int v = rest0 + t; v < hi; v += RT) softmax::store_elem<DT>(stage, v - lo, load_scalar<DT>(rowp, v));
     if (warp == 0 && bytes > 0) {
       const bool ok = mbar_poll_warp(&s_bar, 0, a.wait_polls ? a.wait_polls : SPIN);
       if (!ok && lane == 0) {
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
     }
     __syncthreads();
     if (bytes > 0) (void)mbar_test_wait(&s_bar, 0);  // each thread observes the completed phase itself
-    for (int q = 0; q < nvec; ++q) {
+    for (int q = t; q < nv; q += RT) {
       Vec16<DT> x;
       x.r = sv[q];
       const float m = x.vmax();
@@ -162,23 +162,23 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
         tm = fmaxf(tm, m);
       }
     }
-    for (int v = v0 + nvec * EPL; v < v1; ++v) {
-      const float x = softmax::stage_elem<DT>(stage, v - lo);
-      if (x != x) nan = true;
-      tm = fmaxf(tm, x);
+  }
+  // elements after the whole vectors (every element when the row is not
+  // 16-byte aligned: staged here with plain loads)
+  for (int base = rest0 + t; base < hi; base += RT * UNR) {
+    float x[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int v = base + u * RT;
+      x[u] = v < hi ? (vec ? softmax::stage_elem<DT>(stage, v - lo) : load_scalar<DT>(rowp, v)) : -INFINITY;
     }
-  } else {
-    for (int base = v0; base < v1; base += UNR) {
-      float x[UNR];
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) x[u] = base + u < v1 ? load_scalar<DT>(rowp, base + u) : -INFINITY;
-#pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        if (base + u >= v1) break;
-        softmax::store_elem<DT>(stage, base + u - lo, x[u]);
-        if (x[u] != x[u]) nan = true;
-        tm = fmaxf(tm, x[u]);
-      }
+    for (int u = 0; u < UNR; ++u) {
+      const int v = base + u * RT;
+      if (v >= hi) break;
+      if (!vec) softmax::store_elem<DT>(stage, v - lo, x[u]);
+      if (x[u] != x[u]) nan = true;
+      tm = fmaxf(tm, x[u]);
     }
   }
   if (nan) atomicOr(a.err, GRAFT_ERR_NAN);
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
 
   // 3. this CTA's elements >= T, from shared memory, then its top-8
   if (!exact) {
-    for (int q = 0; q < nvec; ++q) {
+    for (int q = t; q < nv; q += RT) {
       Vec16<DT> x;
       x.r = sv[q];
       unsigned m = x.ge_mask(T);
@@ -207,10 +207,10 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
         const int e = __ffs(m) - 1;
         m &= m - 1;
         const int pos = atomicAdd(&s_nc, 1);
-        if (pos < RCAP) s_list[pos] = make_key(x.elem(e), v0 + q * EPL + e);
+        if (pos < RCAP) s_list[pos] = make_key(x.elem(e), lo + q * EPL + e);
       }
     }
-    for (int v = v0 + nvec * EPL; v < v1; ++v) {
+    for (int v = rest0 + t; v < hi; v += RT) {
       const float x = softmax::stage_elem<DT>(stage, v - lo);
       if (x >= T) {
         const int pos = atomicAdd(&s_nc, 1);
@@ -229,7 +229,16 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
     u64 prev = ~0ull;
     for (int r = 0; r < K; ++r) {
       u64 best = 0ull;
-      for (int v = v0; v < v1; ++v) {
+      for (int q = t; q < nv; q += RT) {
+        Vec16<DT> x;
+        x.r = sv[q];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const u64 key = make_key(x.elem(e), lo + q * EPL + e);
+          if (key < prev && key > best) best = key;
+        }
+      }
+      for (int v = rest0 + t; v < hi; v += RT) {
         const u64 key = make_key(softmax::stage_elem<DT>(stage, v - lo), v);
         if (key < prev && key > best) best = key;
       }
@@ -267,12 +276,12 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
   if (!later && lane < K) st_keep(C + (size_t)tok * K + lane, id, l2_keep_policy());
   if (a.sample) return;  // stochastic verification accepts in its own kernel
   // the warp that completes the request's last valid row runs acceptance
-  const int nv = request_valid(a, stok, b, lane);
+  const int nvalid = request_valid(a, stok, b, lane);
   __syncwarp();
   int tk = 0;
   if (lane == 0) tk = ticket_acq_rel(&a.req_ticket[b]);
   tk = __shfl_sync(FULL, tk, 0);
-  if (tk == nv - 1) {
+  if (tk == nvalid - 1) {
     if (lane == 0) a.req_ticket[b] = 0;
     __syncwarp();
     accept_staged(a, b, lane, stok, spar, spos, smask);
@@ -308,11 +317,11 @@ bool cluster_select_fits(int rows, int V, int esize) {
   return rows <= CLUSTER_MAX_ROWS && softmax::stage_bytes(V, esize) <= CLUSTER_STAGE_MAX;
 }
 
-// Measured on GB300 (verify_update, L2 flushed): one request of 61 rows of
-// 32000 fp32 (16 KB per CTA), 15.0-17.0 us against 18.1-19.0 us on the
-// two-pass scan; of 128256 bf16 (32 KB per CTA), 25.1 against 19.6; of
-// 151936 bf16 (38 KB), 20.5 against 20.4; two requests or more, slower (each
-// further ~61 rows adds a wave of clusters).
+// Measured on GB300 (verify_update, L2 flushed), one request of 61 rows:
+// 32000 fp32 (16 KB per CTA) 14.3-15.0 us against 17.1-18.8 us on the
+// two-pass scan; 128256 bf16 (32 KB) 16.4 against 18.9; 151936 bf16 (38 KB)
+// 18.4 against 19.3-20.5.  Two requests or more are slower at every size
+// (each further ~61 rows is another wave of clusters).
 bool cluster_select_auto(int rows, int V, int esize) {
   return rows <= CLUSTER_AUTO_ROWS && softmax::stage_bytes(V, esize) <= CLUSTER_AUTO_STAGE;
 }

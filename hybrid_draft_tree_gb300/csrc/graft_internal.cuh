@@ -18,7 +18,7 @@ constexpr int WARM_TWO_PASS_ROWS = 4096;  // warm-up rows per call on the two-pa
 constexpr int CLUSTER_MAX_ROWS = 256;     // verified rows per call on the cluster-per-row verify
 constexpr int CLUSTER_STAGE_MAX = 200 * 1024;  // shared-memory bytes of one CTA's eighth of a row there
 constexpr int CLUSTER_AUTO_ROWS = 64;     // the automatic choice takes the cluster-per-row verify up to here
-constexpr int CLUSTER_AUTO_STAGE = 16 * 1024;  // ... and up to this many bytes of a row per CTA
+constexpr int CLUSTER_AUTO_STAGE = 48 * 1024;  // ... and up to this many bytes of a row per CTA
 
 // Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth;
 // maxdepth[R] = the largest depth among entries 0 .. R-1 (maxdepth[0] = 0).
