@@ -731,6 +731,16 @@ def test_cluster_verify_ties_overflow_and_sparse_rows(dtype, fn):
     _verify_case(20000, dtype, 33, 2, fn, seed=12, scan_kernel=5)
 
 
+@pytest.mark.parametrize("V,dtype", [(300000, W.F32), (300007, W.F32), (500000, W.BF16), (420000, W.F32)])
+def test_cluster_verify_wide_rows(V, dtype):
+    """Rows whose eighth needs more than the default 48 KB of shared memory
+    (the kernel opts in per launch): 16-byte aligned rows take several 32 KB
+    bulk copies per CTA, V = 300007 fp32 rows (not aligned) the plain-load
+    staging; past 200 KB per CTA (420000 fp32) the call takes the two-pass
+    scan."""
+    _verify_case(V, dtype, 9, 2, _normal, seed=V % 1000, scan_kernel=5)
+
+
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
 @pytest.mark.parametrize("pad,off", [(1, 0), (3, 1)])
 def test_cluster_verify_unaligned_rows(dtype, pad, off):
