@@ -22,6 +22,7 @@ struct graft_handle {
   int S = 0;
   int device = 0;
   int num_sms = 0;
+  int cluster_max_active = 0;  // clusters of the cluster-per-row verify resident at once (0: not available)
   int warm_ctas = 0;        // resident CTAs of the warm-up scan
   int scan_ctas_target = 0; // CTAs wanted per verify launch
   bool tma_ready = false;   // the TMA scan's shared-memory opt-in succeeded
@@ -290,6 +291,7 @@ int graft_init(const graft_config* cfg, graft_handle** out) {
   h->warm_ctas = h->num_sms * 4;
   h->scan_ctas_target = h->num_sms * 8;
   h->tma_ready = graft::prepare_verify_tma() == cudaSuccess;
+  h->cluster_max_active = graft::cluster_select_max_active(cfg->vocab, cfg->logits_dtype);
   cudaGetLastError();
   *out = h;
   return GRAFT_OK;
@@ -646,7 +648,9 @@ int verify_impl(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const
   // few rows, each staged in a cluster's shared memory: one launch, no reload
   const int esize = c.logits_dtype == GRAFT_BF16 ? 2 : 4;
   const bool use_cluster = graft::cluster_select_fits((int)rows, c.vocab, esize) &&
-                           (c.scan_kernel == 5 || (c.scan_kernel == 0 && graft::cluster_select_auto((int)rows, c.vocab, esize)));
+                           (c.scan_kernel == 5 ||
+                            (c.scan_kernel == 0 &&
+                             graft::cluster_select_auto((int)rows, c.vocab, esize, h->cluster_max_active)));
   const bool use_two_pass = !use_tma && two_pass_fits && (c.scan_kernel == 0 || c.scan_kernel >= 3);
   const int grid = h->num_sms * graft::verify_ctas_per_sm();
   if (!use_tma && !use_two_pass && rows > graft::verify_max_rows(grid))

@@ -72,7 +72,7 @@ __device__ __forceinline__ int32_t top8_of_pairs(int32_t x0, int32_t x1, int lan
 }
 
 template <int DT>
-__global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C) {
+__global__ void __launch_bounds__(RT, 8) k_cluster_select(VerifyArgs a, int32_t* C) {
   extern __shared__ __align__(16) char stage[];
   __shared__ int32_t stok[CLUSTER_MAX_ROWS];
   __shared__ uint64_t smask[MAX_S];  // CTA 0: the tree arrays of this row's request
@@ -288,6 +288,32 @@ __global__ void __launch_bounds__(RT) k_cluster_select(VerifyArgs a, int32_t* C)
   }
 }
 
+// Clusters of this kernel that fit on the device at once with V-element rows
+// (0 when the rows do not fit the kernel, or on any error).
+template <int DT>
+int cluster_select_max_active_impl(int V) {
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  const int bytes = softmax::stage_bytes(V, ES);
+  if (bytes > CLUSTER_STAGE_MAX) return 0;
+  if (bytes > 48 * 1024 &&
+      cudaFuncSetAttribute(k_cluster_select<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(CL);
+  cfg.blockDim = dim3(RT);
+  cfg.dynamicSmemBytes = bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_cluster_select<DT>, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
 template <int DT>
 cudaError_t cluster_select_impl(const VerifyArgs& a, int32_t* C, cudaStream_t s) {
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
@@ -317,13 +343,22 @@ bool cluster_select_fits(int rows, int V, int esize) {
   return rows <= CLUSTER_MAX_ROWS && softmax::stage_bytes(V, esize) <= CLUSTER_STAGE_MAX;
 }
 
+int cluster_select_max_active(int V, int dtype) {
+  const int n = dtype == GRAFT_BF16 ? cluster_select_max_active_impl<GRAFT_BF16>(V)
+                                    : cluster_select_max_active_impl<GRAFT_F32>(V);
+  cudaGetLastError();  // a failed query leaves no error behind
+  return n;
+}
+
 // Measured on GB300 (verify_update, L2 flushed), one request of 61 rows:
 // 32000 fp32 (16 KB per CTA) 14.3-15.0 us against 17.1-18.8 us on the
 // two-pass scan; 128256 bf16 (32 KB) 16.4 against 18.9; 151936 bf16 (38 KB)
-// 18.4 against 19.3-20.5.  Two requests or more are slower at every size
-// (each further ~61 rows is another wave of clusters).
-bool cluster_select_auto(int rows, int V, int esize) {
-  return rows <= CLUSTER_AUTO_ROWS && softmax::stage_bytes(V, esize) <= CLUSTER_AUTO_STAGE;
+// 18.4 against 19.3-20.5; two requests of 32000 fp32 (122 clusters, all
+// resident) 18.4 against 19.1.  Once the clusters no longer fit at once
+// (three requests of 32000 fp32; two of 151936 bf16, 5 CTAs per SM by shared
+// memory) each further wave makes it slower than the two-pass scan.
+bool cluster_select_auto(int rows, int V, int esize, int max_active) {
+  return rows <= max_active && rows <= CLUSTER_AUTO_ROWS && softmax::stage_bytes(V, esize) <= CLUSTER_AUTO_STAGE;
 }
 
 cudaError_t launch_cluster_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s) {

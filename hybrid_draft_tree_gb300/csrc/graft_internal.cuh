@@ -17,7 +17,7 @@ constexpr int TWO_PASS_MAX_UNITS = 1024;  // 512-byte units per row on the two-p
 constexpr int WARM_TWO_PASS_ROWS = 4096;  // warm-up rows per call on the two-pass scan (the rest: single pass)
 constexpr int CLUSTER_MAX_ROWS = 256;     // verified rows per call on the cluster-per-row verify
 constexpr int CLUSTER_STAGE_MAX = 200 * 1024;  // shared-memory bytes of one CTA's eighth of a row there
-constexpr int CLUSTER_AUTO_ROWS = 64;     // the automatic choice takes the cluster-per-row verify up to here
+constexpr int CLUSTER_AUTO_ROWS = 256;    // the automatic choice takes the cluster-per-row verify up to here
 constexpr int CLUSTER_AUTO_STAGE = 48 * 1024;  // ... and up to this many bytes of a row per CTA
 
 // Template entry j (j < tpl_len): parent entry (-1 = anchor), rank, depth;
@@ -164,7 +164,8 @@ cudaError_t launch_finish(const VerifyArgs& a, int32_t* C, cudaStream_t s);
 cudaError_t launch_two_pass_umax(const VerifyArgs& a, int dtype, int grid, cudaStream_t s);
 cudaError_t launch_two_pass_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s);
 bool cluster_select_fits(int rows, int V, int esize);
-bool cluster_select_auto(int rows, int V, int esize);
+bool cluster_select_auto(int rows, int V, int esize, int max_active);
+int cluster_select_max_active(int V, int dtype);
 cudaError_t launch_cluster_select(const VerifyArgs& a, int dtype, int32_t* C, cudaStream_t s);
 int two_pass_ctas_per_sm();
 int two_pass_max_rows(int grid);

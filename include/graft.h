@@ -88,8 +88,9 @@ typedef struct {
   float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15) */
   float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4) */
   int32_t max_draft_nodes;/* largest draft tree (<= 256) or block (<= budget) per request */
-  int32_t scan_kernel;    /* verify scan: 0 = automatic (cluster per row for up to 64 rows
-                             whose eighth is at most 48 KB, else two-pass with unit maxima on
+  int32_t scan_kernel;    /* verify scan: 0 = automatic (cluster per row when every row's
+                             cluster fits on the GPU at once and a row's eighth is at most
+                             48 KB, else two-pass with unit maxima on
                              16-byte aligned rows, else single-pass), 1 = single-pass with a shared
                              running top-8, 2 = TMA-pipelined (aligned rows of >= 32 KB only),
                              3 = two-pass with unit maxima (pass 2 reads every candidate unit
