@@ -246,10 +246,11 @@ int graft_set_thresholds(graft_handle* h, const float* thr);
 int graft_coverage(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
                    const int32_t* d_info, const void* d_logits, int64_t row_stride, float* d_gain, void* stream);
 
-/* Steps 4-5 (article §二 gear 3, §三): one streaming pass over the logits of
- * every valid slot (plus a re-read of the few 512-byte pieces of a row that
- * can hold its largest values) computes its top-8 (element 0 = the greedy
- * argmax), then
+/* Steps 4-5 (article §二 gear 3, §三): one pass over the logits of every
+ * valid slot (the two-pass scan re-reads the few 512-byte pieces of a row
+ * that can hold its largest values; for small steps each row is staged in
+ * the shared memory of a thread-block cluster and read once) computes its
+ * top-8 (element 0 = the greedy argmax), then
  *   accepted(i)  <=> every non-root node j on the root->i path has
  *                    tok[j] == argmax(row of parent(j));
  *   winner       =  the accepted slot of greatest position (ties: lower slot);
@@ -257,7 +258,9 @@ int graft_coverage(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, co
  *   d_out_tokens[b][S] = the winner's path tokens after the root, then the
  *                        bonus token argmax(row of winner), then -1s;
  * and every valid slot overwrites C[its token] with its top-8 (the last
- * writer in (request, slot) order wins).  Pad slots (tok < 0) are not read.
+ * writer in (request, slot) order wins).  Pad slots (tok < 0) are not read;
+ * a request without a valid root (all its slots pads) gets d_accept_len 0
+ * and d_out_tokens all -1.
  * The tree arrays are those written by graft_assemble (or equivalent ones).
  * d_logits row (b, i) starts at element (b*S + i) * row_stride (row_stride >= V). */
 int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,

@@ -748,6 +748,46 @@ def test_cluster_verify_unaligned_rows(dtype, pad, off):
     _verify_case(3001, dtype, 17, 3, _normal, stride_pad=pad, offset_elems=off, seed=pad + 7, scan_kernel=5)
 
 
+@pytest.mark.parametrize("scan_kernel", [0, 1, 3, 5])
+def test_verify_request_without_valid_slots(scan_kernel):
+    """A request whose slots are all pads (token -1) has no row to finish it:
+    the verify still writes its acceptance (nothing accepted, nothing
+    emitted; the oracle takes only trees with a valid root), and the other
+    requests match the oracle."""
+    g_ = G()
+    rng = np.random.default_rng(31)
+    V, B, S = 3000, 3, 61
+    vals = rng.normal(size=(B * S, V)).astype(np.float32)
+    trees = []
+    for b in range(B):
+        n = 0 if b == 1 else int(rng.integers(1, S + 1))
+        tok = np.full(S, -1, np.int32)
+        par = np.full(S, -1, np.int32)
+        tok[:n] = rng.integers(0, V, n)
+        for i in range(1, n):
+            par[i] = rng.integers(0, i)
+        trees.append(_tree_from_parents(tok, par))
+    eng = g_.Graft(g_.graft_default_config(V, B, 0, W.F32, scan_kernel=scan_kernel))
+    tt = torch.from_numpy(np.stack([t.tok for t in trees])).cuda()
+    tp = torch.from_numpy(np.stack([t.par for t in trees]).astype(np.int8)).cuda()
+    tpos = torch.from_numpy(np.stack([t.pos for t in trees])).cuda()
+    tm = torch.from_numpy(np.stack([t.mask for t in trees]).view(np.int64)).cuda()
+    acc = torch.full((B,), 77, dtype=torch.int32, device="cuda")
+    out = torch.full((B, S), 77, dtype=torch.int32, device="cuda")
+    eng.verify_update(B, tt, tp, tpos, tm, torch.from_numpy(vals).cuda(), acc, out)
+    C = oracle.new_matrix(V)
+    hr = vals.reshape(B, S, V)
+    for b in (0, 2):
+        a, o, topk = oracle.verify(trees[b], hr[b], W.F32)
+        oracle.update(C, trees[b], topk)
+        assert acc.cpu().numpy()[b] == a
+        assert np.array_equal(out.cpu().numpy()[b], o)
+    assert acc.cpu().numpy()[1] == 0 and (out.cpu().numpy()[1] == -1).all()
+    assert np.array_equal(eng.get_matrix(), C)
+    assert eng.sync() == 0
+    eng.close()
+
+
 def test_batch_zero_is_a_noop():
     g_ = G()
     eng = g_.Graft(g_.graft_default_config(100, 4, 0, W.BF16))
