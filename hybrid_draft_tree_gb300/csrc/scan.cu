@@ -541,7 +541,11 @@ __global__ __launch_bounds__(FT) void k_finish(VerifyArgs a, int32_t* C) {
 }
 
 // ---- warm-up -----------------------------------------------------------------------
+// The warm-up's kernels run as a chain of programmatic dependent launches:
+// each may be scheduled as its predecessor's CTAs leave and waits for the
+// predecessor's results (grid_dependency_wait) before reading them.
 __global__ void k_warm_mark(WarmArgs a) {
+  grid_dependents_launch();
   const int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= a.n_rows) return;
   const int32_t t = a.tokens[n];
@@ -549,6 +553,8 @@ __global__ void k_warm_mark(WarmArgs a) {
   atomicMax(&a.winner[t], (int32_t)(n + 1));
 }
 __global__ void k_warm_list(WarmArgs a) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // every mark is in
   const int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= a.n_rows) return;
   const int32_t t = a.tokens[n];
@@ -572,6 +578,7 @@ __global__ __launch_bounds__(ST) void k_warm_scan(WarmArgs a) {
   }
 }
 __global__ void k_warm_reset(WarmArgs a) {
+  grid_dependency_wait();  // the kernels before it have read the list and the marks
   const int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (n == 0) *a.count = 0;
   if (n >= a.n_rows) return;
@@ -607,8 +614,8 @@ cudaError_t launch_warmup_begin(const WarmArgs& a, cudaStream_t s) {
   const int t = 256;
   const unsigned g = (unsigned)((a.n_rows + t - 1) / t);
   k_warm_mark<<<g, t, 0, s>>>(a);
-  k_warm_list<<<g, t, 0, s>>>(a);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : launch_dependent(k_warm_list, dim3(g), dim3(t), 0, s, a);
 }
 cudaError_t launch_warmup_scan(const WarmArgs& a, int dtype, int grid_ctas, cudaStream_t s) {
   if (dtype == GRAFT_BF16)
@@ -618,8 +625,7 @@ cudaError_t launch_warmup_scan(const WarmArgs& a, int dtype, int grid_ctas, cuda
 cudaError_t launch_warmup_end(const WarmArgs& a, cudaStream_t s) {
   const int t = 256;
   const unsigned g = (unsigned)((a.n_rows + t - 1) / t);
-  k_warm_reset<<<g, t, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(k_warm_reset, dim3(g), dim3(t), 0, s, a);
 }
 
 }  // namespace graft

@@ -231,6 +231,7 @@ __global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a, const int32_t* lis
   __shared__ int warpsum[UW];
   __shared__ int rowlist[UMAXROWS];
   grid_dependents_launch();  // pass 2 may be scheduled as SMs free up; it waits for this grid's results
+  if (LIST) grid_dependency_wait();  // the warm-up's list comes from the kernel ahead
   const Slice sl = compact_rows<LIST>(a, list, count, cap, rowlist, warpsum);
   if (!sl.live) return;
   stream_units<DT, LIST, TOP2>(a, sl, rowlist, threadIdx.x >> 5, threadIdx.x & 31);
@@ -239,6 +240,9 @@ __global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a, const int32_t* lis
 template <int DT, bool LIST>
 cudaError_t umax_impl(const VerifyArgs& a, const int32_t* list, const int32_t* count, int cap, int grid,
                       cudaStream_t s) {
+  if (LIST)  // the warm-up: a programmatic dependent of its listing kernel
+    return a.top2 ? launch_dependent(k_umax<DT, LIST, true>, dim3(grid), dim3(UT), 0, s, a, list, count, cap)
+                  : launch_dependent(k_umax<DT, LIST, false>, dim3(grid), dim3(UT), 0, s, a, list, count, cap);
   if (a.top2) k_umax<DT, LIST, true><<<grid, UT, 0, s>>>(a, list, count, cap);
   else k_umax<DT, LIST, false><<<grid, UT, 0, s>>>(a, list, count, cap);
   return cudaGetLastError();
