@@ -889,12 +889,14 @@ def test_invalid_arguments_are_rejected():
             g_.Graft(g_.graft_default_config(100, 2, mode, W.BF16, **kw))
 
 
-def test_step_replays_from_a_cuda_graph():
-    """assemble + verify_update (with the dependent launch of pass 2) are
-    captured into a CUDA graph and replayed: the same trees, acceptance and
-    matrix as the same calls made directly on an identical handle."""
+@pytest.mark.parametrize("B", [4, 1])
+def test_step_replays_from_a_cuda_graph(B):
+    """assemble + verify_update are captured into a CUDA graph and replayed:
+    the same trees, acceptance and matrix as the same calls made directly on
+    an identical handle.  Four requests take the two-pass scan (with the
+    dependent launch of pass 2), one request the cluster-per-row verify."""
     from workloads.device_loop import DeviceLoop
-    w = W.WORKLOADS[2].scaled(V=40000, B=4)
+    w = W.WORKLOADS[2].scaled(V=40000, B=B)
     eager = engine_for(w)
     graphed = engine_for(w)
     loop = DeviceLoop(w, eager)
