@@ -19,6 +19,7 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
+#include "bulk_copy.cuh"
 #include "graft_internal.cuh"
 #include "scan_common.cuh"
 
@@ -83,22 +84,76 @@ __device__ __host__ __forceinline__ int stage_bytes(int V, int esize) {
 // be reading).  On return st.M, st.W hold the row's statistics in every CTA;
 // st.m / st.s / st.lo / st.hi / st.ch describe this CTA's chunks.  With
 // `stage` (stage_bytes(V, esize) bytes of shared memory, 16-byte aligned),
-// element v of this CTA's range is left at stage[v - lo].
-template <int DT, int NT>
+// element v of this CTA's range is left at stage[v - lo].  With BULK (a
+// stage, an aligned row and `bar`, an initialised mbarrier; pass p waits for
+// its phase p & 1, so every call must stage), the range arrives by bulk copies issued by
+// one thread (the wait bounded by `polls`, a timeout flagged in `err` and
+// drained before the stage is read) and the threads then read their chunks
+// from shared memory; the chunks then hold an odd number of 16-byte vectors,
+// so the threads of a warp read distinct banks.
+template <int DT, int NT, bool BULK = false>
 __device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* rowp, int V, bool vec, float k2,
-                                  ClusterRow<NT>& st, int pass, char* stage = nullptr) {
+                                  ClusterRow<NT>& st, int pass, char* stage = nullptr,
+                                  unsigned long long* bar = nullptr, uint32_t* err = nullptr, uint32_t polls = 0) {
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   const int t = threadIdx.x;
   constexpr int EPL = Vec16<DT>::EPL;
   constexpr int UNR = 8;  // 16-byte loads in flight per thread
   const int epl = vec ? EPL : 1;
+  const bool bulk = BULK;  // the caller guarantees a stage, an aligned row and a barrier
   int lo, hi;
   cta_range(V, epl, (int)cluster.block_rank(), lo, hi);
   int ch = (hi - lo + NT - 1) / NT;
   ch = (ch + epl - 1) / epl * epl;
+  if (bulk && ((ch / EPL) & 1) == 0) ch += EPL;  // an odd number of vectors per chunk
   const int v0 = min(lo + t * ch, hi), v1 = min(v0 + ch, hi);
   float m = -INFINITY, s = 0.f;
-  if (vec) {
+  if (bulk) {
+    const uint32_t bytes = (uint32_t)((hi - lo) / EPL) * 16u;  // the range's whole vectors
+    const uint32_t parity = (uint32_t)pass & 1u;
+    if (t == 0 && bytes > 0) {
+      bulk::mbar_expect_tx(bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += 32768u)
+        bulk::bulk_g2s(stage + off, rowp + (size_t)lo * ES + off, min(32768u, bytes - off), bar);
+    }
+    for (int v = lo + (int)(bytes / ES) + t; v < hi; v += NT) store_elem<DT>(stage, v - lo, load_scalar<DT>(rowp, v));
+    if (t < 32 && bytes > 0) {
+      const bool ok = bulk::mbar_poll_warp(bar, parity, polls ? polls : bulk::SPIN);
+      if (!ok && t == 0) {
+        atomicOr(err, GRAFT_ERR_TIMEOUT);  // the step's results are not valid
+        bulk::mbar_wait_drain(bar, parity);  // the copies land before the stage is read or rewritten
+      }
+    }
+    __syncthreads();
+    if (bytes > 0) (void)bulk::mbar_test_wait(bar, parity);  // each thread observes the completed phase itself
+    constexpr int UNS = 4;  // vectors per batch from shared memory
+    const uint4* sp = reinterpret_cast<const uint4*>(stage + (size_t)(v0 - lo) * ES);
+    const int nvec = (v1 - v0) / EPL;
+    for (int base = 0; base < nvec; base += UNS) {
+      Vec16<DT> x[UNS];
+#pragma unroll
+      for (int u = 0; u < UNS; ++u)
+        if (base + u < nvec) x[u].r = sp[base + u];
+      float bm = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < UNS; ++u) {
+        if (base + u >= nvec) break;
+        bm = fmaxf(bm, x[u].vmax());
+      }
+      if (bm > m) { s *= exp2f((m - bm) * k2); m = bm; }
+      if (m != -INFINITY) {
+        float q[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < UNS; ++u) {
+          if (base + u >= nvec) break;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) q[e & 3] += exp2f((x[u].elem(e) - m) * k2);
+        }
+        s += (q[0] + q[1]) + (q[2] + q[3]);
+      }
+    }
+    for (int v = v0 + nvec * EPL; v < v1; ++v) online_add(m, s, stage_elem<DT>(stage, v - lo), k2);
+  } else if (!BULK && vec) {
     const uint4* p = reinterpret_cast<const uint4*>(rowp) + v0 / EPL;
     const int nvec = (v1 - v0) / EPL;  // whole vectors of the chunk (only the row's last chunk has a rest)
     uint4* sp = stage ? reinterpret_cast<uint4*>(stage + (size_t)(v0 - lo) * ES) : nullptr;

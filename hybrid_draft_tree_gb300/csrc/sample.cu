@@ -38,7 +38,9 @@ constexpr int PT = 256;  // threads per CTA (CL CTAs per request)
 constexpr int STAGE_MAX = 160 * 1024;  // shared memory for a CTA's range of the row; larger rows read it again
 constexpr float LOG2E = 1.4426950408889634f;
 
-template <int DT>
+// BULK: the rows are staged by bulk copies (aligned rows whose CTA range fits
+// the stage); otherwise by the threads' loads, or read again (staged = 0).
+template <int DT, bool BULK>
 __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   extern __shared__ __align__(16) char s_stage[];  // this CTA's range of the current row (when staged)
@@ -49,6 +51,7 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
   __shared__ float s_cw[PT];           // chunk weights of the final draw
   __shared__ int s_acc, s_nrej, s_chunk, s_pick;
   __shared__ float s_target, s_before, s_ures;
+  __shared__ unsigned long long s_bar;  // the row staging's bulk copies
   const cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / CL, t = threadIdx.x, lane = t & 31, warp = t >> 5, S = a.S, V = a.g.V;
@@ -58,7 +61,11 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
     s_par[t] = a.tree_parent[(int64_t)b * S + t];
     s_u[t] = a.u_accept[(int64_t)b * S + t];
   }
-  if (t == 0) s_ures = a.u_resid[b];
+  if (t == 0) {
+    s_ures = a.u_resid[b];
+    bulk::mbar_init(&s_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   char* stage = staged ? s_stage : nullptr;
   __syncthreads();
   int32_t* out = a.out_tokens + (int64_t)b * S;
@@ -80,7 +87,8 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
         s_x[j] = (j > node && s_par[j] == node && tk >= 0 && tk < V) ? load_scalar<DT>(rowp, tk) : 0.f;
       }
     }
-    cluster_row_stats<DT, PT>(cluster, rowp, V, a.g.vec != 0, k2, st, depth, stage);
+    cluster_row_stats<DT, PT, BULK>(cluster, rowp, V, a.g.vec != 0, k2, st, depth, stage, &s_bar, a.err,
+                                    a.wait_polls);
     const float M = st.M, W = st.W;
     if (warp == 0) {  // the same decisions in every CTA of the cluster
       // the node's children in slot order, found by the whole warp; then one
@@ -258,13 +266,11 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
   grid_dependency_wait();
 }
 
-template <int DT>
-cudaError_t sample_impl(const VerifyArgs& a, cudaStream_t s) {
-  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
-  const int bytes = stage_bytes(a.g.V, ES);
-  const int staged = bytes <= STAGE_MAX ? 1 : 0;
+template <int DT, bool BULK>
+cudaError_t sample_launch(const VerifyArgs& a, int staged, int bytes, cudaStream_t s) {
   if (staged && bytes > 48 * 1024) {  // above the default limit the kernel must opt in (per device: set it each time)
-    const cudaError_t e = cudaFuncSetAttribute(k_sample<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_sample<DT, BULK>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg{};
@@ -283,7 +289,15 @@ cudaError_t sample_impl(const VerifyArgs& a, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_sample<DT>, a, staged);
+  return cudaLaunchKernelEx(&cfg, k_sample<DT, BULK>, a, staged);
+}
+
+template <int DT>
+cudaError_t sample_impl(const VerifyArgs& a, cudaStream_t s) {
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  const int bytes = stage_bytes(a.g.V, ES);
+  const int staged = bytes <= STAGE_MAX ? 1 : 0;
+  return staged && a.g.vec ? sample_launch<DT, true>(a, staged, bytes, s) : sample_launch<DT, false>(a, staged, bytes, s);
 }
 
 }  // namespace
