@@ -360,8 +360,9 @@ int graft_profile_read(graft_handle* h, const char** names, float* ms, int32_t m
 int32_t graft_last_launch_count(const graft_handle* h);
 
 /* Failure detection: the kernels that stage logits with bulk copies (the
- * TMA-pipelined verify scan, scan_kernel 2, and the cluster-per-row verify,
- * scan_kernel 5 or the automatic choice for small steps) bound every
+ * TMA-pipelined verify scan, scan_kernel 2, the cluster-per-row verify,
+ * scan_kernel 5 or the automatic choice for small steps, and the stochastic
+ * walk of graft_verify_update_sample on aligned rows) bound every
  * mbarrier wait by a number of polls; on expiry they set GRAFT_ERR_TIMEOUT in
  * the handle's error word, stop issuing copies, wait (for about a second at
  * most) for the copies they have in flight, and finish, leaving the handle

@@ -788,6 +788,49 @@ def test_verify_request_without_valid_slots(scan_kernel):
     eng.close()
 
 
+def test_stochastic_walk_wait_limit_expires_and_the_handle_recovers():
+    """The stochastic walk's staging wait (bulk copies on an mbarrier) gets a
+    limit of one poll: the kernel flags GRAFT_ERR_TIMEOUT, lets its copies
+    land and finishes.  With the default limit restored, the next call on the
+    same handle is clean and gives the same acceptance as a fresh handle."""
+    g_ = G()
+    rng = np.random.default_rng(23)
+    V, B, S = 40000, 4, 61
+    vals = rng.normal(size=(B * S, V)).astype(np.float32)
+    logits = u16_to_bf16_tensor((vals.view(np.uint32) >> 16).astype(np.uint16))
+    trees = []
+    for b in range(B):
+        tok = rng.integers(0, V, S).astype(np.int32)
+        par = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, S)], np.int32)
+        trees.append(_tree_from_parents(tok, par))
+    tt = torch.from_numpy(np.stack([t.tok for t in trees])).cuda()
+    tp = torch.from_numpy(np.stack([t.par for t in trees]).astype(np.int8)).cuda()
+    tpos = torch.from_numpy(np.stack([t.pos for t in trees])).cuda()
+    tm = torch.from_numpy(np.stack([t.mask for t in trees]).view(np.int64)).cuda()
+    u = torch.from_numpy(rng.random((B, S)).astype(np.float32)).cuda()
+    ur = torch.from_numpy(rng.random(B).astype(np.float32)).cuda()
+
+    def call(eng):
+        acc = torch.empty(B, dtype=torch.int32, device="cuda")
+        out = torch.empty((B, S), dtype=torch.int32, device="cuda")
+        eng.verify_update_sample(B, tt, tp, tpos, tm, logits, 1.0, u, ur, acc, out)
+        return acc, out
+
+    eng = g_.Graft(g_.graft_default_config(V, B, 0, W.BF16))
+    eng.set_wait_limit(1)
+    call(eng)
+    assert eng.sync(raise_on_error=False) & g_.graft.GRAFT_ERR_TIMEOUT
+    eng.set_wait_limit(0)
+    acc, out = call(eng)
+    assert eng.sync() == 0
+    fresh = g_.Graft(g_.graft_default_config(V, B, 0, W.BF16))
+    acc2, out2 = call(fresh)
+    assert fresh.sync() == 0
+    assert torch.equal(acc, acc2) and torch.equal(out, out2)
+    eng.close()
+    fresh.close()
+
+
 def test_batch_zero_is_a_noop():
     g_ = G()
     eng = g_.Graft(g_.graft_default_config(100, 4, 0, W.BF16))
