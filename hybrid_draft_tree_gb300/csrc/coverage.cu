@@ -9,7 +9,8 @@
 // parent carries it.  The gain is the sum, over the new tokens, of their
 // softmax probability in the parent's logits row.  A diagnostic off the hot
 // path: one thread-block cluster of CL CTAs per request streams each boundary
-// parent's row once, split over the cluster's SMs (row_softmax.cuh).
+// parent's row once, split over the cluster's SMs (row_softmax.cuh; aligned
+// rows whose eighth fits STAGE_MAX arrive by bulk copies into shared memory).
 #include <cuda_bf16.h>
 
 #include "graft_internal.cuh"
@@ -22,12 +23,17 @@ using namespace scan;
 using namespace softmax;
 
 constexpr int CT = 256;  // threads per CTA (CL CTAs per request)
+constexpr int STAGE_MAX = 160 * 1024;  // shared memory for a CTA's eighth of a row (bulk staging)
 
 constexpr float LOG2E = 1.4426950408889634f;
 
-template <int DT>
+// BULK: each row pass stages the CTA's eighth of the row by bulk copies;
+// otherwise the threads load their chunks.
+template <int DT, bool BULK>
 __global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t* info, float* gain) {
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  extern __shared__ __align__(16) char s_stage[];  // BULK: this CTA's range of the current row
+  __shared__ unsigned long long s_bar;
   __shared__ ClusterRow<CT> st;
   __shared__ int32_t s_tok[MAX_S], s_par[MAX_S];
   __shared__ float s_x[MAX_S];  // a boundary candidate's logit in its parent's row, by slot
@@ -39,6 +45,10 @@ __global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t*
   if (t < S) {
     s_tok[t] = a.tree_tok[(int64_t)b * S + t];
     s_par[t] = a.tree_parent[(int64_t)b * S + t];
+  }
+  if (BULK && t == 0) {
+    bulk::mbar_init(&s_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   // boundary parents (a kept slot with a retrieved child), in slot order
@@ -63,7 +73,8 @@ __global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t*
       if (j >= r0 && j < r1 && s_par[j] == p && s_tok[j] >= 0 && s_tok[j] < a.g.V)
         s_x[j] = load_scalar<DT>(rowp, s_tok[j]);
     }
-    cluster_row_stats<DT, CT>(cluster, rowp, a.g.V, a.g.vec != 0, LOG2E, st, pass++);
+    cluster_row_stats<DT, CT, BULK>(cluster, rowp, a.g.V, a.g.vec != 0, LOG2E, st, pass++, BULK ? s_stage : nullptr,
+                                    &s_bar, a.err, a.wait_polls);
     const float M = st.M, Z = st.W;
     if (warp == 0 && rank == 0 && Z > 0.f) {
       // the kept draft children of p; a candidate with one of their tokens is not new
@@ -90,12 +101,17 @@ __global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t*
   if (pass > 0) cluster.sync();  // the last pass's pairs are read before any CTA of the cluster exits
 }
 
-template <int DT>
-cudaError_t coverage_impl(const VerifyArgs& a, const int32_t* info, float* gain, cudaStream_t s) {
+template <int DT, bool BULK>
+cudaError_t coverage_launch(const VerifyArgs& a, const int32_t* info, float* gain, int bytes, cudaStream_t s) {
+  if (BULK && bytes > 48 * 1024) {  // above the default limit the kernel must opt in (per device: set it each time)
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_coverage<DT, BULK>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.batch * CL);
   cfg.blockDim = dim3(CT);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = BULK ? bytes : 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -104,7 +120,15 @@ cudaError_t coverage_impl(const VerifyArgs& a, const int32_t* info, float* gain,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_coverage<DT>, a, info, gain);
+  return cudaLaunchKernelEx(&cfg, k_coverage<DT, BULK>, a, info, gain);
+}
+
+template <int DT>
+cudaError_t coverage_impl(const VerifyArgs& a, const int32_t* info, float* gain, cudaStream_t s) {
+  constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
+  const int bytes = stage_bytes(a.g.V, ES);
+  return a.g.vec && bytes <= STAGE_MAX ? coverage_launch<DT, true>(a, info, gain, bytes, s)
+                                       : coverage_launch<DT, false>(a, info, gain, bytes, s);
 }
 
 }  // namespace
