@@ -224,15 +224,16 @@ def measured_peak_gbs():
     return 6800.0, "fallback"
 
 
-def traffic_record(kernel):
+def traffic_record(kernel, workload):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, valid
-    only while that kernel's source file is unchanged."""
+    only for the workload it was captured on (the name before the record's
+    first comma) and while that kernel's source file is unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f).get(kernel)
-    if not rec:
+    if not rec or rec.get("workload", "").split(",")[0].strip() != workload:
         return None
     path = os.path.join(ROOT, "hybrid_draft_tree_gb300", "csrc", rec["source"])
     if not os.path.exists(path):
@@ -449,7 +450,7 @@ def run_graft(args, ws, rank, local):
     dom_s = kern[dominant] / 1e3
     achieved = algo_bytes / dom_s / 1e9
     peak, peak_kind = measured_peak_gbs()
-    tr = traffic_record(dominant)
+    tr = traffic_record(dominant, w.name)
     mat = float(np.mean(np.concatenate(accs))) + 1.0
 
     # incremental drafting (checkpoint mode): the critical-path assembly when

@@ -26,15 +26,16 @@ def test_traffic_record_follows_the_kernel_source(tmp_path):
     csrc.mkdir(parents=True)
     (csrc / "k.cu").write_text("kernel v1\n")
     rec = {"k_x": {"source": "k.cu", "source_sha256": hashlib.sha256(b"kernel v1\n").hexdigest(),
-                   "bytes_per_launch": 123}}
+                   "bytes_per_launch": 123, "workload": "w-big, 976 valid rows"}}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     b.ROOT = str(tmp_path)
-    assert b.traffic_record("k_x")["bytes_per_launch"] == 123
-    assert b.traffic_record("k_other") is None
+    assert b.traffic_record("k_x", "w-big")["bytes_per_launch"] == 123
+    assert b.traffic_record("k_x", "w-small") is None       # captured on another workload
+    assert b.traffic_record("k_other", "w-big") is None
     (csrc / "k.cu").write_text("kernel v2\n")                 # the kernel changed since the capture
-    assert b.traffic_record("k_x") is None
+    assert b.traffic_record("k_x", "w-big") is None
     (csrc / "k.cu").unlink()
-    assert b.traffic_record("k_x") is None
+    assert b.traffic_record("k_x", "w-big") is None
 
 
 def test_peak_prefers_the_measured_file(tmp_path):
