@@ -50,6 +50,7 @@ __global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t*
     bulk::mbar_init(&s_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  cluster_started_arrive();
   __syncthreads();
   // boundary parents (a kept slot with a retrieved child), in slot order
   __shared__ unsigned long long s_bmask;
@@ -98,7 +99,7 @@ __global__ __launch_bounds__(CT, 4) void k_coverage(VerifyArgs a, const int32_t*
     __syncthreads();  // s_x is read before the next parent's loads
   }
   if (t == 0 && rank == 0) gain[b] = total;
-  if (pass > 0) cluster.sync();  // the last pass's pairs are read before any CTA of the cluster exits
+  if (pass == 0) cluster_started_wait();  // (no pass: the start barrier still completes)
 }
 
 template <int DT, bool BULK>

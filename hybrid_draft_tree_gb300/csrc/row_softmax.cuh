@@ -6,11 +6,12 @@
 // cluster owns a contiguous range of the row, and thread t of the CTA owns a
 // contiguous chunk of that range (lengths multiples of the vector width when
 // the row is 16-byte aligned, so chunks are read with 16-byte loads).  Each
-// thread keeps an online (max, sum of exp2((x - max) * k2)) over its chunk,
-// k2 = log2(e) / temperature; warp 0 folds them into the CTA's pair, and the
-// CTAs exchange their pairs through distributed shared memory, each folding
-// the CL pairs in rank order, so every CTA of the cluster holds the same row
-// maximum and sum.  The chunks' pairs stay in shared memory, so an inverse-CDF
+// thread keeps a (max, sum of exp2((x - max) * k2)) over its chunk (online
+// while reading the row, or the maximum first when the chunk is staged),
+// k2 = log2(e) / temperature; warp 0 folds them into the CTA's pair, and each
+// CTA writes its pair into every CTA of the cluster (distributed shared
+// memory), each then folding the CL pairs in rank order, so every CTA of the
+// cluster holds the same row maximum and sum.  The chunks' pairs stay in shared memory, so an inverse-CDF
 // draw over the row can locate its CTA and its chunk without another pass;
 // given a staging buffer, the CTA also keeps its range of the row in shared
 // memory, so the draw reads no global memory at all.
@@ -34,11 +35,21 @@ template <int NT>
 struct ClusterRow {
   float m[NT];        // chunk maxima
   float s[NT];        // chunk sums of exp2((x - m[t]) * k2)
-  float cm[2], cs[2]; // this CTA's (max, sum) of the current pass, by pass parity (read by the other CTAs)
-  float ct;           // this CTA's weight in a final draw (read by the other CTAs)
+  float pm[2][CL], ps[2][CL];  // every CTA's (max, sum) by pass parity and rank, written by that CTA
+  float em[CL], es[CL];        // every CTA's (max, sum) of the last pass, by rank
   float M, W;         // row maximum and sum of exp2((x - M) * k2), the same in every CTA of the cluster
   int lo, hi, ch;     // this CTA's element range and its chunk length
 };
+
+// The cluster's start barrier, split: every thread of every CTA arrives once
+// at the start of the kernel (cluster_started_arrive) and waits before its
+// first write into another CTA's shared memory (cluster_started_wait, called by
+// the first pass of cluster_row_stats; a kernel that makes no pass calls it
+// before it exits), so no CTA is written to before it runs.
+__device__ __forceinline__ void cluster_started_arrive() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_started_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
 // (m, s) <- online update with element x.
 __device__ __forceinline__ void online_add(float& m, float& s, float x, float k2) {
@@ -79,18 +90,19 @@ __device__ __host__ __forceinline__ int stage_bytes(int V, int esize) {
   return per * esize;
 }
 
-// One pass over row `rowp` (pass index `pass`: consecutive passes alternate
-// the exchange slots, so a CTA never overwrites a pair another CTA may still
-// be reading).  On return st.M, st.W hold the row's statistics in every CTA;
-// st.m / st.s / st.lo / st.hi / st.ch describe this CTA's chunks.  With
-// `stage` (stage_bytes(V, esize) bytes of shared memory, 16-byte aligned),
-// element v of this CTA's range is left at stage[v - lo].  With BULK (a
-// stage, an aligned row and `bar`, an initialised mbarrier; pass p waits for
-// its phase p & 1, so every call must stage), the range arrives by bulk copies issued by
-// one thread (the wait bounded by `polls`, a timeout flagged in `err` and
-// drained before the stage is read) and the threads then read their chunks
-// from shared memory; the chunks then hold an odd number of 16-byte vectors,
-// so the threads of a warp read distinct banks.
+// One pass over row `rowp` (pass index `pass`, from 0: consecutive passes
+// alternate the exchange slots, so a CTA never overwrites a pair another CTA
+// may still be reading; the kernel must have called cluster_started_arrive).
+// On return st.M, st.W hold the row's statistics in every CTA; st.m / st.s /
+// st.lo / st.hi / st.ch describe this CTA's chunks and st.em / st.es every
+// CTA's pair.  With `stage` (stage_bytes(V, esize) bytes of shared memory,
+// 16-byte aligned), element v of this CTA's range is left at stage[v - lo].
+// With BULK (a stage, an aligned row and `bar`, an initialised mbarrier; pass
+// p waits for its phase p & 1, so every call must stage), the range arrives
+// by bulk copies issued by one thread (the wait bounded by `polls`, a timeout
+// flagged in `err` and drained before the stage is read) and the threads then
+// read their chunks from shared memory; the chunks then hold an odd number of
+// 16-byte vectors, so the threads of a warp read distinct banks.
 template <int DT, int NT, bool BULK = false>
 __device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* rowp, int V, bool vec, float k2,
                                   ClusterRow<NT>& st, int pass, char* stage = nullptr,
@@ -126,33 +138,52 @@ __device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* 
     }
     __syncthreads();
     if (bytes > 0) (void)bulk::mbar_test_wait(bar, parity);  // each thread observes the completed phase itself
-    constexpr int UNS = 4;  // vectors per batch from shared memory
+    // the chunk is in shared memory, so it is read twice: its maximum first
+    // (four independent maxima), then its exponentials into eight independent
+    // partial sums, with no rescaling between them
     const uint4* sp = reinterpret_cast<const uint4*>(stage + (size_t)(v0 - lo) * ES);
     const int nvec = (v1 - v0) / EPL;
-    for (int base = 0; base < nvec; base += UNS) {
-      Vec16<DT> x[UNS];
-#pragma unroll
-      for (int u = 0; u < UNS; ++u)
-        if (base + u < nvec) x[u].r = sp[base + u];
-      float bm = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < UNS; ++u) {
-        if (base + u >= nvec) break;
-        bm = fmaxf(bm, x[u].vmax());
-      }
-      if (bm > m) { s *= exp2f((m - bm) * k2); m = bm; }
-      if (m != -INFINITY) {
-        float q[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int u = 0; u < UNS; ++u) {
-          if (base + u >= nvec) break;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) q[e & 3] += exp2f((x[u].elem(e) - m) * k2);
-        }
-        s += (q[0] + q[1]) + (q[2] + q[3]);
-      }
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+    int i = 0;
+    for (; i + 4 <= nvec; i += 4) {
+      Vec16<DT> x0, x1, x2, x3;
+      x0.r = sp[i];
+      x1.r = sp[i + 1];
+      x2.r = sp[i + 2];
+      x3.r = sp[i + 3];
+      m0 = fmaxf(m0, x0.vmax());
+      m1 = fmaxf(m1, x1.vmax());
+      m2 = fmaxf(m2, x2.vmax());
+      m3 = fmaxf(m3, x3.vmax());
     }
-    for (int v = v0 + nvec * EPL; v < v1; ++v) online_add(m, s, stage_elem<DT>(stage, v - lo), k2);
+    for (; i < nvec; ++i) {
+      Vec16<DT> x0;
+      x0.r = sp[i];
+      m0 = fmaxf(m0, x0.vmax());
+    }
+    for (int v = v0 + nvec * EPL; v < v1; ++v) m1 = fmaxf(m1, stage_elem<DT>(stage, v - lo));
+    m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+    if (m != -INFINITY) {
+      float qa[4] = {0.f, 0.f, 0.f, 0.f}, qb[4] = {0.f, 0.f, 0.f, 0.f};
+      for (i = 0; i + 2 <= nvec; i += 2) {
+        Vec16<DT> x0, x1;
+        x0.r = sp[i];
+        x1.r = sp[i + 1];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          qa[e & 3] += exp2f((x0.elem(e) - m) * k2);
+          qb[e & 3] += exp2f((x1.elem(e) - m) * k2);
+        }
+      }
+      if (i < nvec) {
+        Vec16<DT> x0;
+        x0.r = sp[i];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) qa[e & 3] += exp2f((x0.elem(e) - m) * k2);
+      }
+      for (int v = v0 + nvec * EPL; v < v1; ++v) qb[v & 3] += exp2f((stage_elem<DT>(stage, v - lo) - m) * k2);
+      s = ((qa[0] + qa[1]) + (qa[2] + qa[3])) + ((qb[0] + qb[1]) + (qb[2] + qb[3]));
+    }
   } else if (!BULK && vec) {
     const uint4* p = reinterpret_cast<const uint4*>(rowp) + v0 / EPL;
     const int nvec = (v1 - v0) / EPL;  // whole vectors of the chunk (only the row's last chunk has a rest)
@@ -200,6 +231,7 @@ __device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* 
   if (t == 0) { st.lo = lo; st.hi = hi; st.ch = ch; }
   __syncthreads();
   const int slot = pass & 1;
+  if (pass == 0) cluster_started_wait();
   if (t < 32) {
     float cm = -INFINITY;
     for (int i = t; i < NT; i += 32) cm = fmaxf(cm, st.m[i]);
@@ -210,16 +242,24 @@ __device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* 
       for (int i = t; i < NT; i += 32) cs += st.m[i] == -INFINITY ? 0.f : st.s[i] * exp2f((st.m[i] - cm) * k2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cs += __shfl_xor_sync(FULL, cs, o);
-    if (t == 0) { st.cm[slot] = cm; st.cs[slot] = cs; }
+    if (t < CL) {  // this CTA's pair, written into every CTA of the cluster
+      const int rank = (int)cluster.block_rank();
+      *cluster.map_shared_rank(&st.pm[slot][rank], t) = cm;
+      *cluster.map_shared_rank(&st.ps[slot][rank], t) = cs;
+    }
   }
-  cluster.sync();  // every CTA's pair of this pass is written
+  // every CTA's pair of this pass is in every CTA; no CTA reads another's
+  // shared memory, so a CTA may exit after its last pass
+  cluster.sync();
   if (t < 32) {
     // lane r folds CTA r's pair; the same butterflies over the same values in
     // every CTA give every CTA the same (M, W)
     float mr = -INFINITY, sr = 0.f;
     if (t < CL) {
-      mr = *cluster.map_shared_rank(&st.cm[slot], t);
-      sr = *cluster.map_shared_rank(&st.cs[slot], t);
+      mr = st.pm[slot][t];
+      sr = st.ps[slot][t];
+      st.em[t] = mr;
+      st.es[t] = sr;
     }
     float M = mr;
 #pragma unroll

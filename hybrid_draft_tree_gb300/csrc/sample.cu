@@ -46,11 +46,12 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
   extern __shared__ __align__(16) char s_stage[];  // this CTA's range of the current row (when staged)
   __shared__ ClusterRow<PT> st;
   __shared__ int32_t s_tok[MAX_S], s_par[MAX_S], s_rej[MAX_S];
+  __shared__ float s_rejx[MAX_S];      // the rejected tokens' logits
   __shared__ float s_x[MAX_S];         // logits of the node's children, by slot
   __shared__ float s_u[MAX_S];         // the request's acceptance uniforms, by slot
   __shared__ float s_cw[PT];           // chunk weights of the final draw
-  __shared__ int s_acc, s_nrej, s_chunk, s_pick;
-  __shared__ float s_target, s_before, s_ures;
+  __shared__ int s_acc, s_nrej, s_chunk, s_pick, s_owner;
+  __shared__ float s_target, s_before, s_ures, s_cbefore;
   __shared__ unsigned long long s_bar;  // the row staging's bulk copies
   const cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -66,12 +67,14 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
     bulk::mbar_init(&s_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  cluster_started_arrive();
   char* stage = staged ? s_stage : nullptr;
   __syncthreads();
   int32_t* out = a.out_tokens + (int64_t)b * S;
   if (s_tok[0] < 0 || s_tok[0] >= V) {  // no valid root: nothing accepted, nothing emitted (uniform in the cluster)
     if (rank == 0 && t < S) out[t] = -1;
     if (rank == 0 && t == 0) a.accept_len[b] = 0;
+    cluster_started_wait();
     grid_dependency_wait();
     return;
   }
@@ -111,7 +114,7 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
           if (seen) continue;  // a repeated token: its mass is gone
           const float pc = exp2f((s_x[j] - M) * k2) / W;
           if (s_u[j] * rem < pc) acc = j;
-          else { rem -= pc; s_rej[nrej++] = tk; }
+          else { rem -= pc; s_rejx[nrej] = s_x[j]; s_rej[nrej++] = tk; }
         }
         s_acc = acc;
         s_nrej = nrej;
@@ -126,59 +129,77 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
       continue;
     }
     // every child rejected (or a leaf): draw from the unrejected tokens.
-    // 1. chunk weights relative to M, minus the rejected tokens in the chunk
+    // 1. every CTA's weight relative to M, from the pairs the statistics
+    //    exchanged, minus the rejected tokens in its range: the same values in
+    //    every CTA, so each finds the CTA holding the target by itself
     const int nrej = s_nrej;
-    const int ch = st.ch, lo = st.lo, hi = st.hi;
-    // element v of this CTA's range
-    auto elem = [&](int v) { return stage ? stage_elem<DT>(stage, v - lo) : load_scalar<DT>(rowp, v); };
-    const int c0 = min(lo + t * ch, hi), c1 = min(c0 + ch, hi);
-    float cw = st.m[t] == -INFINITY ? 0.f : st.s[t] * exp2f((st.m[t] - M) * k2);
-    for (int q = 0; q < nrej; ++q) {
-      const int32_t r = s_rej[q];
-      if (r >= c0 && r < c1) cw -= exp2f((elem(r) - M) * k2);
-    }
-    cw = fmaxf(cw, 0.f);
-    s_cw[t] = cw;
-    __syncthreads();
-    // 2. warp 0: lane l sums chunks CPL*l .. CPL*l + CPL-1 in order, a warp
-    //    scan orders the lanes (a fixed summation order); the CTA's weight goes
-    //    to the other CTAs, which fold the CL weights in rank order
-    constexpr int CPL = PT / 32;
-    float w8[CPL];
-    float lsum = 0.f, incl = 0.f;
     if (warp == 0) {
-#pragma unroll
-      for (int i = 0; i < CPL; ++i) { w8[i] = s_cw[lane * CPL + i]; lsum += w8[i]; }
-      incl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o) incl += y;
+      float wr = 0.f;
+      if (lane < CL) {
+        const float cmr = st.em[lane], csr = st.es[lane];
+        wr = cmr == -INFINITY ? 0.f : csr * exp2f((cmr - M) * k2);
+        int rlo, rhi;
+        cta_range(V, a.g.vec ? Vec16<DT>::EPL : 1, lane, rlo, rhi);
+        for (int q = 0; q < nrej; ++q) {
+          const int32_t r = s_rej[q];
+          if (r >= rlo && r < rhi) wr -= exp2f((s_rejx[q] - M) * k2);
+        }
+        wr = fmaxf(wr, 0.f);
       }
-      if (lane == 31) st.ct = incl;
-    }
-    cluster.sync();  // every CTA's weight is written
-    int owner = -1;
-    float before_cta = 0.f, target = 0.f;
-    if (warp == 0) {
-      const float cwr = lane < CL ? *cluster.map_shared_rank(&st.ct, lane) : 0.f;
-      float ci = cwr;  // inclusive scan over the ranks
+      float ci = wr;  // inclusive scan over the ranks
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float y = __shfl_up_sync(FULL, ci, o);
         if (lane >= o) ci += y;
       }
       const float total = __shfl_sync(FULL, ci, CL - 1);
-      target = s_ures * total;
-      const unsigned hit = __ballot_sync(FULL, lane < CL && cwr > 0.f && ci > target);
-      const unsigned any = __ballot_sync(FULL, lane < CL && cwr > 0.f);
-      owner = hit ? __ffs(hit) - 1 : (any ? 31 - __clz(any) : -1);  // else rounding: the last CTA with weight
-      before_cta = __shfl_sync(FULL, ci - cwr, owner >= 0 ? owner : 0);
+      const float target = s_ures * total;
+      const unsigned hit = __ballot_sync(FULL, lane < CL && wr > 0.f && ci > target);
+      const unsigned any = __ballot_sync(FULL, lane < CL && wr > 0.f);
+      const int own = hit ? __ffs(hit) - 1 : (any ? 31 - __clz(any) : -1);  // else rounding: the last CTA with weight
+      const float bc = __shfl_sync(FULL, ci - wr, own >= 0 ? own : 0);
+      if (lane == 0) {
+        s_owner = own;
+        s_cbefore = bc;
+        s_target = target;
+      }
     }
-    cluster.sync();  // the weights are read: no CTA's shared memory is accessed from here on
-    if (warp == 0 && owner < 0 && rank == 0 && lane == 0) s_pick = -1;  // no token has weight
+    __syncthreads();
+    const int owner = s_owner;
+    if (owner < 0 && rank == 0 && t == 0) s_pick = -1;  // no token has weight
+    const int ch = st.ch, lo = st.lo, hi = st.hi;
+    // element v of this CTA's range
+    auto elem = [&](int v) { return stage ? stage_elem<DT>(stage, v - lo) : load_scalar<DT>(rowp, v); };
+    constexpr int CPL = PT / 32;
+    float w8[CPL];
+    float lsum = 0.f, incl = 0.f;
+    if (owner == rank) {
+      // 2. this CTA holds the target: its chunk weights, minus the rejected
+      //    tokens in each chunk; warp 0's lane l sums chunks CPL*l ..
+      //    CPL*l + CPL-1 in order and a warp scan orders the lanes
+      const int c0 = min(lo + t * ch, hi), c1 = min(c0 + ch, hi);
+      float cw = st.m[t] == -INFINITY ? 0.f : st.s[t] * exp2f((st.m[t] - M) * k2);
+      for (int q = 0; q < nrej; ++q) {
+        const int32_t r = s_rej[q];
+        if (r >= c0 && r < c1) cw -= exp2f((elem(r) - M) * k2);
+      }
+      cw = fmaxf(cw, 0.f);
+      s_cw[t] = cw;
+      __syncthreads();  // (uniform in the CTA)
+      if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) { w8[i] = s_cw[lane * CPL + i]; lsum += w8[i]; }
+        incl = lsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(FULL, incl, o);
+          if (lane >= o) incl += y;
+        }
+      }
+    }
+    const float before_cta = s_cbefore, target = s_target;
     if (warp == 0 && owner == rank) {
-      // 3. this CTA holds the target: its chunk, from the lanes' sums
+      // 3. its chunk, from the lanes' sums
       float run = before_cta + incl - lsum;  // weight before this lane's chunks
       int c = -1, last = -1;
       float cb = 0.f, last_before = 0.f;
