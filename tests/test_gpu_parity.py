@@ -788,6 +788,63 @@ def test_verify_request_without_valid_slots(scan_kernel):
     eng.close()
 
 
+@pytest.mark.parametrize("dtype,pad", [(W.BF16, 0), (W.F32, 0), (W.BF16, 3)])
+def test_stochastic_request_without_valid_slots(dtype, pad):
+    """Stochastic verification with an all-pad request beside valid ones, on
+    the walk's bulk-staged rows (aligned) and its thread-loaded rows (a padded
+    stride): the empty request's cluster leaves at once (nothing accepted,
+    nothing emitted), and every other request matches the oracle's fp64 walk
+    on the same uniforms."""
+    g_ = G()
+    rng = np.random.default_rng(41 + pad)
+    V, B, S = 5003, 4, 61
+    vals = (rng.normal(size=(B * S, V)) * 2.0).astype(np.float32)
+    host = (vals.view(np.uint32) >> 16).astype(np.uint16) if dtype == W.BF16 else vals
+    hb = host.reshape(B, S, V)  # the oracle's input: float32, or bf16 as uint16 bit patterns
+    hr = (host.astype(np.uint32) << 16).view(np.float32).reshape(B, S, V) if dtype == W.BF16 else hb
+    trees = []
+    for b in range(B):
+        n = 0 if b == 2 else int(rng.integers(1, S + 1))
+        tok = np.full(S, -1, np.int32)
+        par = np.full(S, -1, np.int32)
+        tok[:n] = rng.integers(0, V, n)
+        for i in range(1, n):
+            par[i] = rng.integers(0, i)
+            if rng.random() < 0.6:
+                tok[i] = int(np.argmax(hr[b, par[i]]))
+        trees.append(_tree_from_parents(tok, par))
+    stride = V + pad
+    buf = np.zeros((B * S, stride), host.dtype)
+    buf[:, :V] = host
+    logits = u16_to_bf16_tensor(buf.reshape(-1)).view(B * S, stride) if dtype == W.BF16 else torch.from_numpy(buf).cuda()
+    eng = g_.Graft(g_.graft_default_config(V, B, 0, dtype))
+    tt = torch.from_numpy(np.stack([t.tok for t in trees])).cuda()
+    tp = torch.from_numpy(np.stack([t.par for t in trees]).astype(np.int8)).cuda()
+    tpos = torch.from_numpy(np.stack([t.pos for t in trees])).cuda()
+    tm = torch.from_numpy(np.stack([t.mask for t in trees]).view(np.int64)).cuda()
+    u = rng.random((B, S)).astype(np.float32)
+    ur = rng.random(B).astype(np.float32)
+    acc = torch.full((B,), 77, dtype=torch.int32, device="cuda")
+    out = torch.full((B, S), 77, dtype=torch.int32, device="cuda")
+    eng.verify_update_sample(B, tt, tp, tpos, tm, logits, 1.0, torch.from_numpy(u).cuda(), torch.from_numpy(ur).cuda(),
+                             acc, out)
+    acc_g, out_g = acc.cpu().numpy(), out.cpu().numpy()
+    assert acc_g[2] == 0 and (out_g[2] == -1).all()
+    C = oracle.new_matrix(V)
+    compared = 0
+    for b in (0, 1, 3):
+        a, o, margin = oracle.verify_sample(trees[b], hb[b], dtype, 1.0, u[b].astype(np.float64), float(ur[b]))
+        if margin > 2e-5:
+            compared += 1
+            assert acc_g[b] == a and np.array_equal(out_g[b], o), (b, acc_g[b], a, out_g[b], o)
+        _, _, topk = oracle.verify(trees[b], hb[b], dtype)
+        oracle.update(C, trees[b], topk)
+    assert compared >= 2
+    assert np.array_equal(eng.get_matrix(), C)
+    assert eng.sync() == 0
+    eng.close()
+
+
 def test_stochastic_walk_wait_limit_expires_and_the_handle_recovers():
     """The stochastic walk's staging wait (bulk copies on an mbarrier) gets a
     limit of one poll: the kernel flags GRAFT_ERR_TIMEOUT, lets its copies
