@@ -16,9 +16,10 @@
 // (row_softmax.cuh: each node's row is read once, split over the cluster's
 // SMs, each CTA keeping its range in shared memory).  Every CTA takes the same
 // decisions from the same statistics, so the walk needs no further exchange;
-// the final draw exchanges the CTAs' weights once, and the CTA holding the
-// target finds its chunk and one warp scans it in shared memory, so no second
-// pass over the row is needed.  The top-8 and matrix update come
+// for the final draw every CTA derives every CTA's weight from the exchanged
+// (max, sum) pairs, so all agree on the CTA holding the target without another
+// exchange, and that CTA finds its chunk and one warp scans it in shared
+// memory, so no second pass over the row is needed.  The top-8 and matrix update come
 // from the scan kernels as in greedy verification; this kernel reads only the
 // logits and the trees, so it is launched as a programmatic dependent of the
 // update kernel and runs beside it (it waits for that kernel only before it
