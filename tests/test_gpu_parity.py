@@ -156,6 +156,24 @@ def test_lockstep_small(wid, V, B, sigma, steps):
     assert any(a > 0 for _, a in stats)
 
 
+@pytest.mark.parametrize("seed", range(40))
+def test_lockstep_random_configurations(seed):
+    """Seeded random configurations (mode, logits type, vocabulary, batch,
+    draft spread and verify path drawn together), four closed-loop steps
+    each against the oracle: combinations the hand-picked cases above leave
+    out (e.g. fp32 static trees on the cluster verify, small tail batches on
+    the unit-record scan)."""
+    rng = np.random.default_rng(1000 + seed)
+    wid = int(rng.choice([0, 1, 2, 4]))
+    V = int(rng.integers(300, 50001))
+    dtype = int(rng.choice([W.F32, W.BF16]))
+    B = int(rng.integers(1, 9)) if wid != 4 else int(rng.integers(1, 65))
+    sigma = float(rng.choice([0.5, 0.75, 2.0]))
+    scan_kernel = int(rng.choice([0, 1, 2, 3, 4, 5]))
+    w = W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=sigma, dtype=dtype)
+    lockstep(w, 4, check_rows=2, scan_kernel=scan_kernel)
+
+
 @pytest.mark.parametrize("wid,V,B,sigma", [(0, 3000, 3, 0.75), (2, 777, 16, 0.75), (4, 6007, 64, 2.0)])
 def test_slot_provenance(wid, V, B, sigma):
     """graft_assemble_src writes the same trees as graft_assemble (compared
