@@ -453,7 +453,7 @@ def test_stochastic_verification_full_size_static():
     _stochastic_case(W.WORKLOADS[2].scaled(bias=20.0, hit_rate=1.0), 1.0, 2, 99)
 
 
-def _stochastic_case(w, temp, steps, seed, min_fraction=0.5, **cfg):
+def _stochastic_case(w, temp, steps, seed, min_fraction=0.5, need_accept=True, **cfg):
     from workloads.device_loop import DeviceLoop
     eng = engine_for(w, **cfg)
     loop = DeviceLoop(w, eng)
@@ -491,8 +491,27 @@ def _stochastic_case(w, temp, steps, seed, min_fraction=0.5, **cfg):
         assert np.array_equal(eng.get_matrix(), C), step
         loop.advance()
     assert eng.sync() == 0
-    assert compared >= min_fraction * total and accepted > 0, (compared, total, accepted)
+    assert compared >= min_fraction * total and (accepted > 0 or not need_accept), (compared, total, accepted)
     eng.close()
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_stochastic_random_configurations(seed):
+    """Seeded random configurations of the stochastic walk (mode, logits
+    type, vocabulary, batch, temperature, verify path) in closed loop against
+    the oracle's fp64 walk on the same uniforms."""
+    rng = np.random.default_rng(2000 + seed)
+    wid = int(rng.choice([0, 1, 2, 4]))
+    # the draw is compared only where the target lies more than 2e-5 of the
+    # mass from a token boundary: vocabularies and temperatures that keep
+    # most draws comparable
+    V = int(rng.integers(300, 12001))
+    dtype = int(rng.choice([W.F32, W.BF16]))
+    B = int(rng.integers(1, 7)) if wid != 4 else int(rng.integers(1, 33))
+    temp = float(rng.choice([0.25, 0.5, 1.0]))
+    scan_kernel = int(rng.choice([0, 3, 5]))
+    w = W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=0.75, dtype=dtype)
+    _stochastic_case(w, temp, 4, 3000 + seed, min_fraction=0.3, need_accept=False, scan_kernel=scan_kernel)
 
 
 @pytest.mark.parametrize("dtype,V,n,distinct,pad", [
@@ -522,6 +541,33 @@ def test_warmup_paths_match_oracle(dtype, V, n, distinct, pad):
         C = oracle.new_matrix(V)
         oracle.warmup(C, toks, host_rows, dtype)
         assert np.array_equal(eng.get_matrix(), C), call
+    assert eng.sync() == 0
+    eng.close()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_warmup_random_configurations(seed):
+    """Seeded random warm-up loads (logits type, vocabulary, row count,
+    distinct tokens, row padding) against the oracle's row-by-row load."""
+    g_ = G()
+    rng = np.random.default_rng(4000 + seed)
+    dtype = int(rng.choice([W.F32, W.BF16]))
+    V = int(rng.integers(100, 40001))
+    n = int(rng.integers(1, max(2, min(6000, 40_000_000 // V))))
+    distinct = int(rng.integers(1, min(V, n) + 1))
+    pad = int(rng.choice([0, 0, 1, 3]))
+    pool = rng.choice(V, distinct, replace=False).astype(np.int32)
+    toks = pool[rng.integers(0, distinct, n)]
+    vals = rng.normal(size=(n, V)).astype(np.float32)
+    host_rows = (vals.view(np.uint32) >> 16).astype(np.uint16) if dtype == W.BF16 else vals
+    buf = np.zeros((n, V + pad), host_rows.dtype)
+    buf[:, :V] = host_rows
+    dev = u16_to_bf16_tensor(buf) if dtype == W.BF16 else torch.from_numpy(buf).cuda()
+    eng = g_.Graft(g_.graft_default_config(V, 1, 0, dtype))
+    eng.warmup(torch.from_numpy(toks).cuda(), dev[:, :V])
+    C = oracle.new_matrix(V)
+    oracle.warmup(C, toks, host_rows, dtype)
+    assert np.array_equal(eng.get_matrix(), C), (dtype, V, n, distinct, pad)
     assert eng.sync() == 0
     eng.close()
 
