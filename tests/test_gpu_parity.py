@@ -382,13 +382,27 @@ def test_coverage_gain_matches_oracle(wid, B):
     _coverage_case(W.WORKLOADS[wid].scaled(V=5000, B=B, draft_sigma=0.75), 10)
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_coverage_gain_random_configurations(seed):
+    """The coverage diagnostic on seeded random configurations (checkpoint
+    or tail mode, logits type, vocabulary with ragged tails, batch, draft
+    spread) against the oracle's fp64 value."""
+    rng = np.random.default_rng(5000 + seed)
+    wid = int(rng.choice([0, 1, 4]))
+    V = int(rng.integers(300, 60001))
+    dtype = int(rng.choice([W.F32, W.BF16]))
+    B = int(rng.integers(1, 7)) if wid != 4 else int(rng.integers(1, 65))
+    sigma = float(rng.choice([0.5, 0.75, 2.0]))
+    _coverage_case(W.WORKLOADS[wid].scaled(V=V, B=B, draft_sigma=sigma, dtype=dtype), 8, need_gain=False)
+
+
 @pytest.mark.slow
 def test_coverage_gain_full_size_tail():
     """The same on the tail workload at full size (64 requests, V = 151936)."""
     _coverage_case(W.WORKLOADS[4], 2)
 
 
-def _coverage_case(w, steps):
+def _coverage_case(w, steps, need_gain=True):
     from workloads.device_loop import DeviceLoop
     B = w.B
     eng = engine_for(w)
@@ -411,8 +425,9 @@ def _coverage_case(w, steps):
             seen += exp > 0
         loop.verify_update()
         loop.advance()
-    assert seen > 0
+    assert seen > 0 or not need_gain
     eng.close()
+    return seen
 
 
 @pytest.mark.parametrize("wid,B,temp", [(0, 4, 1.0), (0, 4, 0.7), (2, 4, 1.0), (4, 8, 1.5)])
