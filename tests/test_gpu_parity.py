@@ -442,6 +442,15 @@ def test_stochastic_verification_matches_oracle(wid, B, temp):
     _stochastic_case(w, temp, 10, wid * 10 + int(temp * 10))
 
 
+@pytest.mark.parametrize("wid,B,temp,dtype", [(4, 64, 1.0, W.BF16), (4, 48, 0.5, W.F32), (2, 40, 0.5, W.BF16),
+                                               (2, 32, 1.0, W.F32)])
+def test_stochastic_verification_many_requests(wid, B, temp, dtype):
+    """Batches of 32 requests and more: more clusters than fit beside pass 2's
+    CTAs at once, so the walk's CTAs start in several waves."""
+    w = W.WORKLOADS[wid].scaled(V=6007 if wid == 4 else 7001, B=B, draft_sigma=0.75, dtype=dtype)
+    _stochastic_case(w, temp, 5, 60 + B, min_fraction=0.4)
+
+
 @pytest.mark.parametrize("V,B", [(100003, 2), (330007, 1)])
 def test_stochastic_verification_long_fp32_rows(V, B):
     """fp32 rows whose eighth per cluster CTA needs more than the default 48 KB
