@@ -717,7 +717,8 @@ int graft_verify_update_sample(graft_handle* h, int32_t batch, const int32_t* d_
                                const float* d_u_resid, int32_t* d_accept_len, int32_t* d_out_tokens, void* stream) {
   NvtxRange nvtx("graft_verify_update_sample");
   if (!h) return GRAFT_EINVAL;
-  if (!(temperature > 0.f) || !std::isfinite(temperature)) return fail(h, GRAFT_EINVAL, "temperature must be > 0");
+  if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(1.f / temperature))
+    return fail(h, GRAFT_EINVAL, "temperature must be finite and > 0, with a finite inverse");
   if (batch > 0 && (!d_u_accept || !d_u_resid)) return fail(h, GRAFT_EINVAL, "null pointer");
   return verify_impl(h, batch, d_tree_tok, d_tree_parent, d_tree_pos, d_tree_mask, d_logits, row_stride, d_accept_len,
                      d_out_tokens, true, temperature, d_u_accept, d_u_resid, stream);

@@ -283,7 +283,8 @@ int graft_verify_update(graft_handle* h, int32_t batch, const int32_t* d_tree_to
  *   d_u_resid   DEVICE float [batch], uniforms in [0, 1)
  *   d_accept_len[b] = accepted path length; d_out_tokens[b] = path tokens,
  *   then the final token, then -1s.  Probabilities are computed in fp32.
- * Asynchronous; GRAFT_EINVAL for a temperature that is not finite and > 0. */
+ * Asynchronous; GRAFT_EINVAL for a temperature that is not finite and > 0,
+ * or whose inverse is not finite (below about 3e-39). */
 int graft_verify_update_sample(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const int8_t* d_tree_parent,
                                const int32_t* d_tree_pos, const uint64_t* d_tree_mask, const void* d_logits,
                                int64_t row_stride, float temperature, const float* d_u_accept,

@@ -1070,6 +1070,22 @@ def test_invalid_arguments_are_rejected():
                      torch.ones((2, 4), device="cuda"), 0, ev)
     with pytest.raises(g_.GraftError):
         eng.check(2, torch.zeros((2, 4), dtype=torch.int16, device="cuda"), torch.ones((2, 4), device="cuda"), -1, ev)
+    tok = torch.full((2, eng.S), -1, dtype=torch.int32, device="cuda")    # a root (token 0) and pads
+    tok[:, 0] = 0
+    par = torch.full((2, eng.S), -1, dtype=torch.int8, device="cuda")
+    pos = torch.full((2, eng.S), -1, dtype=torch.int32, device="cuda")
+    pos[:, 0] = 0
+    mask = torch.zeros((2, eng.S), dtype=torch.int64, device="cuda")
+    mask[:, 0] = 1
+    lg = torch.zeros((2 * eng.S, 100), dtype=torch.bfloat16, device="cuda")
+    u, ur = torch.full((2, eng.S), 0.5, device="cuda"), torch.full((2,), 0.5, device="cuda")
+    acc = torch.empty(2, dtype=torch.int32, device="cuda")
+    out = torch.empty((2, eng.S), dtype=torch.int32, device="cuda")
+    for temp in (0.0, -1.0, float("inf"), float("nan"), 1e-39):   # the last: a subnormal with an infinite inverse
+        with pytest.raises(g_.GraftError):
+            eng.verify_update_sample(2, tok, par, pos, mask, lg, temp, u, ur, acc, out)
+    eng.verify_update_sample(2, tok, par, pos, mask, lg, 1e-30, u, ur, acc, out)     # tiny but invertible
+    assert eng.sync() == 0
     for mode, kw in ((0, dict(topk=4)), (1, dict(ablation=1)), (2, dict(ablation=2)), (0, dict(ablation=3)),
                      (0, dict(ablation=2, fixed_draft=61)), (0, dict(tpl_width=65)), (0, dict(tpl_depth=17)),
                      (0, dict(scan_kernel=6)), (0, dict(scan_kernel=-1))):
