@@ -166,6 +166,11 @@ int check_cfg(const graft_config* c, graft_handle* h) {
     for (int k = 0; k < 3; ++k)
       if (c->ckpt_draft[k] < 0 || c->ckpt_draft[k] > c->budget || c->ckpt_depth[k] < 0)
         return fail(h, GRAFT_EINVAL, "checkpoint %d: draft slots must be in [0, budget], depth >= 0", k);
+  for (int k = 0; k < 3; ++k)
+    if (!(c->ckpt_thr[k] >= 0.f && c->ckpt_thr[k] <= 1.f))
+      return fail(h, GRAFT_EINVAL, "checkpoint threshold %d must be in [0, 1]", k);
+  if (!(c->static_thr >= 0.f && c->static_thr <= 1.f) || !(c->tail_thr >= 0.f && c->tail_thr <= 1.f))
+    return fail(h, GRAFT_EINVAL, "static and tail thresholds must be in [0, 1]");
   if (c->tpl_depth < 1 || c->tpl_depth > 16 || c->tpl_width < 1 || c->tpl_width > 64)
     return fail(h, GRAFT_EINVAL, "template depth must be in [1, 16] and width in [1, 64]");
   if (c->ablation < 0 || c->ablation > 2 || (c->ablation != 0 && c->mode != GRAFT_MODE_CHECKPOINT))

@@ -81,12 +81,12 @@ typedef struct {
   int32_t mode;           /* graft_mode */
   int32_t logits_dtype;   /* graft_dtype of every logits buffer */
   int32_t ckpt_depth[3];  /* checkpoint draft layers, checked in this order (0, 1, 5) */
-  float ckpt_thr[3];      /* fire when the layer's best path confidence < thr (0.30, 0.20, 0.10) */
+  float ckpt_thr[3];      /* fire when the layer's best path confidence < thr (0.30, 0.20, 0.10); in [0, 1] */
   int32_t ckpt_draft[3];  /* draft slots kept when that checkpoint fires (8, 24, 40); retrieval gets the rest */
   int32_t tpl_depth;      /* retrieval template depth (8) */
   int32_t tpl_width;      /* template root width; rank-r node fan-out max(1, width >> r), at most 8 (8) */
-  float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15) */
-  float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4) */
+  float static_thr;       /* static mode: nodes with path confidence < thr are replaced (0.15); in [0, 1] */
+  float tail_thr;         /* tail mode: first block position with confidence < thr starts the tail (0.4); in [0, 1] */
   int32_t max_draft_nodes;/* largest draft tree (<= 256) or block (<= budget) per request */
   int32_t scan_kernel;    /* verify scan: 0 = automatic (cluster per row when every row's
                              cluster fits on the GPU at once and a row's eighth is at most

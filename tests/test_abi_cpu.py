@@ -105,7 +105,9 @@ def test_config_validation_before_any_device_call():
            dict(mode=3), dict(dtype=2), dict(ckpt_draft=(8, 24, 61)), dict(ckpt_depth=(0, -1, 5)),
            dict(tpl_depth=0), dict(tpl_depth=17), dict(tpl_width=0), dict(tpl_width=65), dict(ablation=3),
            dict(ablation=1, mode=g.GRAFT_MODE_STATIC), dict(ablation=2, fixed_draft=61), dict(max_draft_nodes=-1),
-           dict(max_draft_nodes=17, mode=g.GRAFT_MODE_TAIL), dict(scan_kernel=6)]
+           dict(max_draft_nodes=17, mode=g.GRAFT_MODE_TAIL), dict(scan_kernel=6), dict(ckpt_thr=(0.3, 1.5, 0.1)),
+           dict(ckpt_thr=(float("nan"), 0.2, 0.1)), dict(static_thr=-0.1, mode=g.GRAFT_MODE_STATIC),
+           dict(tail_thr=float("inf"), mode=g.GRAFT_MODE_TAIL)]
     for kw in bad:
         assert init(**dict(kw)) == gb.GRAFT_EINVAL, kw
 
