@@ -319,6 +319,8 @@ int graft_warmup(graft_handle* h, const int32_t* d_tokens, const void* d_logits,
   if (n_rows == 0) return GRAFT_OK;
   if (!d_tokens || !d_logits) return fail(h, GRAFT_EINVAL, "null pointer");
   if (row_stride < h->cfg.vocab) return fail(h, GRAFT_EINVAL, "row_stride < vocab");
+  if (graft::misaligned(d_tokens, 4) || graft::misaligned(d_logits, h->cfg.logits_dtype == GRAFT_BF16 ? 2 : 4))
+    return fail(h, GRAFT_EINVAL, "a buffer is not aligned to its element size");
   graft::WarmArgs a{};
   a.g = scan_geom(h, d_logits, row_stride, n_rows, 0);
   a.g.nsplit = 1;
@@ -407,6 +409,11 @@ int assemble_impl(graft_handle* h, int32_t batch, const int32_t* d_root_tok, con
     return fail(h, GRAFT_EINVAL, "null pointer");
   if (draft_nodes > 0 && (!d_draft_tok || !d_draft_aux || (c.mode != GRAFT_MODE_TAIL && !d_draft_parent)))
     return fail(h, GRAFT_EINVAL, "null draft pointer");
+  if (graft::misaligned(d_root_tok, 4) || graft::misaligned(d_draft_tok, 4) || graft::misaligned(d_draft_parent, 2) ||
+      graft::misaligned(d_draft_aux, 4) || graft::misaligned(d_event, 4) || graft::misaligned(d_retrieved, 4) ||
+      graft::misaligned(d_tree_tok, 4) || graft::misaligned(d_tree_pos, 4) || graft::misaligned(d_tree_mask, 8) ||
+      graft::misaligned(d_info, 4))
+    return fail(h, GRAFT_EINVAL, "a buffer is not aligned to its element size");
   graft::AssembleArgs a = assemble_args(h, batch, draft_nodes);
   a.root_tok = d_root_tok; a.draft_tok = d_draft_tok; a.draft_parent = d_draft_parent; a.draft_aux = d_draft_aux;
   a.event_in = d_event;
@@ -460,6 +467,8 @@ int graft_check(graft_handle* h, int32_t batch, const int16_t* d_draft_parent, c
   if (layer < 0) return fail(h, GRAFT_EINVAL, "layer must be >= 0");
   if (batch == 0) return GRAFT_OK;
   if (!d_event || (draft_nodes > 0 && (!d_draft_parent || !d_draft_prob))) return fail(h, GRAFT_EINVAL, "null pointer");
+  if (graft::misaligned(d_event, 4) || graft::misaligned(d_draft_parent, 2) || graft::misaligned(d_draft_prob, 4))
+    return fail(h, GRAFT_EINVAL, "a buffer is not aligned to its element size");
   if (c.ablation == 2) return GRAFT_OK;  // the fixed split has no checkpoints
   graft::AssembleArgs a = assemble_args(h, batch, draft_nodes);
   a.draft_parent = d_draft_parent; a.draft_aux = d_draft_prob; a.layer = layer;
@@ -483,6 +492,8 @@ int graft_retrieve(graft_handle* h, int32_t batch, const int32_t* d_root_tok, co
   if (batch < 0 || batch > c.max_batch) return fail(h, GRAFT_EINVAL, "batch %d outside [0, %d]", batch, c.max_batch);
   if (batch == 0) return GRAFT_OK;
   if (!d_root_tok || !d_event || !d_retrieved) return fail(h, GRAFT_EINVAL, "null pointer");
+  if (graft::misaligned(d_root_tok, 4) || graft::misaligned(d_event, 4) || graft::misaligned(d_retrieved, 4))
+    return fail(h, GRAFT_EINVAL, "a buffer is not aligned to its element size");
   graft::AssembleArgs a = assemble_args(h, batch, 0);
   a.root_tok = d_root_tok;
   cudaError_t e;
@@ -520,6 +531,8 @@ int graft_confidence(graft_handle* h, int32_t batch, const int16_t* d_draft_pare
     return fail(h, GRAFT_EINVAL, "draft_nodes %d outside [0, %d]", draft_nodes, c.max_draft_nodes);
   if (batch == 0) return GRAFT_OK;
   if (!d_best || (draft_nodes > 0 && (!d_draft_parent || !d_draft_prob))) return fail(h, GRAFT_EINVAL, "null pointer");
+  if (graft::misaligned(d_best, 4) || graft::misaligned(d_draft_parent, 2) || graft::misaligned(d_draft_prob, 4))
+    return fail(h, GRAFT_EINVAL, "a buffer is not aligned to its element size");
   graft::AssembleArgs a = assemble_args(h, batch, draft_nodes);
   a.draft_parent = d_draft_parent; a.draft_aux = d_draft_prob; a.layer = INT32_MAX;
   cudaError_t e;
@@ -589,6 +602,9 @@ int graft_coverage(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, co
   if (batch == 0) return GRAFT_OK;
   if (!d_tree_tok || !d_tree_parent || !d_info || !d_logits || !d_gain) return fail(h, GRAFT_EINVAL, "null pointer");
   if (row_stride < c.vocab) return fail(h, GRAFT_EINVAL, "row_stride < vocab");
+  if (graft::misaligned(d_tree_tok, 4) || graft::misaligned(d_info, 4) || graft::misaligned(d_gain, 4) ||
+      graft::misaligned(d_logits, c.logits_dtype == GRAFT_BF16 ? 2 : 4))
+    return fail(h, GRAFT_EINVAL, "a buffer is not aligned to its element size");
   graft::VerifyArgs a{};
   a.g = scan_geom(h, d_logits, row_stride, (int64_t)batch * h->S, h->scan_ctas_target);  // 16-byte loads when aligned
   a.S = h->S; a.batch = batch; a.logits = d_logits;
@@ -631,6 +647,10 @@ int verify_impl(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const
   if (!d_tree_tok || !d_tree_parent || !d_tree_pos || !d_tree_mask || !d_logits || !d_accept_len || !d_out_tokens)
     return fail(h, GRAFT_EINVAL, "null pointer");
   if (row_stride < c.vocab) return fail(h, GRAFT_EINVAL, "row_stride < vocab");
+  if (graft::misaligned(d_tree_tok, 4) || graft::misaligned(d_tree_pos, 4) || graft::misaligned(d_tree_mask, 8) ||
+      graft::misaligned(d_logits, c.logits_dtype == GRAFT_BF16 ? 2 : 4) || graft::misaligned(d_accept_len, 4) ||
+      graft::misaligned(d_out_tokens, 4) || graft::misaligned(d_u_accept, 4) || graft::misaligned(d_u_resid, 4))
+    return fail(h, GRAFT_EINVAL, "a buffer is not aligned to its element size");
   const int64_t rows = (int64_t)batch * h->S;
   graft::VerifyArgs a{};
   a.g = scan_geom(h, d_logits, row_stride, rows, h->scan_ctas_target);

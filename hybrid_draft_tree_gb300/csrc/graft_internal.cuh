@@ -68,6 +68,11 @@ struct ScanGeom {
   int64_t row_vec_bytes;  // bytes of a row's full 16-byte vectors
 };
 
+// True when device pointer p is not aligned to a (a power of two) bytes;
+// the ABI refuses such buffers (a null pointer counts as aligned: the null
+// checks are separate).
+inline bool misaligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
+
 struct VerifyArgs {
   ScanGeom g;
   int32_t S, batch;

@@ -127,6 +127,10 @@ extern "C" int graft_verify_update_noalloc(int32_t vocab, int32_t logits_dtype, 
   if (!d_tree_tok || !d_tree_parent || !d_tree_pos || !d_tree_mask || !d_logits || !d_matrix || !d_accept_len ||
       !d_out_tokens || !d_err_flags)
     return GRAFT_EINVAL;
+  if (graft::misaligned(d_tree_tok, 4) || graft::misaligned(d_tree_pos, 4) || graft::misaligned(d_tree_mask, 8) ||
+      graft::misaligned(d_logits, logits_dtype == GRAFT_BF16 ? 2 : 4) || graft::misaligned(d_matrix, 4) ||
+      graft::misaligned(d_accept_len, 4) || graft::misaligned(d_out_tokens, 4) || graft::misaligned(d_err_flags, 4))
+    return GRAFT_EINVAL;  // a buffer not aligned to its element size
   DeviceSetup* dev = nullptr;
   const int rc = setup_current_device(stream, &dev);
   if (rc != GRAFT_OK) return rc;

@@ -28,7 +28,10 @@
  * Conventions (all entry points):
  *   - Pointers named d_* are DEVICE pointers owned by the caller; they must
  *     stay valid until the work queued on `stream` has finished.  `stream` is
- *     a cudaStream_t (NULL = legacy default stream).
+ *     a cudaStream_t (NULL = legacy default stream).  Each must be aligned to
+ *     its element size (GRAFT_EINVAL otherwise); the logits are read with
+ *     16-byte loads when the rows start on 16-byte boundaries, with element
+ *     loads otherwise.
  *   - Every call is asynchronous and stream-ordered unless stated otherwise.
  *     Argument errors are returned at once and nothing is queued.
  *   - Device-side data errors (token id out of range, NaN logits or

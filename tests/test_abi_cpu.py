@@ -124,15 +124,21 @@ def test_noalloc_argument_checks_before_any_device_call():
     L = g.load()
     some = ctypes.c_void_p(4096)            # never dereferenced: every call below returns before any access
 
-    def call(V=1000, dt=g.GRAFT_BF16, B=2, S=61, stride=1000, ptr=some):
-        return L.graft_verify_update_noalloc(V, dt, B, S, ptr, ptr, ptr, ptr, ptr, ctypes.c_int64(stride), ptr, ptr,
+    def call(V=1000, dt=g.GRAFT_BF16, B=2, S=61, stride=1000, ptr=some, logits=None, mask=None):
+        lg = ptr if logits is None else logits
+        mk = ptr if mask is None else mask
+        return L.graft_verify_update_noalloc(V, dt, B, S, ptr, ptr, ptr, mk, lg, ctypes.c_int64(stride), ptr, ptr,
                                              ptr, ptr, ctypes.c_void_p(0))
 
     assert call(B=0) == gb.GRAFT_OK
     for kw in (dict(V=0), dict(dt=2), dict(S=0), dict(S=65), dict(B=-1), dict(B=2048 // 61 + 1), dict(stride=999),
-               dict(ptr=ctypes.c_void_p(None))):
+               dict(ptr=ctypes.c_void_p(None)), dict(ptr=ctypes.c_void_p(4098)),       # int32 buffers off 4 bytes
+               dict(logits=ctypes.c_void_p(4097)),                                      # bf16 logits off 2 bytes
+               dict(dt=g.GRAFT_F32, logits=ctypes.c_void_p(4098)),                      # fp32 logits off 4 bytes
+               dict(mask=ctypes.c_void_p(4100))):                                       # uint64 masks off 8 bytes
         assert call(**kw) == gb.GRAFT_EINVAL, kw
     assert call() not in (gb.GRAFT_OK, gb.GRAFT_EINVAL)     # valid arguments: stops at the missing device
+    assert call(logits=ctypes.c_void_p(4098)) not in (gb.GRAFT_OK, gb.GRAFT_EINVAL)   # bf16 on a 2-byte boundary
 
 
 def test_product_code_never_loads_the_oracle():

@@ -8,6 +8,8 @@ rows that overflow the candidate list (all-equal values), warm-up, the
 device-side error flags, and full-size cases in the benchmark's launch
 configuration.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -1085,6 +1087,17 @@ def test_invalid_arguments_are_rejected():
         with pytest.raises(g_.GraftError):
             eng.verify_update_sample(2, tok, par, pos, mask, lg, temp, u, ur, acc, out)
     eng.verify_update_sample(2, tok, par, pos, mask, lg, 1e-30, u, ur, acc, out)     # tiny but invertible
+    assert eng.sync() == 0
+    # raw calls past the binding: buffers off their element alignment are refused before anything is queued
+    from hybrid_draft_tree_gb300 import graft as gb
+    L = g_.load()
+    p = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + off)
+    args = [p(tok), p(par), p(pos), p(mask), p(lg), ctypes.c_int64(100), p(acc), p(out), ctypes.c_void_p(0)]
+    assert L.graft_verify_update(eng.h, 2, *args) == gb.GRAFT_OK
+    for i, off in ((0, 2), (2, 2), (3, 4), (4, 1), (6, 2), (7, 2)):
+        bad = list(args)
+        bad[i] = p([tok, par, pos, mask, lg, None, acc, out][i], off)
+        assert L.graft_verify_update(eng.h, 2, *bad) == gb.GRAFT_EINVAL, (i, off)
     assert eng.sync() == 0
     for mode, kw in ((0, dict(topk=4)), (1, dict(ablation=1)), (2, dict(ablation=2)), (0, dict(ablation=3)),
                      (0, dict(ablation=2, fixed_draft=61)), (0, dict(tpl_width=65)), (0, dict(tpl_depth=17)),
