@@ -1106,12 +1106,14 @@ def test_invalid_arguments_are_rejected():
             g_.Graft(g_.graft_default_config(100, 2, mode, W.BF16, **kw))
 
 
-@pytest.mark.parametrize("B", [4, 1])
-def test_step_replays_from_a_cuda_graph(B):
-    """assemble + verify_update are captured into a CUDA graph and replayed:
-    the same trees, acceptance and matrix as the same calls made directly on
-    an identical handle.  Four requests take the two-pass scan (with the
-    dependent launch of pass 2), one request the cluster-per-row verify."""
+@pytest.mark.parametrize("B,sample", [(4, False), (1, False), (4, True), (1, True)])
+def test_step_replays_from_a_cuda_graph(B, sample):
+    """assemble + verify_update (or verify_update_sample, on fixed uniforms)
+    are captured into a CUDA graph and replayed: the same trees, acceptance
+    and matrix as the same calls made directly on an identical handle.  Four
+    requests take the two-pass scan (with the dependent launch of pass 2, and
+    the walk's clusters as its dependent), one request the cluster-per-row
+    verify."""
     from workloads.device_loop import DeviceLoop
     w = W.WORKLOADS[2].scaled(V=40000, B=B)
     eager = engine_for(w)
@@ -1129,10 +1131,17 @@ def test_step_replays_from_a_cuda_graph(B):
         out = torch.empty_like(loop.out_tokens)
         par = loop.d_par
 
+        u = torch.linspace(0.05, 0.95, w.B * w.S, device="cuda").view(w.B, w.S)
+        ur = torch.linspace(0.1, 0.9, w.B, device="cuda")
+
         def step():
             eng.assemble(w.B, loop.root, loop.d_tok, par, loop.d_aux, *bufs, stream=torch.cuda.current_stream())
-            eng.verify_update(w.B, bufs[0], bufs[1], bufs[2], bufs[3], loop.logits, acc, out,
-                              stream=torch.cuda.current_stream())
+            if sample:
+                eng.verify_update_sample(w.B, bufs[0], bufs[1], bufs[2], bufs[3], loop.logits, 1.0, u, ur, acc, out,
+                                         stream=torch.cuda.current_stream())
+            else:
+                eng.verify_update(w.B, bufs[0], bufs[1], bufs[2], bufs[3], loop.logits, acc, out,
+                                  stream=torch.cuda.current_stream())
         if name == "graph":
             with torch.cuda.stream(side):
                 step()                                 # first call on the stream: nothing new is set up in capture
