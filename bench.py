@@ -249,7 +249,8 @@ def workload_config(w, ws):
     """The `config` object of both arms' JSON lines: what the workload is."""
     return {"workload": w.name, "vocab": w.V, "batch": w.B, "slots_per_request": w.S, "draft_sigma": w.draft_sigma,
             "mode": ["checkpoint", "static", "tail"][w.mode], "logits_bytes_per_step": w.logits_bytes_per_step(),
-            "parallelism": "replicas" if ws > 1 else "single"}
+            "parallelism": "replicas" if ws > 1 else "single",
+            "l2_between_steps": "flushed before each graft call (256 MB written, then read back)"}
 
 
 def max_over_ranks(x: float, device=None) -> float:
