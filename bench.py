@@ -397,9 +397,12 @@ def run_graft(args, ws, rank, local):
     from hybrid_draft_tree_gb300 import _build
     from workloads.device_loop import DeviceLoop
 
-    _build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if rank == 0:
+        _build.build()  # a no-op when the library is current; one rank only, so no two compile the same objects
+    if ws > 1:
+        torch.distributed.barrier()
     w = W.WORKLOADS[args.workload]
     if args.draft_sigma is not None:
         w = w.scaled(draft_sigma=args.draft_sigma)
