@@ -51,6 +51,15 @@ __device__ __forceinline__ void cluster_started_arrive() {
 }
 __device__ __forceinline__ void cluster_started_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
+// 16 bytes of shared memory at shared-space address a.  The stage reaches the
+// statistics as a generic pointer (it may be null in the kernels), so its
+// loads are made explicit shared-memory loads.
+__device__ __forceinline__ uint4 lds16(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
 // (m, s) <- online update with element x.
 __device__ __forceinline__ void online_add(float& m, float& s, float x, float k2) {
   if (x > m) {
@@ -141,45 +150,47 @@ __device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* 
     // the chunk is in shared memory, so it is read twice: its maximum first
     // (four independent maxima), then its exponentials into eight independent
     // partial sums, with no rescaling between them
-    const uint4* sp = reinterpret_cast<const uint4*>(stage + (size_t)(v0 - lo) * ES);
+    const uint32_t sp = bulk::smem_u32(stage) + (uint32_t)(v0 - lo) * ES;  // the chunk, 16-byte aligned
     const int nvec = (v1 - v0) / EPL;
     float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
     int i = 0;
     for (; i + 4 <= nvec; i += 4) {
       Vec16<DT> x0, x1, x2, x3;
-      x0.r = sp[i];
-      x1.r = sp[i + 1];
-      x2.r = sp[i + 2];
-      x3.r = sp[i + 3];
-      m0 = fmaxf(m0, x0.vmax());
-      m1 = fmaxf(m1, x1.vmax());
-      m2 = fmaxf(m2, x2.vmax());
-      m3 = fmaxf(m3, x3.vmax());
+      x0.r = lds16(sp + 16u * i);
+      x1.r = lds16(sp + 16u * (i + 1));
+      x2.r = lds16(sp + 16u * (i + 2));
+      x3.r = lds16(sp + 16u * (i + 3));
+      m0 = fmaxf(m0, x0.vmax_drop_nan());
+      m1 = fmaxf(m1, x1.vmax_drop_nan());
+      m2 = fmaxf(m2, x2.vmax_drop_nan());
+      m3 = fmaxf(m3, x3.vmax_drop_nan());
     }
     for (; i < nvec; ++i) {
       Vec16<DT> x0;
-      x0.r = sp[i];
-      m0 = fmaxf(m0, x0.vmax());
+      x0.r = lds16(sp + 16u * i);
+      m0 = fmaxf(m0, x0.vmax_drop_nan());
     }
     for (int v = v0 + nvec * EPL; v < v1; ++v) m1 = fmaxf(m1, stage_elem<DT>(stage, v - lo));
     m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
     if (m != -INFINITY) {
+      // exp2(x * k2 - m * k2): one fused multiply-add per element
+      const float mk = m * k2;
       float qa[4] = {0.f, 0.f, 0.f, 0.f}, qb[4] = {0.f, 0.f, 0.f, 0.f};
       for (i = 0; i + 2 <= nvec; i += 2) {
         Vec16<DT> x0, x1;
-        x0.r = sp[i];
-        x1.r = sp[i + 1];
+        x0.r = lds16(sp + 16u * i);
+        x1.r = lds16(sp + 16u * (i + 1));
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
-          qa[e & 3] += exp2f((x0.elem(e) - m) * k2);
-          qb[e & 3] += exp2f((x1.elem(e) - m) * k2);
+          qa[e & 3] += exp2f(fmaf(x0.elem(e), k2, -mk));
+          qb[e & 3] += exp2f(fmaf(x1.elem(e), k2, -mk));
         }
       }
       if (i < nvec) {
         Vec16<DT> x0;
-        x0.r = sp[i];
+        x0.r = lds16(sp + 16u * i);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) qa[e & 3] += exp2f((x0.elem(e) - m) * k2);
+        for (int e = 0; e < EPL; ++e) qa[e & 3] += exp2f(fmaf(x0.elem(e), k2, -mk));
       }
       for (int v = v0 + nvec * EPL; v < v1; ++v) qb[v & 3] += exp2f((stage_elem<DT>(stage, v - lo) - m) * k2);
       s = ((qa[0] + qa[1]) + (qa[2] + qa[3])) + ((qb[0] + qb[1]) + (qb[2] + qb[3]));

@@ -95,6 +95,18 @@ template <> struct Vec16<GRAFT_BF16> {
     const uint32_t u = *reinterpret_cast<const uint32_t*>(&m);
     return max_nan(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
   }
+  // the largest element, NaN left out (a NaN element is never the result
+  // unless all eight are NaN): for callers that fold the result with fmaxf
+  // anyway, one instruction per pair instead of the NaN-propagating form
+  __device__ __forceinline__ float vmax_drop_nan() const {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
+    const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(&m);
+    return fmaxf(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  }
   // the largest element (NaN-propagating) and the second largest of the eight
   // (the largest of the others; equal to m1 when the maximum repeats):
   // pairwise max/min of the even and of the odd halves, then their merge
@@ -135,6 +147,9 @@ template <> struct Vec16<GRAFT_F32> {
   __device__ __forceinline__ float vmax() const {
     return max_nan(max_nan(__uint_as_float(r.x), __uint_as_float(r.y)),
                    max_nan(__uint_as_float(r.z), __uint_as_float(r.w)));
+  }
+  __device__ __forceinline__ float vmax_drop_nan() const {
+    return fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)), fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
   }
   __device__ __forceinline__ float elem(int e) const {
     return __uint_as_float(e == 0 ? r.x : e == 1 ? r.y : e == 2 ? r.z : r.w);
