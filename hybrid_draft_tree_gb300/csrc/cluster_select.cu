@@ -7,16 +7,16 @@
 // maxima, a candidate reload and the request ticket.  Here one cluster of CL
 // CTAs takes one row: each CTA stages its range of the row in shared memory
 // (the row's only read: bulk copies into shared memory), then every thread
-// takes the maximum of its elements, and the CTA takes T, the 8th
-// largest of its threads' maxima.  Eight distinct elements of the range reach
-// T (each is its thread's maximum), so every element of the range's top-8 is
-// >= T; the CTA lists its elements >= T from shared memory and sorts them
-// into its exact top-8 (value desc, id asc).  The row's top-8 is among the 8
+// takes the maximum of its elements, each warp the maximum of its threads',
+// and the CTA takes T, the smallest of its 8 warps' maxima.  Eight distinct
+// elements of the range reach T (each is its warp's maximum), so every
+// element of the range's top-8 is >= T; the CTA lists its elements >= T from
+// shared memory and sorts them into its exact top-8 (value desc, id asc).  The row's top-8 is among the 8
 // CTAs' top-8s: CTA 0 of the cluster merges the 64 keys through distributed
 // shared memory, writes the row's share of the update and, for the row
 // completing a request, runs its acceptance from the request's tree arrays,
 // which it staged in shared memory at the start.  A range with fewer than 8
-// finite thread maxima, or with more than RCAP elements >= T (heavy ties),
+// finite warp maxima, or with more than RCAP elements >= T (heavy ties),
 // takes its exact top-8 by repeated maxima over the staged range instead.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -41,34 +41,19 @@ constexpr int RCAP = 128;   // elements >= T one CTA may list before its exact p
 constexpr int UNR = 8;      // 16-byte loads in flight per thread while staging (unaligned rows)
 constexpr uint32_t BULK = 32768;  // bytes per bulk copy
 
-// The 8 largest of the 32 lanes' x (ordered ints, with multiplicity; INT_MIN
-// past the end): lane r < 8 returns the r-th.
-__device__ __forceinline__ int32_t top8_of_lanes(int32_t x, int lane) {
-  int32_t out = INT_MIN;
+// Lanes 16g .. 16g + 15 hold two descending runs of 8 keys (lanes 16g ..
+// 16g + 7 and 16g + 8 .. 16g + 15); lanes 16g .. 16g + 7 get the 8 largest of
+// the 16, descending.  The second run reversed makes the 16 a bitonic
+// sequence, which four compare-exchange stages sort.
+__device__ __forceinline__ u64 top8_of_two_runs(u64 key, int lane) {
+  const u64 r = __shfl_xor_sync(FULL, key, 7);
+  if (lane & 8) key = r;
 #pragma unroll
-  for (int r = 0; r < K; ++r) {
-    const int32_t m = __reduce_max_sync(FULL, x);
-    const int owner = __ffs(__ballot_sync(FULL, x == m)) - 1;
-    if (lane == owner) x = INT_MIN;
-    if (lane == r) out = m;
+  for (int j = 8; j > 0; j >>= 1) {
+    const u64 o = __shfl_xor_sync(FULL, key, j);
+    key = (lane & j) == 0 ? (key > o ? key : o) : (key < o ? key : o);
   }
-  return out;
-}
-
-// The same over 64 values, two per lane (x0, x1).
-__device__ __forceinline__ int32_t top8_of_pairs(int32_t x0, int32_t x1, int lane) {
-  int32_t out = INT_MIN;
-#pragma unroll
-  for (int r = 0; r < K; ++r) {
-    const int32_t m = __reduce_max_sync(FULL, max(x0, x1));
-    const int owner = __ffs(__ballot_sync(FULL, x0 == m || x1 == m)) - 1;
-    if (lane == owner) {
-      if (x0 == m) x0 = INT_MIN;
-      else x1 = INT_MIN;
-    }
-    if (lane == r) out = m;
-  }
-  return out;
+  return key;
 }
 
 template <int DT>
@@ -78,11 +63,11 @@ __global__ void __launch_bounds__(RT, 8) k_cluster_select(VerifyArgs a, int32_t*
   __shared__ uint64_t smask[MAX_S];  // CTA 0: the tree arrays of this row's request
   __shared__ int32_t spos[MAX_S];
   __shared__ int8_t spar[MAX_S];
-  __shared__ int32_t wtop[RW][K];    // each warp's 8 largest thread maxima
+  __shared__ int32_t wmax[RW];       // each warp's largest thread maximum
   __shared__ u64 s_list[RCAP];       // this CTA's elements >= T
   __shared__ u64 s_top[K];           // this CTA's top-8 keys (read by CTA 0)
   __shared__ u64 s_wbest[RW];
-  __shared__ int s_nc, s_T;
+  __shared__ int s_nc;
   __shared__ unsigned long long s_bar;  // the staging copies' barrier
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   constexpr int EPL = Vec16<DT>::EPL;
@@ -183,19 +168,17 @@ __global__ void __launch_bounds__(RT, 8) k_cluster_select(VerifyArgs a, int32_t*
   }
   if (nan) atomicOr(a.err, GRAFT_ERR_NAN);
 
-  // 2. T = the 8th largest of this CTA's thread maxima
+  // 2. T = the smallest of this CTA's 8 warp maxima
   {
-    const int32_t w8 = top8_of_lanes(ord_int(tm), lane);
-    if (lane < K) wtop[warp][lane] = w8;
+    const int32_t wm = __reduce_max_sync(FULL, ord_int(tm));
+    if (lane == 0) wmax[warp] = wm;
   }
   __syncthreads();
-  if (warp == 0) {
-    const int32_t c8 = top8_of_pairs(wtop[lane >> 3][lane & 7], wtop[4 + (lane >> 3)][lane & 7], lane);
-    if (lane == K - 1) s_T = c8;
-  }
-  __syncthreads();
-  const float T = from_ord_int(s_T);
-  bool exact = !(s_T != INT_MIN && T > -INFINITY);  // fewer than 8 finite thread maxima
+  int32_t Ti = INT_MAX;
+#pragma unroll
+  for (int w = 0; w < RW; ++w) Ti = min(Ti, wmax[w]);
+  const float T = from_ord_int(Ti);
+  bool exact = !(Ti != INT_MIN && T > -INFINITY);  // a warp without a finite maximum
 
   // 3. this CTA's elements >= T, from shared memory, then its top-8
   if (!exact) {
@@ -257,12 +240,17 @@ __global__ void __launch_bounds__(RT, 8) k_cluster_select(VerifyArgs a, int32_t*
   // 4. CTA 0 merges the 8 CTAs' top-8s (lane l reads keys l and l + 32 of the 64)
   u64 top = 0ull;
   if (rank == 0 && warp == 0) {
-    const u64 k0 = *cluster.map_shared_rank(&s_top[lane & 7], lane >> 3);
-    const u64 k1 = *cluster.map_shared_rank(&s_top[lane & 7], 4 + (lane >> 3));
-    const u64 hi0 = bitonic32_desc(k0, lane), hi1 = bitonic32_desc(k1, lane);
-    // the top-8 of two descending lists of 32: lanes 0..7 of the first, 8..15 take the second's 0..7
-    const u64 y = __shfl_sync(FULL, hi1, lane & 7);
-    top = bitonic32_desc(lane < K ? hi0 : (lane < 2 * K ? y : 0ull), lane);
+    // a tournament of bitonic merges over the 8 descending lists: CTAs
+    // (0, 1), (2, 3), (4, 5), (6, 7), then the pairs' winners, then the halves'
+    u64 k0 = *cluster.map_shared_rank(&s_top[lane & 7], lane >> 3);
+    u64 k1 = *cluster.map_shared_rank(&s_top[lane & 7], 4 + (lane >> 3));
+    k0 = top8_of_two_runs(k0, lane);  // lanes 0..7: CTAs 0, 1; lanes 16..23: CTAs 2, 3
+    k1 = top8_of_two_runs(k1, lane);  // the same for CTAs 4 .. 7
+    const int down = (lane & 7) | ((lane & 8) << 1);  // lanes 8..15 take lanes 16..23
+    k0 = top8_of_two_runs(__shfl_sync(FULL, k0, down), lane);  // lanes 0..7: CTAs 0 .. 3
+    k1 = top8_of_two_runs(__shfl_sync(FULL, k1, down), lane);  // lanes 0..7: CTAs 4 .. 7
+    const u64 k1d = __shfl_sync(FULL, k1, lane & 7);
+    top = top8_of_two_runs((lane & 8) ? k1d : k0, lane);        // lanes 0..7: the row's top-8
   }
   cluster.sync();  // CTA 0 has read the keys: the other CTAs may leave
   if (rank != 0 || warp != 0) return;
