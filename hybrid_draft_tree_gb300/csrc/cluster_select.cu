@@ -203,7 +203,13 @@ __global__ void __launch_bounds__(RT, 8) k_cluster_select(VerifyArgs a, int32_t*
     __syncthreads();
     exact = s_nc > RCAP;  // heavy ties: the list overflowed
     if (!exact && warp == 0) {
-      const u64 top = warp_merge(0ull, s_list, s_nc, lane);
+      // up to 32 candidates: one bitonic sort of them (of 16 when they fit);
+      // more: chunks merged into a running top-8
+      const int nc = s_nc;
+      u64 top;
+      if (nc <= 16) top = bitonic_desc<16>(lane < nc ? s_list[lane] : 0ull, lane);
+      else if (nc <= 32) top = bitonic_desc<32>(lane < nc ? s_list[lane] : 0ull, lane);
+      else top = warp_merge(0ull, s_list, nc, lane);
       if (lane < K) s_top[lane] = top;
     }
   }
