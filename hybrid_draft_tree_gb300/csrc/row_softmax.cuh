@@ -272,12 +272,14 @@ __device__ void cluster_row_stats(const cg::cluster_group& cluster, const char* 
       st.em[t] = mr;
       st.es[t] = sr;
     }
+    // (the CL = 8 pairs sit in lanes 0..7: three butterfly steps fold them)
+    static_assert(CL == 8, "the fold below covers 8 lanes");
     float M = mr;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+    for (int o = CL / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
     float W = (mr == -INFINITY) ? 0.f : sr * exp2f((mr - M) * k2);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(FULL, W, o);
+    for (int o = CL / 2; o > 0; o >>= 1) W += __shfl_xor_sync(FULL, W, o);
     if (t == 0) { st.M = M; st.W = W; }
   }
   __syncthreads();

@@ -147,9 +147,9 @@ __global__ __launch_bounds__(PT, 4) void k_sample(VerifyArgs a, int staged) {
         }
         wr = fmaxf(wr, 0.f);
       }
-      float ci = wr;  // inclusive scan over the ranks
+      float ci = wr;  // inclusive scan over the ranks (lanes 0 .. CL - 1)
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
+      for (int o = 1; o < CL; o <<= 1) {
         const float y = __shfl_up_sync(FULL, ci, o);
         if (lane >= o) ci += y;
       }
