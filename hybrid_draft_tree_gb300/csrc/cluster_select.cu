@@ -7,16 +7,16 @@
 // maxima, a candidate reload and the request ticket.  Here one cluster of CL
 // CTAs takes one row: each CTA stages its range of the row in shared memory
 // (the row's only read: bulk copies into shared memory), then every thread
-// takes the maximum of its elements, each warp the maximum of its threads',
-// and the CTA takes T, the smallest of its 8 warps' maxima.  Eight distinct
-// elements of the range reach T (each is its warp's maximum), so every
-// element of the range's top-8 is >= T; the CTA lists its elements >= T from
+// takes the maximum of its elements, each warp the two largest of its
+// threads' maxima, and the CTA takes T, the 8th largest of those 16.  Eight
+// distinct elements of the range reach T (each is its thread's maximum), so
+// every element of the range's top-8 is >= T; the CTA lists its elements >= T from
 // shared memory and sorts them into its exact top-8 (value desc, id asc).  The row's top-8 is among the 8
 // CTAs' top-8s: CTA 0 of the cluster merges the 64 keys through distributed
 // shared memory, writes the row's share of the update and, for the row
 // completing a request, runs its acceptance from the request's tree arrays,
 // which it staged in shared memory at the start.  A range with fewer than 8
-// finite warp maxima, or with more than RCAP elements >= T (heavy ties),
+// finite values among the 16, or with more than RCAP elements >= T (heavy ties),
 // takes its exact top-8 by repeated maxima over the staged range instead.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -63,11 +63,11 @@ __global__ void __launch_bounds__(RT, 8) k_cluster_select(VerifyArgs a, int32_t*
   __shared__ uint64_t smask[MAX_S];  // CTA 0: the tree arrays of this row's request
   __shared__ int32_t spos[MAX_S];
   __shared__ int8_t spar[MAX_S];
-  __shared__ int32_t wmax[RW];       // each warp's largest thread maximum
+  __shared__ int32_t wmax[2 * RW];   // each warp's two largest thread maxima
   __shared__ u64 s_list[RCAP];       // this CTA's elements >= T
   __shared__ u64 s_top[K];           // this CTA's top-8 keys (read by CTA 0)
   __shared__ u64 s_wbest[RW];
-  __shared__ int s_nc;
+  __shared__ int s_nc, s_T;
   __shared__ unsigned long long s_bar;  // the staging copies' barrier
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   constexpr int EPL = Vec16<DT>::EPL;
@@ -168,17 +168,33 @@ __global__ void __launch_bounds__(RT, 8) k_cluster_select(VerifyArgs a, int32_t*
   }
   if (nan) atomicOr(a.err, GRAFT_ERR_NAN);
 
-  // 2. T = the smallest of this CTA's 8 warp maxima
+  // 2. T = the 8th largest of the warps' two largest thread maxima (16
+  //    values from 16 threads: 16 distinct elements)
   {
-    const int32_t wm = __reduce_max_sync(FULL, ord_int(tm));
-    if (lane == 0) wmax[warp] = wm;
+    const int32_t k1 = ord_int(tm);
+    const int32_t m1 = __reduce_max_sync(FULL, k1);
+    const int lead = __ffs(__ballot_sync(FULL, k1 == m1)) - 1;
+    const int32_t m2 = __reduce_max_sync(FULL, lane == lead ? INT_MIN : k1);
+    if (lane == 0) { wmax[2 * warp] = m1; wmax[2 * warp + 1] = m2; }
   }
   __syncthreads();
-  int32_t Ti = INT_MAX;
+  if (warp == 0) {
+    // lane l < 16 counts the values above its own (ties by position); the
+    // lane with 7 above holds the 8th largest
+    const int32_t v = lane < 2 * RW ? wmax[lane] : INT_MIN;
+    int above = 0;
 #pragma unroll
-  for (int w = 0; w < RW; ++w) Ti = min(Ti, wmax[w]);
+    for (int i = 0; i < 2 * RW; ++i) {
+      const int32_t x = wmax[i];
+      above += (x > v) || (x == v && i < lane);
+    }
+    const unsigned at8 = __ballot_sync(FULL, lane < 2 * RW && above == K - 1);
+    if (lane == __ffs(at8) - 1) s_T = v;
+  }
+  __syncthreads();
+  const int32_t Ti = s_T;
   const float T = from_ord_int(Ti);
-  bool exact = !(Ti != INT_MIN && T > -INFINITY);  // a warp without a finite maximum
+  bool exact = !(Ti != INT_MIN && T > -INFINITY);  // fewer than 8 finite values
 
   // 3. this CTA's elements >= T, from shared memory, then its top-8
   if (!exact) {
