@@ -135,16 +135,45 @@ __global__ void __launch_bounds__(RT, 8) k_cluster_select(VerifyArgs a, int32_t*
     }
     __syncthreads();
     if (bytes > 0) (void)mbar_test_wait(&s_bar, 0);  // each thread observes the completed phase itself
-    for (int q = t; q < nv; q += RT) {
-      Vec16<DT> x;
-      x.r = sv[q];
-      const float m = x.vmax();
-      if (m != m) {
+    if (DT == GRAFT_BF16) {
+      // a NaN-propagating running maximum of bf16 pairs (four pair
+      // operations per vector); a NaN in it sends the thread through its
+      // vectors again with NaN left out
+      const __nv_bfloat162 ninf = __float2bfloat162_rn(-INFINITY);
+      __nv_bfloat162 acc = ninf;
+      for (int q = t; q < nv; q += RT) {
+        const uint4 r = sv[q];
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
+        const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
+        acc = __hmax2_nan(acc, __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d)));
+      }
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(&acc);
+      const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xFFFF0000u);
+      if (lo != lo || hi != hi) {
         nan = true;
+        for (int q = t; q < nv; q += RT) {
+          Vec16<DT> x;
+          x.r = sv[q];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) tm = fmaxf(tm, x.elem(e));  // fmaxf drops NaN
+          for (int e = 0; e < EPL; ++e) tm = fmaxf(tm, x.elem(e));  // fmaxf drops NaN
+        }
       } else {
-        tm = fmaxf(tm, m);
+        tm = fmaxf(lo, hi);
+      }
+    } else {
+      for (int q = t; q < nv; q += RT) {
+        Vec16<DT> x;
+        x.r = sv[q];
+        const float m = x.vmax();
+        if (m != m) {
+          nan = true;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) tm = fmaxf(tm, x.elem(e));  // fmaxf drops NaN
+        } else {
+          tm = fmaxf(tm, m);
+        }
       }
     }
   }
