@@ -32,71 +32,115 @@ __device__ __forceinline__ uint4 neg_inf_vec(int dt) {
 
 // This CTA's share: units [u0, u1) of the rows' NU = rows * upr units, which
 // fall in compacted rows k0 .. klast (rowlist[k - k0] = the row behind k).
+// NU <= 4096 rows x 1024 units (the warm-up's list: 4096 rows at most) fits
+// in 32 bits.
 struct Slice {
-  int64_t u0, u1, k0, klast;
-  bool live;  // false: nothing to stream here (the whole CTA agrees)
+  int u0, u1, k0, klast;
+  int live;  // 0: nothing to stream here (the whole CTA agrees)
 };
 
-// Compacts the rows and fills `rowlist` for this CTA's slice (ends with a
-// CTA barrier).  LIST = false: the valid tree rows.  LIST = true: the first
-// min(*count, cap) entries of `list`.  warpsum: UW ints of shared memory.
-template <bool LIST>
-__device__ __forceinline__ Slice compact_rows(const VerifyArgs& a, const int32_t* list, const int32_t* count, int cap,
-                                              int* rowlist, int* warpsum) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rows = LIST ? 0 : a.batch * a.S;
-  const int V = a.g.V;
-  const int64_t upr = a.upr;
-  const int per = (rows + UT - 1) / UT;
-  const int r0 = min(tid * per, rows), r1 = min(r0 + per, rows);
-  int cnt = 0;
-  for (int r = r0; r < r1; ++r) {
-    const int32_t t = a.tree_tok[r];
-    cnt += (t >= 0 && t < V);
-    if (t >= V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
-  }
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(FULL, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warpsum[warp] = incl;
-  __syncthreads();
-  int wbase = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < UW; ++w) {
-    const int x = warpsum[w];
-    wbase += (w < warp) ? x : 0;
-    total += x;
-  }
-  if (LIST) total = min(__ldcg(count), cap);
-  Slice s{0, 0, 0, -1, false};
-  const int64_t NU = (int64_t)total * upr;
-  const int Ge = (int)min((int64_t)gridDim.x, NU);
+constexpr int UCHUNKS = TWO_PASS_MAX_ROWS / UT;  // row chunks of UT, one row per thread each
+
+// Thread 0's part: this CTA's slice of `total` compacted rows (equal shares
+// of the units, the first NU % Ge CTAs one unit more).
+__device__ __forceinline__ Slice slice_of(int total, int upr, const VerifyArgs& a) {
+  Slice s{0, 0, 0, -1, 0};
+  const int NU = total * upr;
+  const int Ge = min((int)gridDim.x, NU);
   const int c = blockIdx.x;
   if (NU > 0 && c < Ge) {
-    s.u0 = (int64_t)c * NU / Ge;
-    s.u1 = (int64_t)(c + 1) * NU / Ge;
+    const int q = NU / Ge, rem = NU - q * Ge;
+    s.u0 = c * q + min(c, rem);
+    s.u1 = s.u0 + q + (c < rem ? 1 : 0);
     s.k0 = s.u0 / upr;
     s.klast = (s.u1 - 1) / upr;
-    s.live = true;
+    s.live = 1;
     if (s.klast - s.k0 + 1 > UMAXROWS) {  // the host keeps rows <= (UMAXROWS - 2) * grid
-      if (tid == 0) atomicOr(a.err, GRAFT_ERR_TREE);
-      s.live = false;
+      atomicOr(a.err, GRAFT_ERR_TREE);
+      s.live = 0;
     }
   }
+  return s;
+}
+
+// Compacts the rows and fills `rowlist` for this CTA's slice (ends with a
+// CTA barrier).  LIST = false: the valid tree rows, in row order: thread t
+// tests rows t, t + UT, ... (all its loads issued at once), each warp counts
+// its chunk's valid rows with a ballot, warp 0 scans the counts and thread 0
+// takes the slice; a valid row's compacted index is its chunk-warp's prefix
+// plus the valid lanes below it.  LIST = true: the first min(*count, cap)
+// entries of `list`.  wpre: UCHUNKS * UW ints of shared memory.
+template <bool LIST>
+__device__ __forceinline__ Slice compact_rows(const VerifyArgs& a, const int32_t* list, const int32_t* count, int cap,
+                                              int* rowlist, int* wpre, Slice* s_slice) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int upr = a.upr;
+  if (LIST) {
+    if (tid == 0) *s_slice = slice_of(min(__ldcg(count), cap), upr, a);
+    __syncthreads();
+    const Slice s = *s_slice;
+    if (s.live)
+      for (int k = s.k0 + tid; k <= s.klast; k += UT) rowlist[k - s.k0] = __ldcg(list + k);
+    __syncthreads();
+    return s;
+  }
+  const int rows = a.batch * a.S;  // <= TWO_PASS_MAX_ROWS on this path (the host checks)
+  if (rows > TWO_PASS_MAX_ROWS) {
+    if (tid == 0) atomicOr(a.err, GRAFT_ERR_TREE);
+    return Slice{0, 0, 0, -1, 0};
+  }
+  const int V = a.g.V;
+  const int nchunk = (rows + UT - 1) / UT;
+  int32_t tok[UCHUNKS];
+#pragma unroll
+  for (int i = 0; i < UCHUNKS; ++i) tok[i] = (i < nchunk && i * UT + tid < rows) ? a.tree_tok[i * UT + tid] : -1;
+  unsigned vm = 0;  // bit i: row i * UT + tid is valid
+#pragma unroll
+  for (int i = 0; i < UCHUNKS; ++i) {
+    if (i < nchunk) {
+      const bool ok = tok[i] >= 0 && tok[i] < V;
+      if (tok[i] >= V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
+      const unsigned b = __ballot_sync(FULL, ok);
+      if (lane == 0) wpre[i * UW + warp] = __popc(b);
+      vm |= (ok ? 1u : 0u) << i;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive prefix of the nchunk * UW counts, 4 consecutive per lane
+    const int n = nchunk * UW;
+    int c4[4], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      c4[q] = (lane * 4 + q < n) ? wpre[lane * 4 + q] : 0;
+      sum += c4[q];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (lane * 4 + q < n) wpre[lane * 4 + q] = run;
+      run += c4[q];
+    }
+    const int total = __shfl_sync(FULL, incl, 31);
+    if (lane == 0) *s_slice = slice_of(total, upr, a);
+  }
+  __syncthreads();
+  const Slice s = *s_slice;
   if (s.live) {
-    if (LIST) {
-      for (int64_t k = s.k0 + tid; k <= s.klast; k += UT) rowlist[k - s.k0] = __ldcg(list + k);
-    } else {
-      int64_t vidx = wbase + incl - cnt;
-      for (int r = r0; r < r1; ++r) {
-        const int32_t t = a.tree_tok[r];
-        if (t >= 0 && t < V) {
-          if (vidx >= s.k0 && vidx <= s.klast) rowlist[vidx - s.k0] = r;
-          ++vidx;
-        }
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < UCHUNKS; ++i) {
+      if (i < nchunk) {
+        const bool ok = (vm >> i) & 1u;
+        const unsigned b = __ballot_sync(FULL, ok);
+        const int vidx = wpre[i * UW + warp] + __popc(b & below);
+        if (ok && vidx >= s.k0 && vidx <= s.klast) rowlist[vidx - s.k0] = i * UT + tid;
       }
     }
   }
@@ -121,16 +165,19 @@ __device__ __forceinline__ void stream_units(const VerifyArgs& a, const Slice& s
   constexpr int ES = DT == GRAFT_BF16 ? 2 : 4;
   const ScanGeom& g = a.g;
   const int64_t nslot = g.nslot;
-  const int64_t upr = a.upr;
   const char* base = reinterpret_cast<const char*>(a.logits);
   const size_t rstride = (size_t)g.stride * ES;
-  const int64_t nu = sl.u1 - sl.u0;
+  const int nu = sl.u1 - sl.u0;
   const int upr32 = a.upr;  // <= TWO_PASS_MAX_UNITS
   // the group's first unit as (compacted row k, unit j of that row), walked
-  // forward from one division
-  int64_t k = (sl.u0 + (int64_t)warp * UNV) / upr;
-  int j = (int)(sl.u0 + (int64_t)warp * UNV - k * upr);
-  for (int64_t g0 = (int64_t)warp * UNV; g0 < nu; g0 += (int64_t)UW * UNV) {
+  // forward from the slice's first unit
+  int64_t k = sl.k0;
+  int j = sl.u0 - sl.k0 * upr32 + warp * UNV;
+  while (j >= upr32) {
+    j -= upr32;
+    ++k;
+  }
+  for (int g0 = warp * UNV; g0 < nu; g0 += UW * UNV) {
     const bool one_row = j + UNV <= upr32 && g0 + UNV <= nu;
     const int row0 = rowlist[k - sl.k0];
     // unit kk of the group: its compacted row kr, its row, its index jj in the row
@@ -138,7 +185,7 @@ __device__ __forceinline__ void stream_units(const VerifyArgs& a, const Slice& s
       if (one_row) {
         kr = k; row = row0; jj = j + kk;
       } else {
-        kr = min(k + (j + kk) / upr32, sl.klast);  // units past the slice end are masked out
+        kr = min(k + (j + kk) / upr32, (int64_t)sl.klast);  // units past the slice end are masked out
         jj = (j + kk) % upr32;
         row = rowlist[kr - sl.k0];
       }
@@ -228,11 +275,12 @@ __device__ __forceinline__ void stream_units(const VerifyArgs& a, const Slice& s
 // their second largest element and the position of their maximum.
 template <int DT, bool LIST, bool TOP2>
 __global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a, const int32_t* list, const int32_t* count, int cap) {
-  __shared__ int warpsum[UW];
+  __shared__ int wpre[UCHUNKS * UW];
   __shared__ int rowlist[UMAXROWS];
+  __shared__ Slice s_slice;
   grid_dependents_launch();  // pass 2 may be scheduled as SMs free up; it waits for this grid's results
   if (LIST) grid_dependency_wait();  // the warm-up's list comes from the kernel ahead
-  const Slice sl = compact_rows<LIST>(a, list, count, cap, rowlist, warpsum);
+  const Slice sl = compact_rows<LIST>(a, list, count, cap, rowlist, wpre, &s_slice);
   if (!sl.live) return;
   stream_units<DT, LIST, TOP2>(a, sl, rowlist, threadIdx.x >> 5, threadIdx.x & 31);
 }
