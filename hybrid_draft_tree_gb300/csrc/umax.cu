@@ -91,19 +91,22 @@ __device__ __forceinline__ Slice compact_rows(const VerifyArgs& a, const int32_t
   }
   const int V = a.g.V;
   const int nchunk = (rows + UT - 1) / UT;
+  // the loops stop at nchunk (uniform): the loads still issue back to back
   int32_t tok[UCHUNKS];
 #pragma unroll
-  for (int i = 0; i < UCHUNKS; ++i) tok[i] = (i < nchunk && i * UT + tid < rows) ? a.tree_tok[i * UT + tid] : -1;
+  for (int i = 0; i < UCHUNKS; ++i) {
+    if (i >= nchunk) break;
+    tok[i] = i * UT + tid < rows ? a.tree_tok[i * UT + tid] : -1;
+  }
   unsigned vm = 0;  // bit i: row i * UT + tid is valid
 #pragma unroll
   for (int i = 0; i < UCHUNKS; ++i) {
-    if (i < nchunk) {
-      const bool ok = tok[i] >= 0 && tok[i] < V;
-      if (tok[i] >= V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
-      const unsigned b = __ballot_sync(FULL, ok);
-      if (lane == 0) wpre[i * UW + warp] = __popc(b);
-      vm |= (ok ? 1u : 0u) << i;
-    }
+    if (i >= nchunk) break;
+    const bool ok = tok[i] >= 0 && tok[i] < V;
+    if (tok[i] >= V && blockIdx.x == 0) atomicOr(a.err, GRAFT_ERR_TOKEN);  // such a slot is skipped
+    const unsigned b = __ballot_sync(FULL, ok);
+    if (lane == 0) wpre[i * UW + warp] = __popc(b);
+    vm |= (ok ? 1u : 0u) << i;
   }
   __syncthreads();
   if (warp == 0) {
@@ -134,14 +137,12 @@ __device__ __forceinline__ Slice compact_rows(const VerifyArgs& a, const int32_t
   const Slice s = *s_slice;
   if (s.live) {
     const unsigned below = (1u << lane) - 1u;
-#pragma unroll
-    for (int i = 0; i < UCHUNKS; ++i) {
-      if (i < nchunk) {
-        const bool ok = (vm >> i) & 1u;
-        const unsigned b = __ballot_sync(FULL, ok);
-        const int vidx = wpre[i * UW + warp] + __popc(b & below);
-        if (ok && vidx >= s.k0 && vidx <= s.klast) rowlist[vidx - s.k0] = i * UT + tid;
-      }
+#pragma unroll 1
+    for (int i = 0; i < nchunk; ++i) {
+      const bool ok = (vm >> i) & 1u;
+      const unsigned b = __ballot_sync(FULL, ok);
+      const int vidx = wpre[i * UW + warp] + __popc(b & below);
+      if (ok && vidx >= s.k0 && vidx <= s.klast) rowlist[vidx - s.k0] = i * UT + tid;
     }
   }
   __syncthreads();
