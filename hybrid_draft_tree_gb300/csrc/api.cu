@@ -685,6 +685,7 @@ int verify_impl(graft_handle* h, int32_t batch, const int32_t* d_tree_tok, const
   a.usec = h->usec;
   a.upos = h->upos;
   a.top2 = (c.scan_kernel == 4 && h->usec && h->upos) ? 1 : 0;
+  a.spec = c.mode == GRAFT_MODE_STATIC ? 1 : 0;  // static trees fill every slot
   a.wait_polls = h->wait_polls;  // measured: the records slow pass 1 by more than they save
   cudaError_t e;
   if (use_cluster) {

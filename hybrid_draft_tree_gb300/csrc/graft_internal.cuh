@@ -97,6 +97,8 @@ struct VerifyArgs {
   float* usec;                // two-pass scan with top2: [rows][ups] second largest element of every unit
   uint8_t* upos;              // two-pass scan with top2: [rows][ups] position of the unit's maximum in the unit
   int32_t top2;               // two-pass scan: 1 = units record (max, second, position), 0 = max only
+  int32_t spec;               // two-pass scan: 1 = every row is expected valid (static trees): pass 1 prefetches
+                              // its first groups into L2 before the rows' validity is known
   uint32_t wait_polls;        // TMA scan: polls before an mbarrier wait gives up (0 = the kernel's default)
   int32_t upr;                // two-pass scan: units per row
   int32_t ups;                // two-pass scan: row stride of umax (upr rounded up to a multiple of 4)
@@ -155,6 +157,8 @@ __device__ __forceinline__ uint64_t l2_keep_policy() {
 __device__ __forceinline__ void prefetch_keep(const void* ptr) {
   asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(ptr));
 }
+// A plain prefetch of the 128-byte line holding ptr into L2.
+__device__ __forceinline__ void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
 __device__ __forceinline__ int32_t ld_keep(const int32_t* ptr, uint64_t pol) {
   int32_t v;
   asm volatile("ld.global.L2::cache_hint.s32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol) : "memory");

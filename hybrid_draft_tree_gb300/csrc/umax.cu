@@ -70,7 +70,7 @@ __device__ __forceinline__ Slice slice_of(int total, int upr, const VerifyArgs& 
 // takes the slice; a valid row's compacted index is its chunk-warp's prefix
 // plus the valid lanes below it.  LIST = true: the first min(*count, cap)
 // entries of `list`.  wpre: UCHUNKS * UW ints of shared memory.
-template <bool LIST>
+template <bool LIST, int ES>
 __device__ __forceinline__ Slice compact_rows(const VerifyArgs& a, const int32_t* list, const int32_t* count, int cap,
                                               int* rowlist, int* wpre, Slice* s_slice) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -97,6 +97,32 @@ __device__ __forceinline__ Slice compact_rows(const VerifyArgs& a, const int32_t
   for (int i = 0; i < UCHUNKS; ++i) {
     if (i >= nchunk) break;
     tok[i] = i * UT + tid < rows ? a.tree_tok[i * UT + tid] : -1;
+  }
+  if (a.spec) {
+    // every row expected valid (the compacted index is the row): while the
+    // tree tokens are on their way, this warp's first group of the slice it
+    // would then get is prefetched into L2 (a wrong guess costs one group of
+    // reads per warp)
+    const int NU = rows * upr, Ge = min((int)gridDim.x, NU), c = blockIdx.x;
+    if (c < Ge) {
+      const int q = NU / Ge, rem = NU - q * Ge;
+      const int u0 = c * q + min(c, rem), u1 = u0 + q + (c < rem ? 1 : 0);
+      const int u = u0 + warp * UNV;
+      int row = u / upr, j = u - row * upr;
+      const char* base = reinterpret_cast<const char*>(a.logits);
+      const size_t rstride = (size_t)a.g.stride * ES;
+#pragma unroll
+      for (int kk = 0; kk < UNV; ++kk) {
+        if (u + kk < u1) {
+          const int64_t sl = (int64_t)j * 32 + lane;
+          if (sl < a.g.nslot) prefetch_l2(base + (size_t)row * rstride + (size_t)sl * 16);
+        }
+        if (++j == upr) {
+          j = 0;
+          ++row;
+        }
+      }
+    }
   }
   unsigned vm = 0;  // bit i: row i * UT + tid is valid
 #pragma unroll
@@ -281,7 +307,7 @@ __global__ void __launch_bounds__(UT, 4) k_umax(VerifyArgs a, const int32_t* lis
   __shared__ Slice s_slice;
   grid_dependents_launch();  // pass 2 may be scheduled as SMs free up; it waits for this grid's results
   if (LIST) grid_dependency_wait();  // the warm-up's list comes from the kernel ahead
-  const Slice sl = compact_rows<LIST>(a, list, count, cap, rowlist, wpre, &s_slice);
+  const Slice sl = compact_rows<LIST, DT == GRAFT_BF16 ? 2 : 4>(a, list, count, cap, rowlist, wpre, &s_slice);
   if (!sl.live) return;
   stream_units<DT, LIST, TOP2>(a, sl, rowlist, threadIdx.x >> 5, threadIdx.x & 31);
 }
