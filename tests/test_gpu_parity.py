@@ -838,12 +838,15 @@ def test_cluster_verify_unaligned_rows(dtype, pad, off):
     _verify_case(3001, dtype, 17, 3, _normal, stride_pad=pad, offset_elems=off, seed=pad + 7, scan_kernel=5)
 
 
+@pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("scan_kernel", [0, 1, 3, 5])
-def test_verify_request_without_valid_slots(scan_kernel):
+def test_verify_request_without_valid_slots(scan_kernel, mode):
     """A request whose slots are all pads (token -1) has no row to finish it:
     the verify still writes its acceptance (nothing accepted, nothing
     emitted; the oracle takes only trees with a valid root), and the other
-    requests match the oracle."""
+    requests match the oracle.  A static-mode handle expects every slot
+    filled (pass 1 prefetches by that guess): with pads the guess is wrong
+    and the results must not change."""
     g_ = G()
     rng = np.random.default_rng(31)
     V, B, S = 3000, 3, 61
@@ -857,7 +860,7 @@ def test_verify_request_without_valid_slots(scan_kernel):
         for i in range(1, n):
             par[i] = rng.integers(0, i)
         trees.append(_tree_from_parents(tok, par))
-    eng = g_.Graft(g_.graft_default_config(V, B, 0, W.F32, scan_kernel=scan_kernel))
+    eng = g_.Graft(g_.graft_default_config(V, B, mode, W.F32, scan_kernel=scan_kernel))
     tt = torch.from_numpy(np.stack([t.tok for t in trees])).cuda()
     tp = torch.from_numpy(np.stack([t.par for t in trees]).astype(np.int8)).cuda()
     tpos = torch.from_numpy(np.stack([t.pos for t in trees])).cuda()
